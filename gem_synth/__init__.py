@@ -61,11 +61,16 @@ def uniform(seed: int, tid: int, count: int) -> np.ndarray:
     return (u >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
-def normal(seed: int, tid: int, count: int) -> np.ndarray:
-    u = draws(seed, tid, 2 * count)
-    u1 = (u[0::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-    u2 = (u[1::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-    return np.sqrt(-2.0 * np.log1p(-u1)) * np.cos(2.0 * np.pi * u2)
+_CHUNK = 1 << 22
+
+
+def normal(seed: int, tid: int, count: int, out_dtype=np.float64) -> np.ndarray:
+    """count N(0,1) values; value i uses draws 2i and 2i+1 (generated in chunks)."""
+    out = np.empty(count, dtype=out_dtype)
+    for s in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - s)
+        out[s:s + n] = _normal_range(seed, tid, s, n)
+    return out
 
 
 def normal_f32(seed: int, tid: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
@@ -76,7 +81,21 @@ def normal_f32(seed: int, tid: int, shape, mean: float = 0.0, std: float = 1.0) 
 def normal_f16_bits(seed: int, tid: int, shape) -> np.ndarray:
     """N(0,1) rounded to binary16; returned as the uint16 bit patterns."""
     n = int(np.prod(shape))
-    return normal(seed, tid, n).astype(np.float16).view(np.uint16).reshape(shape)
+    out = np.empty(n, dtype=np.float16)
+    for s in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s)
+        out[s:s + m] = _normal_range(seed, tid, s, m).astype(np.float16)
+    return out.view(np.uint16).reshape(shape)
+
+
+def _normal_range(seed: int, tid: int, start: int, n: int) -> np.ndarray:
+    k = stream_key(seed, tid)
+    idx = np.arange(2 * start + 1, 2 * (start + n) + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        u = _mix(k + idx * _GAMMA)
+    u1 = (u[0::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    u2 = (u[1::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return np.sqrt(-2.0 * np.log1p(-u1)) * np.cos(2.0 * np.pi * u2)
 
 
 def q4_0_matrix(seed: int, tid: int, n_rows: int, k: int,

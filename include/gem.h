@@ -1,0 +1,200 @@
+/*
+ * gem.h — C ABI of the GB300 (sm_103a) decoder-step library: Q4_0 dequantise-and-matvec,
+ * RMSNorm / per-head QK-norm / RoPE / KV append, grouped-query split-K decode attention,
+ * gated FFN activation, and one whole decoder layer step.
+ *
+ * Sources, cited by page title and section:
+ *   [GEM]  "gem" engine research record (Gemma 4 native engine), sections "Verified model
+ *          facts" and "Native Metal diagnostic: buffer ownership" and the decode-attention
+ *          notes that follow them (split P*V partitions merged in ascending order).
+ *   [GELO] "GELO LLM generation", sections 02 (definitions: decode, KV cache, QK-norm, GQA,
+ *          sliding window, p-RoPE), 04 (Qwen3 family table), 05 (components: apply_qk_norm,
+ *          cached attention with n_kv = n_cache + 1) and 06 (block topology).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer owned by the caller.  The library never
+ *     allocates device memory; calls that need scratch take a caller-provided workspace
+ *     whose size is returned by the matching *_workspace() query.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Every
+ *     call only enqueues work and returns; results are ready when the stream reaches them.
+ *   - Activations are fp32, row-major [B][...] with the given row stride (in elements).
+ *     KV caches hold IEEE binary16 bit patterns (uint16_t), laid out [B][n_kv][cap][d].
+ *   - Q4_0 matrices are raw GGML bytes: N rows, each K/32 blocks of 18 bytes (binary16 scale
+ *     d little endian, then 16 bytes of 4-bit codes q; byte j holds element j in its low
+ *     nibble and element j + 16 in its high nibble); weight = (q - 8) * d.  [GEM]
+ *   - The fast path needs K % 256 == 0 and a 16-byte aligned matrix; other matrices with
+ *     K % 32 == 0 go through a slower general kernel.  K % 32 != 0 is rejected.
+ *   - Batch B is 0..8 (0 = nothing to do).  Larger batches are GEM_ERR_UNSUPPORTED_SHAPE.
+ *   - Arguments are checked on the host before anything is enqueued; a rejected call has
+ *     no effect.  Values only the device can see (positions) are checked by the kernels,
+ *     which then skip the offending sequence and OR a GEM_DEVFLAG_* bit into *status
+ *     (when `status` is NULL, into the library's own per-device word, read with
+ *     gem_device_status()).  Kernels never trap or assert.
+ */
+#ifndef GEM_H
+#define GEM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEM_API __attribute__((visibility("default")))
+#else
+#define GEM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gem_status {
+    GEM_OK = 0,
+    GEM_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad stride or enum */
+    GEM_ERR_MISALIGNED = 2,         /* pointer or stride violates a stated alignment */
+    GEM_ERR_UNSUPPORTED_SHAPE = 3,  /* K % 32 != 0, B > 8, head_dim not supported, ... */
+    GEM_ERR_CUDA = 4,               /* a CUDA runtime call failed; see gem_last_cuda_error() */
+    GEM_ERR_DEVICE_FLAG = 5,        /* gem_device_status() found a device-side flag set */
+    GEM_ERR_TIMEOUT = 6,            /* a device-side wait gave up (GEM_DEVFLAG_TIMEOUT) */
+    GEM_ERR_WORKSPACE = 7           /* workspace missing or smaller than the query returned */
+} gem_status;
+
+/* Device-side flag bits. */
+#define GEM_DEVFLAG_POS_RANGE 1 /* pos[b] < 0, or pos[b] >= cache_cap for full attention */
+#define GEM_DEVFLAG_TIMEOUT 2   /* a bounded wait on an asynchronous copy gave up */
+
+/* Static description of a status code. */
+GEM_API const char *gem_status_string(int status);
+/* cudaError_t of the last CUDA failure seen by a gem_* call on this thread (0 = none). */
+GEM_API int gem_last_cuda_error(void);
+/* Library version, major * 10000 + minor * 100 + patch. */
+GEM_API int gem_version(void);
+
+/* Synchronously read (and, if reset != 0, clear) the library's device-side flag word on
+ * the current device.  *flags receives the GEM_DEVFLAG_* bits.  Returns GEM_OK or
+ * GEM_ERR_CUDA.  Not for use inside stream capture. */
+GEM_API gem_status gem_device_status(int32_t *flags, int reset);
+
+/*
+ * Q4_0 dequantise-and-matvec  [GEM] "Native Metal diagnostic: buffer ownership": the
+ * SIMD-group Q4_0 matvec at the 31B FFN shape (5376 -> 21504) and the scalar C check.
+ *
+ *   y[b][n] = sum_{k<K} ((q[n][k] - 8) * d[n][k/32]) * x[b][k]  (+ residual[b][n])
+ *
+ *   W        N x (K/32) x 18 bytes, rows contiguous (row stride K/32*18 bytes).
+ *   x        [B][ldx] fp32, ldx >= K.       y  [B][ldy] fp32, ldy >= N.
+ *   residual nullable, [B][ldy] fp32; may alias y (read before write, element-wise).
+ *   Accumulation is fp32.  y must not overlap W or x.
+ */
+GEM_API gem_status gem_q4_0_gemv(const void *W, int64_t N, int64_t K, const float *x, int64_t ldx,
+                         int B, float *y, int64_t ldy, const float *residual, void *stream);
+
+/*
+ * Weighted RMSNorm  [GEM] "weighted RMSNorm over one or many heads"; [GELO] 06 pre-norm.
+ *   out[b][i] = x[b][i] / sqrt(mean_i x[b][i]^2 + eps) * gamma[i]   (gamma NULL: 1)
+ * x, out: [B][H] fp32 (may alias).
+ */
+GEM_API gem_status gem_rmsnorm(const float *x, int B, int64_t H, const float *gamma, float eps,
+                       float *out, void *stream);
+
+/*
+ * Per-head QK-norm, RoPE and KV append for one new token per sequence.
+ *   [GELO] 02/05 (QK-norm: each head's d-slice RMS-normalised with a shared gamma, before
+ *   RoPE; p-RoPE rotates only the first rope_dim dims); [GEM] "NeoX/proportional RoPE",
+ *   "Verified model facts" (full-attention V = unweighted RMSNorm of the K projection).
+ *
+ *   qkv      [B][ldqkv] fp32, in place.  Columns: Q heads [0, n_q*d), K heads
+ *            [n_q*d, (n_q+n_kv)*d), then V heads (only when v_mode == 0).
+ *   gamma_q, gamma_k  [d] fp32, nullable (NULL = no QK-norm for that tensor).
+ *   v_mode   0: V rows come from qkv;  1: V = RMSNorm(raw K row) with no weight.
+ *   pos      [B] int32 device: the new token's position p (= number of cached positions).
+ *   RoPE     NeoX pairing (i, i + rope_dim/2), angle p * theta^(-2i/rope_dim), evaluated in
+ *            fp64; rope_dim even, 2 <= rope_dim <= d.
+ *   Caches   [B][n_kv][cache_cap][d] binary16; the new K and V rows are written, rounded to
+ *            nearest even, at slot p (window == 0) or p mod window (window > 0, a ring of
+ *            `window` slots; requires window <= cache_cap).  Q and K in qkv are replaced by
+ *            their normalised, rotated fp32 values.
+ *   status   nullable device int32: receives GEM_DEVFLAG_POS_RANGE for a bad pos[b].
+ */
+GEM_API gem_status gem_rmsnorm_qknorm_rope(float *qkv, int64_t ldqkv, int B, int n_q, int n_kv,
+                                   int d, const float *gamma_q, const float *gamma_k,
+                                   int v_mode, float eps, const int32_t *pos, float theta,
+                                   int rope_dim, uint16_t *k_cache, uint16_t *v_cache,
+                                   int64_t cache_cap, int window, int32_t *status,
+                                   void *stream);
+
+/*
+ * Grouped-query decode attention, split-K over cache positions with an ordered merge.
+ *   [GELO] 02 (GQA, sliding window of the last W tokens), 05 (decode attends
+ *   n_kv = n_cache + 1 positions); [GEM] decode-attention notes (attention states over
+ *   disjoint token ranges compose; partials summed in ascending partition order).
+ *
+ *   For sequence b with p = pos[b] and query head h (KV head g = h / (n_q / n_kv)):
+ *     slots   S = {0 .. p} (window == 0) or {0 .. min(window, p + 1) - 1} (ring)
+ *     out[b][h*d + i] = sum_{s in S} softmax_s(scale * q_h . K[b][g][s]) * V[b][g][s][i]
+ *   q       [B][ldq] fp32, query heads contiguous (head h at column h*d).
+ *   caches  [B][n_kv][cache_cap][d] binary16, must already hold the new token's row.
+ *   out     [B][ldo] fp32.
+ *   d       64, 128, 256 or 512.  n_q % n_kv == 0 and n_q / n_kv <= 8.
+ *   workspace  device scratch of gem_gqa_decode_attn_workspace() bytes (same B, n_q, n_kv,
+ *           d, cache_cap, window), 256-byte aligned; contents need no initialisation.
+ *   Results are deterministic: the split count depends only on (p, shape, device), and
+ *   partial states are merged in ascending split order.
+ */
+GEM_API size_t gem_gqa_decode_attn_workspace(int B, int n_q, int n_kv, int d, int64_t cache_cap,
+                                     int window);
+GEM_API gem_status gem_gqa_decode_attn(const float *q, int64_t ldq, const uint16_t *k_cache,
+                               const uint16_t *v_cache, int B, int n_q, int n_kv, int d,
+                               int64_t cache_cap, const int32_t *pos, int window, float scale,
+                               float *out, int64_t ldo, void *workspace, size_t ws_bytes,
+                               int32_t *status, void *stream);
+
+/*
+ * Gated FFN activation  [GELO] 04/05 (Qwen3 SwiGLU; Gemma gelu_pytorch_tanh).
+ *   out = act(gate) * up,  act 0: silu(g) = g / (1 + e^-g);
+ *                          act 1: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
+ *   gate, up, out: [B][F] fp32 contiguous (out may alias either input).
+ */
+GEM_API gem_status gem_swiglu(const float *gate, const float *up, int B, int64_t F, int act,
+                      float *out, void *stream);
+
+/*
+ * One decoder layer step for B sequences (one new token each).
+ *   [GELO] 06 block topology (pre-norm, merged QKV, QK-norm, RoPE, GQA over the cache,
+ *   O projection + residual, pre-FFN norm, merged gate/up, gated activation, down
+ *   projection + residual); [GEM] "Verified model facts" (Gemma 4 full-attention layers:
+ *   no V projection, V = unweighted RMSNorm of the K projection).
+ *
+ *   Weight matrices are Q4_0 (see above):
+ *     w_qkv  [(n_q + n_kv + (v_from_k ? 0 : n_kv)) * d] x H
+ *     w_o    H x (n_q * d)        w_gate, w_up  F x H        w_down  H x F
+ *   Norm weights are fp32: g_attn, g_ffn [H]; g_q, g_k [d] (used when qk_norm);
+ *   g_post_attn, g_post_ffn [H] (used when post_norms: the O and down projection outputs
+ *   are RMS-normalised before each residual add).
+ *   act: 0 SiLU, 1 GELU-tanh.  scale: attention score scale.
+ */
+typedef struct gem_layer_desc {
+    int64_t H, n_q, n_kv, d, F;
+    float eps, theta, scale;
+    int rope_dim, window, act;
+    int qk_norm, v_from_k, post_norms;
+    const void *w_qkv, *w_o, *w_gate, *w_up, *w_down;
+    const float *g_attn, *g_ffn, *g_q, *g_k, *g_post_attn, *g_post_ffn;
+} gem_layer_desc;
+
+/*   x        [B][H] fp32 in/out (the residual stream).
+ *   k_cache, v_cache  this layer's caches [B][n_kv][cache_cap][d] binary16.
+ *   pos      [B] int32 device positions of the new tokens.
+ *   workspace  gem_decode_layer_workspace(L, B, cache_cap) bytes, 256-byte aligned;
+ *            contents need no initialisation.
+ *   The step is enqueued as a short chain of kernels linked by programmatic dependent
+ *   launch, so it can be captured into a CUDA graph for a stack of layers. */
+GEM_API size_t gem_decode_layer_workspace(const gem_layer_desc *L, int B, int64_t cache_cap);
+GEM_API gem_status gem_decode_layer(const gem_layer_desc *L, int B, float *x, uint16_t *k_cache,
+                            uint16_t *v_cache, int64_t cache_cap, const int32_t *pos,
+                            void *workspace, size_t ws_bytes, int32_t *status,
+                            void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GEM_H */

@@ -1,0 +1,196 @@
+"""Python binding of the GB300 decoder-step library (libgem.so, include/gem.h).
+
+Each function marshals torch CUDA tensors into the C ABI call of the same name and
+raises GemError on a non-zero status.  All computation runs in the CUDA library; torch
+only provides device memory and the current stream.  Importing this package fails if
+libgem.so is missing, and every call fails if the tensors are not on a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib
+from ._lib import LayerDesc
+
+lib = _lib.load()
+
+GEM_OK = 0
+ACT_SILU = 0
+ACT_GELU_TANH = 1
+DEVFLAG_POS_RANGE = 1
+DEVFLAG_TIMEOUT = 2
+
+__all__ = ["GemError", "q4_0_gemv", "rmsnorm", "rmsnorm_qknorm_rope", "gqa_decode_attn",
+           "gqa_decode_attn_workspace", "swiglu", "decode_layer", "decode_layer_workspace",
+           "DeviceLayer", "device_status", "LayerDesc"]
+
+
+class GemError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = lib.gem_status_string(status).decode()
+        if status == 4:
+            msg += " (cudaError %d)" % lib.gem_last_cuda_error()
+        super().__init__("%s: %s [status %d]" % (what, msg, status))
+
+
+def _check(st: int, what: str) -> None:
+    if st != GEM_OK:
+        raise GemError(st, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+_HALF_BITS = (torch.int16, torch.uint16)   # binary16 bit patterns
+
+
+def _dev(t: torch.Tensor | None, dtype, name: str):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    ok = t.dtype in dtype if isinstance(dtype, tuple) else t.dtype == dtype
+    if not ok:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def version() -> int:
+    return lib.gem_version()
+
+
+def device_status(reset: bool = False) -> int:
+    v = C.c_int32(0)
+    _check(lib.gem_device_status(C.byref(v), int(reset)), "gem_device_status")
+    return v.value
+
+
+def q4_0_gemv(W: torch.Tensor, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
+              residual: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[b] = deq(W) @ x[b] (+ residual[b]).  x: [B, >=K] fp32, y: [B, >=N] fp32."""
+    B = x.shape[0] if x.dim() == 2 else 1
+    st = lib.gem_q4_0_gemv(_dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"),
+                           x.shape[-1], B, _dev(y, torch.float32, "y"), y.shape[-1],
+                           _dev(residual, torch.float32, "residual"), _stream(stream))
+    _check(st, "gem_q4_0_gemv")
+    return y
+
+
+def rmsnorm(x: torch.Tensor, gamma: torch.Tensor | None, eps: float, out: torch.Tensor,
+            stream=None) -> torch.Tensor:
+    B = x.shape[0] if x.dim() == 2 else 1
+    st = lib.gem_rmsnorm(_dev(x, torch.float32, "x"), B, x.shape[-1],
+                         _dev(gamma, torch.float32, "gamma"), eps,
+                         _dev(out, torch.float32, "out"), _stream(stream))
+    _check(st, "gem_rmsnorm")
+    return out
+
+
+def rmsnorm_qknorm_rope(qkv: torch.Tensor, n_q: int, n_kv: int, d: int,
+                        gamma_q: torch.Tensor | None, gamma_k: torch.Tensor | None, v_mode: int,
+                        eps: float, pos: torch.Tensor, theta: float, rope_dim: int,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, window: int = 0,
+                        status: torch.Tensor | None = None, stream=None) -> None:
+    """qkv [B, ldqkv] fp32 in place; caches binary16 bits (int16/uint16) [B, n_kv, cap, d]; pos int32 [B]."""
+    B = qkv.shape[0]
+    cap = k_cache.shape[2]
+    st = lib.gem_rmsnorm_qknorm_rope(
+        _dev(qkv, torch.float32, "qkv"), qkv.shape[-1], B, n_q, n_kv, d,
+        _dev(gamma_q, torch.float32, "gamma_q"), _dev(gamma_k, torch.float32, "gamma_k"),
+        v_mode, eps, _dev(pos, torch.int32, "pos"), theta, rope_dim,
+        _dev(k_cache, _HALF_BITS, "k_cache"), _dev(v_cache, _HALF_BITS, "v_cache"), cap,
+        window, _dev(status, torch.int32, "status"), _stream(stream))
+    _check(st, "gem_rmsnorm_qknorm_rope")
+
+
+def gqa_decode_attn_workspace(B: int, n_q: int, n_kv: int, d: int, cache_cap: int,
+                              window: int = 0) -> int:
+    return int(lib.gem_gqa_decode_attn_workspace(B, n_q, n_kv, d, cache_cap, window))
+
+
+def gqa_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, n_q: int,
+                    n_kv: int, d: int, pos: torch.Tensor, window: int, scale: float,
+                    out: torch.Tensor, workspace: torch.Tensor | None = None,
+                    status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q [B, ldq] fp32 (head h at column h*d); caches uint16 [B, n_kv, cap, d]."""
+    B = q.shape[0]
+    cap = k_cache.shape[2]
+    ws_ptr = _dev(workspace, torch.uint8, "workspace")
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.gem_gqa_decode_attn(
+        _dev(q, torch.float32, "q"), q.shape[-1], _dev(k_cache, _HALF_BITS, "k_cache"),
+        _dev(v_cache, _HALF_BITS, "v_cache"), B, n_q, n_kv, d, cap,
+        _dev(pos, torch.int32, "pos"), window, scale, _dev(out, torch.float32, "out"),
+        out.shape[-1], ws_ptr, ws_bytes, _dev(status, torch.int32, "status"), _stream(stream))
+    _check(st, "gem_gqa_decode_attn")
+    return out
+
+
+def swiglu(gate: torch.Tensor, up: torch.Tensor, act: int, out: torch.Tensor,
+           stream=None) -> torch.Tensor:
+    B = gate.shape[0] if gate.dim() == 2 else 1
+    st = lib.gem_swiglu(_dev(gate, torch.float32, "gate"), _dev(up, torch.float32, "up"), B,
+                        gate.shape[-1], act, _dev(out, torch.float32, "out"), _stream(stream))
+    _check(st, "gem_swiglu")
+    return out
+
+
+class DeviceLayer:
+    """Device-resident weights of one decoder layer plus its gem_layer_desc."""
+
+    def __init__(self, shape, tensors, device="cuda"):
+        def up(a, dt):
+            return None if a is None else torch.from_numpy(a).to(device=device, dtype=dt).contiguous()
+
+        self.shape = shape
+        self.w_qkv = up(tensors.w_qkv, torch.uint8)
+        self.w_o = up(tensors.w_o, torch.uint8)
+        self.w_gate = up(tensors.w_gate, torch.uint8)
+        self.w_up = up(tensors.w_up, torch.uint8)
+        self.w_down = up(tensors.w_down, torch.uint8)
+        self.g_attn = up(tensors.g_attn, torch.float32)
+        self.g_ffn = up(tensors.g_ffn, torch.float32)
+        self.g_q = up(tensors.g_q, torch.float32)
+        self.g_k = up(tensors.g_k, torch.float32)
+        self.g_post_attn = up(tensors.g_post_attn, torch.float32)
+        self.g_post_ffn = up(tensors.g_post_ffn, torch.float32)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        s = shape
+        self.desc = LayerDesc(
+            H=s.H, n_q=s.n_q, n_kv=s.n_kv, d=s.d, F=s.F, eps=s.eps, theta=s.theta,
+            scale=float(s.scale), rope_dim=s.rope_dim, window=s.window, act=s.act,
+            qk_norm=int(s.qk_norm), v_from_k=int(s.v_from_k), post_norms=int(s.post_norms),
+            w_qkv=ptr(self.w_qkv), w_o=ptr(self.w_o), w_gate=ptr(self.w_gate),
+            w_up=ptr(self.w_up), w_down=ptr(self.w_down), g_attn=ptr(self.g_attn),
+            g_ffn=ptr(self.g_ffn), g_q=ptr(self.g_q), g_k=ptr(self.g_k),
+            g_post_attn=ptr(self.g_post_attn), g_post_ffn=ptr(self.g_post_ffn))
+
+    def weight_bytes(self) -> int:
+        return sum(t.numel() for t in (self.w_qkv, self.w_o, self.w_gate, self.w_up, self.w_down))
+
+
+def decode_layer_workspace(layer: DeviceLayer, B: int, cache_cap: int) -> int:
+    return int(lib.gem_decode_layer_workspace(C.byref(layer.desc), B, cache_cap))
+
+
+def decode_layer(layer: DeviceLayer, x: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, pos: torch.Tensor, workspace: torch.Tensor,
+                 status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One layer step, in place on x [B, H] fp32; caches uint16 [B, n_kv, cap, d]."""
+    B = x.shape[0]
+    st = lib.gem_decode_layer(C.byref(layer.desc), B, _dev(x, torch.float32, "x"),
+                              _dev(k_cache, _HALF_BITS, "k_cache"),
+                              _dev(v_cache, _HALF_BITS, "v_cache"), k_cache.shape[2],
+                              _dev(pos, torch.int32, "pos"), _dev(workspace, torch.uint8, "workspace"),
+                              workspace.numel(), _dev(status, torch.int32, "status"),
+                              _stream(stream))
+    _check(st, "gem_decode_layer")
+    return x

@@ -1,0 +1,512 @@
+// gem_attn.cu — grouped-query decode attention over a binary16 KV cache.
+//
+// GELO LLM generation, sections 02/05: at decode one query per head attends the
+// n_cache + 1 cached positions; G = n_q / n_kv query heads share each KV head; a sliding
+// window keeps the last W positions (here a ring of W slots).  "gem" research record,
+// decode-attention notes: attention states over disjoint token ranges compose, and the
+// partial results are merged in ascending partition order.
+//
+// Schedule.  Grid = (split, kv head, sequence).  The attended slots form the prefix
+// [0, T) of the cache (T = p + 1, or min(W, p + 1) for a ring), cut into tiles of TP slots
+// and split into contiguous tile ranges.  A CTA streams its K tiles and then its V tiles
+// through one ring of shared-memory stages with TMA (2-D map over [B*n_kv*cap][d]
+// binary16, boxes of TP rows x 64 elements, 128-byte swizzle so ldmatrix is conflict-free).
+// When launched inside the layer chain, the tiles are requested before
+// griddepcontrol.wait: only the new token's slot is written by the preceding kernel, and
+// that one row is re-read after the wait.
+//
+// Arithmetic.  Scores S = (scale q) K^T and the value sum P V run on mma.sync m16n8k16
+// (binary16 inputs, fp32 accumulate).  K and V are binary16 already (exact operands); q
+// and the probabilities are fp32 and enter as hi + lo binary16 pairs in rows h and h + 8
+// of the 16-row A operand (G <= 8 heads per KV head), so products keep ~22 bits.  The
+// split's softmax is exact (max over the split first, then exponentials); the split
+// writes (max, denominator, unnormalised output) and a merge kernel combines splits in
+// ascending order.  A split that has the whole range writes the final output directly.
+#include <algorithm>
+#include <map>
+#include <mutex>
+
+#include "gem_device.cuh"
+
+namespace gem {
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kMaxSplitSlots = 1024;   // slots one CTA may own (scores kept in shared memory)
+
+struct AttnParams {
+    const float* q;
+    int64_t ldq;
+    int B, n_q, n_kv, G;
+    int64_t cap;
+    int window;
+    float scale;
+    const int32_t* pos;
+    float* out;
+    int64_t ldo;
+    float* part;          // [B][n_q][nsplit_max][D + 2]
+    int nsplit_max;
+    int tp;               // slots per tile
+    int ltile;            // max tiles per split
+    int ns;               // ring stages
+    int early;            // positions and tiles may be read before griddepcontrol.wait
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off;
+    int* status;
+};
+
+__host__ __device__ __forceinline__ int tile_slots(int d) { return d <= 64 ? 128 : (d <= 128 ? 64 : 32); }
+
+// byte offset of (row r, element c) inside a tile stored as D/64 boxes of [TP][64] with the
+// 128-byte swizzle (16-byte chunk index XOR row mod 8)
+__device__ __forceinline__ uint32_t swz(int r, int c, int tp) {
+    const int box = c >> 6, cc = c & 63;
+    return static_cast<uint32_t>(box * tp * 128 + r * 128 + ((((cc >> 3) ^ r) & 7) << 4) + ((cc & 7) << 1));
+}
+
+__device__ __forceinline__ void split_range(int T, int tp, int nsplit_max, int s, int& nsplit, int& t0, int& t1) {
+    const int nt = (T + tp - 1) / tp;
+    nsplit = min(nsplit_max, nt);
+    t0 = static_cast<int>((static_cast<int64_t>(s) * nt) / nsplit);
+    t1 = static_cast<int>((static_cast<int64_t>(s + 1) * nt) / nsplit);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                 const __grid_constant__ CUtensorMap tmV,
+                                                                 const AttnParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128-byte-swizzled TMA tiles need a 1024-byte aligned base (the host adds the slack)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);
+    __half* qa = reinterpret_cast<__half*>(smem + P.qa_off);   // [16][D + 8]
+    float* sc = reinterpret_cast<float*>(smem + P.sc_off);     // [G][L]
+    __half* pa = reinterpret_cast<__half*>(smem + P.pa_off);   // [16][L + 8]
+    float* st = reinterpret_cast<float*>(smem + P.st_off);     // [8][2]: max, denominator
+    __shared__ int abort_flag;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int TP = P.tp;
+    const int L = P.ltile * TP;       // score row length
+    const int QA = D + 8, PA = L + 8;  // padded row pitches (elements)
+
+    if (!P.early) pdl_wait();
+    const int p = P.pos[b];
+    const bool bad = p < 0 || (P.window == 0 && static_cast<int64_t>(p) >= P.cap);
+    if (bad) {  // every CTA waits before leaving, so completion of this grid implies its predecessor's
+        pdl_trigger();
+        if (P.early) pdl_wait();
+        if (t == 0 && split == 0 && g == 0) atomicOr(P.status, GEM_DEVFLAG_POS_RANGE);
+        return;
+    }
+    const int T = P.window ? min(P.window, p + 1) : p + 1;
+    int nsplit, t0, t1;
+    split_range(T, TP, P.nsplit_max, split, nsplit, t0, t1);
+    if (split >= nsplit) {
+        pdl_trigger();
+        if (P.early) pdl_wait();
+        return;
+    }
+    const int ntile = t1 - t0;
+    const int nseq = 2 * ntile;                  // K tiles, then V tiles
+    const int slot_p = P.window ? p % P.window : p;
+    const int64_t row0 = (static_cast<int64_t>(b) * P.n_kv + g) * P.cap;
+    int npre = 0;
+
+    if (t == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < P.ns; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    __syncthreads();
+    uint64_t policy = 0;
+    auto issue = [&](int i) {
+        const int tile = t0 + (i < ntile ? i : i - ntile);
+        const CUtensorMap* tm = i < ntile ? &tmK : &tmV;
+        const int slot = i % P.ns;
+        uint8_t* dst = smem + static_cast<size_t>(slot) * P.tile_bytes;
+        fence_proxy_async_smem();  // generic writes to this slot (row refresh, zeroing) precede the TMA
+        mbar_arrive_expect_tx(&bars[slot], P.tile_bytes);
+        for (int j = 0; j < D / 64; ++j)
+            tma_load_2d(dst + j * TP * 128, tm, j * 64, static_cast<int32_t>(row0 + static_cast<int64_t>(tile) * TP),
+                        &bars[slot], policy);
+    };
+    if (t == 0) {
+        policy = l2_policy_evict_first();
+        npre = min(P.ns, nseq);
+        for (int i = 0; i < npre; ++i) issue(i);
+    }
+    __shared__ int s_npre;
+    if (t == 0) s_npre = npre;
+    pdl_trigger();
+    if (P.early) pdl_wait();
+
+    // q of this KV head's G query heads -> A operand rows (hi in rows 0..7, lo in 8..15)
+    for (int e = t; e < 16 * D; e += kAttnThreads) {
+        const int row = e / D, col = e - row * D, h = row & 7;
+        float v = 0.f;
+        if (h < P.G) v = P.q[b * P.ldq + static_cast<int64_t>(g * P.G + h) * D + col] * P.scale;
+        __half hi, lo;
+        split_hi_lo(v, hi, lo);
+        qa[row * QA + col] = row < 8 ? hi : lo;
+    }
+    __syncthreads();
+    const int pre = s_npre;
+
+    // refresh the new token's row in a tile that was requested before the wait
+    auto patch = [&](int i, uint8_t* tile) {
+        const int tl = t0 + (i < ntile ? i : i - ntile);
+        const int r = slot_p - tl * TP;
+        if (i < pre && r >= 0 && r < TP) {
+            const uint16_t* src = (i < ntile ? P.k_cache : P.v_cache) + (row0 + slot_p) * D;
+            for (int c = t * 8; c < D; c += kAttnThreads * 8)
+                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) = *reinterpret_cast<const uint4*>(src + c);
+        }
+    };
+
+    // ---- scores -----------------------------------------------------------------------------
+    const int gq = lane >> 2, tq = lane & 3;
+    for (int kt = 0; kt < ntile; ++kt) {
+        const int i = kt, slot = i % P.ns;
+        uint8_t* tile = smem + static_cast<size_t>(slot) * P.tile_bytes;
+        if (!mbar_wait(&bars[slot], static_cast<uint32_t>((i / P.ns) & 1), P.status)) abort_flag = 1;
+        patch(i, tile);
+        __syncthreads();
+        const uint32_t tbase = smem_u32(tile);
+        for (int n8 = warp; n8 < TP / 8; n8 += 4) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k16 = 0; k16 < D / 16; ++k16) {
+                uint32_t a0, a1, a2, a3, b0, b1;
+                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
+                const int brow = n8 * 8 + (lane & 7), bcol = k16 * 16 + ((lane >> 3) & 1) * 8;
+                ldmatrix_x2(b0, b1, tbase + swz(brow, bcol, TP));
+                mma_16816(c, a0, a1, a2, a3, b0, b1);
+            }
+            if (gq < P.G) {
+                const int col = kt * TP + n8 * 8 + 2 * tq;
+                const int s0 = (t0 + kt) * TP + n8 * 8 + 2 * tq;
+                sc[gq * L + col] = s0 < T ? c[0] + c[2] : -INFINITY;
+                sc[gq * L + col + 1] = s0 + 1 < T ? c[1] + c[3] : -INFINITY;
+            }
+        }
+        __syncthreads();
+        if (abort_flag) {  // a copy never landed: drain what is in flight and leave
+            if (t == 0) drain_stages(bars, P.ns, i, min(i + P.ns - 1, nseq - 1));
+            return;
+        }
+        if (t == 0 && i + P.ns < nseq) issue(i + P.ns);
+    }
+
+    // ---- softmax over the split (exact: max first) -------------------------------------------
+    const int Ls = ntile * TP;
+    for (int h = warp; h < 8; h += 4) {
+        float m = -INFINITY, l = 0.f;
+        if (h < P.G) {
+            for (int j = lane; j < Ls; j += 32) m = fmaxf(m, sc[h * L + j]);
+            m = warp_max(m);
+            for (int j = lane; j < Ls; j += 32) {
+                const float e = __expf(sc[h * L + j] - m);
+                l += e;
+                __half hi, lo;
+                split_hi_lo(e, hi, lo);
+                pa[h * PA + j] = hi;
+                pa[(h + 8) * PA + j] = lo;
+            }
+            l = warp_sum(l);
+        } else {
+            for (int j = lane; j < Ls; j += 32) {
+                pa[h * PA + j] = __float2half_rn(0.f);
+                pa[(h + 8) * PA + j] = __float2half_rn(0.f);
+            }
+        }
+        if (lane == 0) {
+            st[2 * h] = m;
+            st[2 * h + 1] = l;
+        }
+    }
+    __syncthreads();
+
+    // ---- P V ---------------------------------------------------------------------------------
+    constexpr int NW = D / 32;  // n8 tiles of output dims per warp
+    float acc[NW][4];
+#pragma unroll
+    for (int n = 0; n < NW; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int vt = 0; vt < ntile; ++vt) {
+        const int i = ntile + vt, slot = i % P.ns;
+        uint8_t* tile = smem + static_cast<size_t>(slot) * P.tile_bytes;
+        if (!mbar_wait(&bars[slot], static_cast<uint32_t>((i / P.ns) & 1), P.status)) abort_flag = 1;
+        patch(i, tile);
+        const int valid = T - (t0 + vt) * TP;   // rows >= valid hold other slots: zero them
+        if (valid < TP)
+            for (int e = t * 8; e < (TP - valid) * D; e += kAttnThreads * 8) {
+                const int r = valid + e / D, c = e % D;
+                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) = make_uint4(0, 0, 0, 0);
+            }
+        __syncthreads();
+        const uint32_t tbase = smem_u32(tile);
+        for (int k16 = 0; k16 < TP / 16; ++k16) {
+            uint32_t a0, a1, a2, a3;
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = vt * TP + k16 * 16 + (lane >> 4) * 8;
+            ldmatrix_x4(a0, a1, a2, a3, smem_u32(pa + arow * PA + acol));
+#pragma unroll
+            for (int n = 0; n < NW; n += 2) {
+                const int d0 = (warp * NW + n) * 8;
+                uint32_t b0, b1, b2, b3;
+                const int vrow = k16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int vcol = d0 + (lane >> 4) * 8;
+                ldmatrix_x4_trans(b0, b1, b2, b3, tbase + swz(vrow, vcol, TP));
+                mma_16816(acc[n], a0, a1, a2, a3, b0, b1);
+                mma_16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncthreads();
+        if (abort_flag) {
+            if (t == 0) drain_stages(bars, P.ns, i, min(i + P.ns - 1, nseq - 1));
+            return;
+        }
+        if (t == 0 && i + P.ns < nseq) issue(i + P.ns);
+    }
+
+    // ---- output ------------------------------------------------------------------------------
+    if (gq < P.G) {
+        const int h = g * P.G + gq;
+        const float m = st[2 * gq], l = st[2 * gq + 1];
+        if (nsplit == 1) {
+            float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int n = 0; n < NW; ++n) {
+                const int dd = (warp * NW + n) * 8 + 2 * tq;
+                o[dd] = (acc[n][0] + acc[n][2]) * inv;
+                o[dd + 1] = (acc[n][1] + acc[n][3]) * inv;
+            }
+        } else {
+            float* o = P.part + ((static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max + split) * (D + 2);
+#pragma unroll
+            for (int n = 0; n < NW; ++n) {
+                const int dd = (warp * NW + n) * 8 + 2 * tq;
+                o[dd] = acc[n][0] + acc[n][2];
+                o[dd + 1] = acc[n][1] + acc[n][3];
+            }
+            if (warp == 0 && tq == 0) {
+                o[D] = m;
+                o[D + 1] = l;
+            }
+        }
+    }
+}
+
+// Ordered merge of split states:  M = max_s m_s,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s
+__global__ void __launch_bounds__(128) gqa_merge_kernel(const AttnParams P, int D) {
+    pdl_trigger();
+    pdl_wait();
+    const int bh = blockIdx.x;
+    const int b = bh / P.n_q, h = bh - b * P.n_q;
+    const int p = P.pos[b];
+    if (p < 0 || (P.window == 0 && static_cast<int64_t>(p) >= P.cap)) return;
+    const int T = P.window ? min(P.window, p + 1) : p + 1;
+    const int nt = (T + P.tp - 1) / P.tp;
+    const int nsplit = min(P.nsplit_max, nt);
+    if (nsplit <= 1) return;
+    const float* base = P.part + (static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max * (D + 2);
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, base[s * (D + 2) + D]);
+    float den = 0.f;
+    for (int s = 0; s < nsplit; ++s) den += __expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + D + 1];
+    const float inv = 1.f / den;
+    float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        float v = 0.f;
+        for (int s = 0; s < nsplit; ++s) v += __expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + i];
+        o[i] = v * inv;
+    }
+}
+
+struct Plan {
+    int tp, nsplit_max, ltile, ns;
+    uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off;
+    size_t smem, ws;
+};
+
+Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num_sms) {
+    Plan pl{};
+    pl.tp = tile_slots(d);
+    const int64_t tmax = window ? std::min<int64_t>(window, cap) : cap;
+    const int64_t nt_max = std::max<int64_t>(1, (tmax + pl.tp - 1) / pl.tp);
+    const int64_t target = 2LL * num_sms;
+    int64_t ns = std::max<int64_t>(1, (target + static_cast<int64_t>(B) * n_kv - 1) / (static_cast<int64_t>(B) * n_kv));
+    ns = std::min(ns, nt_max);
+    const int max_tiles = kMaxSplitSlots / pl.tp;
+    if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
+    pl.nsplit_max = static_cast<int>(ns);
+    pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
+    pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
+    pl.ns = d >= 512 ? 3 : 4;
+    pl.ns = static_cast<int>(std::min<int64_t>(pl.ns, 2 * pl.ltile));
+    const int G = n_q / n_kv;
+    const int L = pl.ltile * pl.tp;
+    size_t off = static_cast<size_t>(pl.ns) * pl.tile_bytes;
+    pl.bar_off = static_cast<uint32_t>(off);
+    off = align_up(off + 8 * 8, 128);
+    pl.qa_off = static_cast<uint32_t>(off);
+    off = align_up(off + 16 * (d + 8) * 2, 128);
+    pl.sc_off = static_cast<uint32_t>(off);
+    off = align_up(off + static_cast<size_t>(G) * L * 4, 128);
+    pl.pa_off = static_cast<uint32_t>(off);
+    off = align_up(off + 16ull * (L + 8) * 2, 128);
+    pl.st_off = static_cast<uint32_t>(off);
+    off += 16 * 4;
+    pl.smem = align_up(off, 1024) + 1024;
+    pl.ws = static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
+    return pl;
+}
+
+using SplitKernel = void (*)(CUtensorMap, CUtensorMap, AttnParams);
+SplitKernel pick(int d) {
+    switch (d) {
+        case 64: return gqa_split_kernel<64>;
+        case 128: return gqa_split_kernel<128>;
+        case 256: return gqa_split_kernel<256>;
+        default: return gqa_split_kernel<512>;
+    }
+}
+
+gem_status ensure_smem_attn(const void* fn, int device, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, size_t> done;
+    std::lock_guard<std::mutex> lk(mu);
+    size_t& have = done[{device, fn}];
+    if (have >= bytes) return GEM_OK;
+    GEM_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)));
+    have = bytes;
+    return GEM_OK;
+}
+
+gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early) {
+    gem_status st = attn_check(op);
+    if (st != GEM_OK || op.B == 0 || op.n_q == 0) return st;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != GEM_OK) return st;
+    const Plan pl = make_plan(op.B, op.n_q, op.n_kv, op.d, op.cache_cap, op.window, di.num_sms);
+    if (pl.nsplit_max > 1 && (!op.workspace || op.ws_bytes < pl.ws)) return GEM_ERR_WORKSPACE;
+    if (pl.smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
+    AttnParams P{};
+    P.q = op.q;
+    P.ldq = op.ldq;
+    P.B = op.B;
+    P.n_q = op.n_q;
+    P.n_kv = op.n_kv;
+    P.G = op.n_q / op.n_kv;
+    P.cap = op.cache_cap;
+    P.window = op.window;
+    P.scale = op.scale;
+    P.pos = op.pos;
+    P.out = op.out;
+    P.ldo = op.ldo;
+    P.part = static_cast<float*>(op.workspace);
+    P.nsplit_max = pl.nsplit_max;
+    P.tp = pl.tp;
+    P.ltile = pl.ltile;
+    P.ns = pl.ns;
+    P.early = early ? 1 : 0;
+    P.k_cache = op.k_cache;
+    P.v_cache = op.v_cache;
+    P.tile_bytes = pl.tile_bytes;
+    P.bar_off = pl.bar_off;
+    P.qa_off = pl.qa_off;
+    P.sc_off = pl.sc_off;
+    P.pa_off = pl.pa_off;
+    P.st_off = pl.st_off;
+    P.status = op.status ? op.status : di.status_word;
+
+    const uint64_t rows = static_cast<uint64_t>(op.B) * op.n_kv * op.cache_cap;
+    CUtensorMap tmK, tmV;
+    if ((st = make_tensor_map_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT16, op.k_cache, op.d, rows,
+                                 static_cast<uint64_t>(op.d) * 2, 64, pl.tp, CU_TENSOR_MAP_SWIZZLE_128B)) != GEM_OK)
+        return st;
+    if ((st = make_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, op.v_cache, op.d, rows,
+                                 static_cast<uint64_t>(op.d) * 2, 64, pl.tp, CU_TENSOR_MAP_SWIZZLE_128B)) != GEM_OK)
+        return st;
+    const void* fn = reinterpret_cast<const void*>(pick(op.d));
+    if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
+    dim3 grid(pl.nsplit_max, op.n_kv, op.B);
+    void* args[] = {&tmK, &tmV, &P};
+    if ((st = launch_pdl(fn, grid, dim3(kAttnThreads), pl.smem, stream, args)) != GEM_OK) return st;
+    if (pl.nsplit_max > 1) {
+        int D = op.d;
+        void* margs[] = {&P, &D};
+        st = launch_pdl(reinterpret_cast<const void*>(gqa_merge_kernel), dim3(op.B * op.n_q), dim3(128), 0, stream,
+                        margs);
+    }
+    return st;
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window) {
+    if (B <= 0 || n_q <= 0 || n_kv <= 0 || cache_cap <= 0) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != GEM_OK) return 0;
+    const Plan pl = make_plan(B, n_q, n_kv, d, cache_cap, window, di.num_sms);
+    return pl.nsplit_max > 1 ? align_up(pl.ws, 256) : 0;
+}
+
+gem_status attn_check(const AttnOp& op) {
+    if (op.B < 0 || op.n_q < 0 || op.n_kv <= 0 || op.cache_cap <= 0 || op.window < 0) return GEM_ERR_INVALID_ARG;
+    if (op.d != 64 && op.d != 128 && op.d != 256 && op.d != 512) return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (op.n_q % op.n_kv) return GEM_ERR_INVALID_ARG;
+    if (op.n_q / op.n_kv > 8) return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (op.window > op.cache_cap) return GEM_ERR_INVALID_ARG;
+    if (op.B == 0 || op.n_q == 0) return GEM_OK;
+    if (!op.q || !op.k_cache || !op.v_cache || !op.pos || !op.out) return GEM_ERR_INVALID_ARG;
+    if (op.ldq < static_cast<int64_t>(op.n_q) * op.d || op.ldo < static_cast<int64_t>(op.n_q) * op.d)
+        return GEM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(op.k_cache) | reinterpret_cast<uintptr_t>(op.v_cache)) & 15)
+        return GEM_ERR_MISALIGNED;
+    if (static_cast<uint64_t>(op.B) * op.n_kv * op.cache_cap >= (1ull << 31)) return GEM_ERR_UNSUPPORTED_SHAPE;
+    return GEM_OK;
+}
+
+gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, false); }
+gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true); }
+
+}  // namespace gem
+
+extern "C" {
+
+size_t gem_gqa_decode_attn_workspace(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window) {
+    return gem::attn_workspace_bytes(B, n_q, n_kv, d, cache_cap, window);
+}
+
+gem_status gem_gqa_decode_attn(const float* q, int64_t ldq, const uint16_t* k_cache, const uint16_t* v_cache, int B,
+                               int n_q, int n_kv, int d, int64_t cache_cap, const int32_t* pos, int window,
+                               float scale, float* out, int64_t ldo, void* workspace, size_t ws_bytes,
+                               int32_t* status, void* stream) {
+    gem::AttnOp op{};
+    op.q = q;
+    op.ldq = ldq;
+    op.k_cache = k_cache;
+    op.v_cache = v_cache;
+    op.B = B;
+    op.n_q = n_q;
+    op.n_kv = n_kv;
+    op.d = d;
+    op.cache_cap = cache_cap;
+    op.pos = pos;
+    op.window = window;
+    op.scale = scale;
+    op.out = out;
+    op.ldo = ldo;
+    op.workspace = workspace;
+    op.ws_bytes = ws_bytes;
+    op.status = status;
+    return gem::attn_enqueue(op, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

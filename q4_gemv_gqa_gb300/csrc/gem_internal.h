@@ -1,0 +1,108 @@
+// gem_internal.h — declarations shared by the library's translation units (host side
+// plans and launchers; constants shared with device code).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gem.h"
+
+// Wall-time limit of every device-side wait on an asynchronous copy (1 s).
+#define GEM_WAIT_LIMIT_NS 1000000000ull
+
+namespace gem {
+
+// Record a CUDA error for gem_last_cuda_error() and map it to a status.
+gem_status cuda_fail(cudaError_t e);
+#define GEM_CUDA_TRY(expr)                              \
+    do {                                                \
+        cudaError_t _e = (expr);                        \
+        if (_e != cudaSuccess) return gem::cuda_fail(_e); \
+    } while (0)
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    size_t smem_optin;   // max dynamic shared memory per block
+    int* status_word;    // library-owned device flag word
+};
+// Properties of the current device (cached per device).
+gem_status device_info(DeviceInfo* out);
+
+// 2-D tiled tensor map (no interleave).  Returns GEM_ERR_CUDA if encoding fails.
+gem_status make_tensor_map_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                              uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes,
+                              uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+
+// Launch with programmatic stream serialization enabled.
+gem_status launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      void** args);
+
+// ---- Q4_0 GEMV ----------------------------------------------------------------------------
+struct GemvOp {
+    const void* W0;            // matrix (gate in pair mode)
+    const void* W1;            // up matrix in pair mode, else nullptr
+    int64_t N, K;
+    int B;
+    const float* x; int64_t ldx;
+    float* y; int64_t ldy;
+    const float* residual; int64_t ldr;   // nullable
+    const float* norm_gamma;              // nullable: RMSNorm x first (gamma over K)
+    float eps;
+    int act;                              // pair mode: 0 SiLU, 1 GELU-tanh
+};
+gem_status gemv_check(const GemvOp& op);
+gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream);
+
+// ---- norms / RoPE / activation -------------------------------------------------------------
+struct RopeOp {
+    float* qkv; int64_t ldqkv;
+    int B, n_q, n_kv, d;
+    const float *gamma_q, *gamma_k;
+    int v_mode;
+    float eps;
+    const int32_t* pos;
+    float theta;
+    int rope_dim;
+    uint16_t *k_cache, *v_cache;
+    int64_t cache_cap;
+    int window;
+    int32_t* status;
+};
+gem_status rope_check(const RopeOp& op);
+gem_status rope_enqueue(const RopeOp& op, cudaStream_t stream);
+
+gem_status rmsnorm_enqueue(const float* x, int B, int64_t H, const float* gamma, float eps, float* out,
+                           cudaStream_t stream);
+gem_status swiglu_enqueue(const float* gate, const float* up, int B, int64_t F, int act, float* out,
+                          cudaStream_t stream);
+// x[b] += RMSNorm(t[b]) * gamma   (Gemma post-attention / post-FFN norm before the residual add)
+gem_status postnorm_residual_enqueue(float* x, const float* t, int B, int64_t H, const float* gamma,
+                                     float eps, cudaStream_t stream);
+
+// ---- attention -----------------------------------------------------------------------------
+struct AttnOp {
+    const float* q; int64_t ldq;
+    const uint16_t *k_cache, *v_cache;
+    int B, n_q, n_kv, d;
+    int64_t cache_cap;
+    const int32_t* pos;
+    int window;
+    float scale;
+    float* out; int64_t ldo;
+    void* workspace; size_t ws_bytes;
+    int32_t* status;
+};
+size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window);
+gem_status attn_check(const AttnOp& op);
+gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream);
+// Same, for use right after the RoPE/append kernel of a layer step: positions and the
+// cached rows are read before griddepcontrol.wait (the preceding kernel writes neither,
+// except the new token's row, which is re-read after the wait).
+gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace gem

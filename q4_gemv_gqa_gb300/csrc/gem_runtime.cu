@@ -1,0 +1,131 @@
+// gem_runtime.cu — host runtime pieces: status strings, CUDA error recording, per-device
+// properties and flag word, tensor-map encoding and PDL launches.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gem_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+// One flag word per device; kernels OR GEM_DEVFLAG_* bits into it when the caller passes
+// no status pointer of its own.
+__device__ int g_device_flags;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+bool g_dev_ready[kMaxDevices];
+gem::DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+}  // namespace
+
+namespace gem {
+
+gem_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return GEM_ERR_CUDA;
+}
+
+gem_status device_info(DeviceInfo* out) {
+    int dev = 0;
+    GEM_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return GEM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        GEM_CUDA_TRY(cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev));
+        int optin = 0;
+        GEM_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        d.smem_optin = static_cast<size_t>(optin);
+        void* p = nullptr;
+        GEM_CUDA_TRY(cudaGetSymbolAddress(&p, g_device_flags));
+        d.status_word = static_cast<int*>(p);
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    return GEM_OK;
+}
+
+gem_status make_tensor_map_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
+                              uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                              CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode_err != cudaSuccess || !g_encode) return cuda_fail(g_encode_err);
+    cuuint64_t dims[2] = {dim0, dim1};
+    cuuint64_t strides[1] = {stride1_bytes};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return GEM_OK;
+}
+
+gem_status launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      void** args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    GEM_CUDA_TRY(cudaLaunchKernelExC(&cfg, kernel, args));
+    return GEM_OK;
+}
+
+}  // namespace gem
+
+extern "C" {
+
+const char* gem_status_string(int status) {
+    switch (status) {
+        case GEM_OK: return "ok";
+        case GEM_ERR_INVALID_ARG: return "invalid argument";
+        case GEM_ERR_MISALIGNED: return "misaligned pointer or stride";
+        case GEM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case GEM_ERR_CUDA: return "CUDA runtime error";
+        case GEM_ERR_DEVICE_FLAG: return "device-side flag set";
+        case GEM_ERR_TIMEOUT: return "device-side wait timed out";
+        case GEM_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int gem_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gem_version(void) { return 100; }
+
+gem_status gem_device_status(int32_t* flags, int reset) {
+    if (!flags) return GEM_ERR_INVALID_ARG;
+    gem::DeviceInfo di;
+    gem_status st = gem::device_info(&di);
+    if (st != GEM_OK) return st;
+    int v = 0;
+    GEM_CUDA_TRY(cudaMemcpy(&v, di.status_word, sizeof(int), cudaMemcpyDeviceToHost));
+    if (reset) GEM_CUDA_TRY(cudaMemset(di.status_word, 0, sizeof(int)));
+    *flags = v;
+    return GEM_OK;
+}
+
+}  // extern "C"

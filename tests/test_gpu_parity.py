@@ -1,0 +1,371 @@
+"""CUDA library vs the fp64 oracle on identical seeded inputs (GPU only).
+
+Every comparison goes through the C ABI (via the thin Python binding).  Tolerances are
+those of tests/parity.py: max-abs <= 2e-3 and relative L2 <= 1e-5.  Binary16 KV rows
+written by the kernels are compared to the oracle's rounding of the same value; a
+rounding decision may differ by one unit where the fp32 (GPU) and fp64 (oracle) values
+straddle a binary16 rounding boundary, and such differences must stay rare."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import gem_synth
+import oracle
+from gem_synth import configs
+from parity import assert_close, f16_ulp_diff
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gem():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import q4_gemv_gqa_gb300 as g
+    g.device_status(reset=True)
+    return g
+
+
+@pytest.fixture(scope="module")
+def torch_mod():
+    import torch
+    return torch
+
+
+def _cu(t, a, dtype=None):
+    x = t.from_numpy(np.ascontiguousarray(a)).cuda()
+    return x if dtype is None else x.to(dtype)
+
+
+def _half_cache(t, bits):
+    return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def _bits(tens):
+    return tens.cpu().numpy().view(np.uint16)
+
+
+# ---- Q4_0 GEMV ----------------------------------------------------------------------------
+
+GEMV_CASES = [
+    # (N, K, B): ragged row tails, several K stages, every batch size
+    (67, 256, 1), (67, 256, 2), (67, 256, 3), (67, 256, 4), (67, 256, 5), (67, 256, 6),
+    (67, 256, 7), (67, 256, 8), (33, 512, 3), (16, 2048, 1), (4096, 2048, 1), (2048, 6144, 1),
+    (6144, 2048, 8), (2560, 9728, 8), (1, 256, 1),
+]
+
+
+@pytest.mark.parametrize("N,K,B", GEMV_CASES)
+def test_gemv_matches_oracle(gem, torch_mod, N, K, B):
+    t = torch_mod
+    W = gem_synth.q4_0_matrix(1, N * 7 + K, N, K)
+    x = gem_synth.normal_f32(1, 3, (B, K))
+    ref = oracle.q4_0_gemv(W, N, K, x)
+    y = t.full((B, N), float("nan"), device="cuda")
+    gem.q4_0_gemv(_cu(t, W), N, K, _cu(t, x), y)
+    t.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, "gemv N=%d K=%d B=%d" % (N, K, B))
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_gemv_31b_ffn_shape_full(gem, torch_mod, B):
+    """The 31B FFN projection (5376 -> 21504, 65,028,096 weight bytes), every output."""
+    t = torch_mod
+    N, K = 21504, 5376
+    W = gem_synth.q4_0_matrix(0, 1000, N, K)
+    assert W.nbytes == 65_028_096
+    x = gem_synth.normal_f32(0, 1001, (B, K))
+    ref = oracle.q4_0_gemv(W, N, K, x)
+    y = t.empty((B, N), device="cuda")
+    gem.q4_0_gemv(_cu(t, W), N, K, _cu(t, x), y)
+    t.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, "gemv 31B FFN B=%d" % B)
+
+
+def test_gemv_residual_in_place(gem, torch_mod):
+    t = torch_mod
+    N, K, B = 300, 768, 2
+    W = gem_synth.q4_0_matrix(2, 5, N, K)
+    x = gem_synth.normal_f32(2, 6, (B, K))
+    r = gem_synth.normal_f32(2, 7, (B, N))
+    ref = oracle.q4_0_gemv(W, N, K, x, residual=r)
+    y = _cu(t, r)
+    gem.q4_0_gemv(_cu(t, W), N, K, _cu(t, x), y, residual=y)
+    t.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, "gemv residual in place")
+
+
+@pytest.mark.parametrize("N,K,B,offset", [(45, 96, 2, 0), (40, 512, 1, 2), (130, 3200, 3, 0)])
+def test_gemv_general_path(gem, torch_mod, N, K, B, offset):
+    """K % 256 != 0 or a matrix not 16-byte aligned runs the general kernel."""
+    t = torch_mod
+    W = gem_synth.q4_0_matrix(3, K, N, K)
+    x = gem_synth.normal_f32(3, 8, (B, K))
+    ref = oracle.q4_0_gemv(W, N, K, x)
+    buf = t.zeros(W.nbytes + 16, dtype=t.uint8, device="cuda")
+    buf[offset:offset + W.nbytes] = _cu(t, W.reshape(-1))
+    y = t.empty((B, N), device="cuda")
+    gem.q4_0_gemv(buf[offset:offset + W.nbytes], N, K, _cu(t, x), y)
+    t.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, "gemv general N=%d K=%d off=%d" % (N, K, offset))
+
+
+def test_gemv_empty_and_rejected(gem, torch_mod):
+    t = torch_mod
+    W = t.zeros(18 * 8, dtype=t.uint8, device="cuda")
+    x = t.zeros((1, 256), device="cuda")
+    y = t.zeros((1, 1), device="cuda")
+    gem.q4_0_gemv(W, 0, 256, x, y)          # N = 0: nothing to do
+    with pytest.raises(gem.GemError):
+        gem.q4_0_gemv(W, 1, 33, x, y)       # K % 32 != 0
+    with pytest.raises(gem.GemError):
+        gem.q4_0_gemv(W, 1, 256, t.zeros((9, 256), device="cuda"), t.zeros((9, 1), device="cuda"))
+
+
+def test_gemv_deterministic(gem, torch_mod):
+    t = torch_mod
+    N, K, B = 5000, 4096, 4
+    W = _cu(t, gem_synth.q4_0_matrix(4, 1, N, K))
+    x = _cu(t, gem_synth.normal_f32(4, 2, (B, K)))
+    y1 = t.empty((B, N), device="cuda")
+    y2 = t.empty((B, N), device="cuda")
+    gem.q4_0_gemv(W, N, K, x, y1)
+    gem.q4_0_gemv(W, N, K, x, y2)
+    t.cuda.synchronize()
+    assert t.equal(y1, y2)
+
+
+# ---- RMSNorm / activation -------------------------------------------------------------------
+
+def test_rmsnorm(gem, torch_mod):
+    t = torch_mod
+    B, H = 3, 2560
+    x = gem_synth.normal_f32(5, 1, (B, H)) * 4
+    g = gem_synth.norm_weight(5, 2, H)
+    out = t.empty((B, H), device="cuda")
+    gem.rmsnorm(_cu(t, x), _cu(t, g), 1e-6, out)
+    t.cuda.synchronize()
+    ref = np.stack([oracle.rmsnorm(x[b].astype(np.float64), g, 1e-6) for b in range(B)])
+    assert_close(out.cpu().numpy(), ref, "rmsnorm")
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_gated_activation(gem, torch_mod, act):
+    t = torch_mod
+    B, F = 2, 9728
+    g = gem_synth.normal_f32(6, 1, (B, F)) * 3
+    u = gem_synth.normal_f32(6, 2, (B, F))
+    out = t.empty((B, F), device="cuda")
+    gem.swiglu(_cu(t, g), _cu(t, u), act, out)
+    t.cuda.synchronize()
+    f = oracle.gelu_tanh if act else oracle.silu
+    ref = np.array([[f(float(g[b, i])) * float(u[b, i]) for i in range(F)] for b in range(B)])
+    assert_close(out.cpu().numpy(), ref, "activation %d" % act)
+
+
+# ---- QK-norm + RoPE + append ----------------------------------------------------------------
+
+ROPE_CASES = [
+    # (n_q, n_kv, d, rope_dim, theta, v_mode, window, pos list, cap)
+    (4, 2, 64, 64, 1e6, 0, 0, [128], 129),
+    (16, 8, 128, 128, 1e6, 0, 0, [4096], 4097),
+    (32, 8, 128, 128, 1e6, 0, 0, [2048, 0, 17, 2047, 1, 5, 100, 2000], 2049),
+    (32, 16, 256, 256, 1e4, 0, 1024, [32768], 1024),
+    (32, 4, 512, 128, 1e6, 1, 0, [32768], 32769),
+]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES, ids=lambda c: "d%d_R%d_v%d_w%d_B%d" % (c[2], c[3], c[5], c[6], len(c[7])))
+def test_qknorm_rope_append(gem, torch_mod, case):
+    t = torch_mod
+    n_q, n_kv, d, R, theta, v_mode, window, pos_l, cap = case
+    B = len(pos_l)
+    nqkv = (n_q + n_kv + (0 if v_mode else n_kv)) * d
+    qkv = gem_synth.normal_f32(7, d, (B, nqkv)) * 2
+    gq = gem_synth.norm_weight(7, 1, d)
+    gk = gem_synth.norm_weight(7, 2, d)
+    kc = gem_synth.normal_f16_bits(7, 3, (B, n_kv, cap, d))
+    vc = gem_synth.normal_f16_bits(7, 4, (B, n_kv, cap, d))
+    pos = np.array(pos_l, np.int32)
+    dq, dk, dv = _cu(t, qkv), _half_cache(t, kc), _half_cache(t, vc)
+    gem.rmsnorm_qknorm_rope(dq, n_q, n_kv, d, _cu(t, gq), _cu(t, gk), v_mode, 1e-6, _cu(t, pos), theta,
+                            R, dk, dv, window)
+    t.cuda.synchronize()
+    got = dq.cpu().numpy()
+    gk_bits, gv_bits = _bits(dk), _bits(dv)
+    for b in range(B):
+        p = int(pos[b])
+        slot = p % window if window else p
+        q = qkv[b, :n_q * d].reshape(n_q, d).astype(np.float64)
+        k = qkv[b, n_q * d:(n_q + n_kv) * d].reshape(n_kv, d).astype(np.float64)
+        rq = np.stack([oracle.rope_neox(oracle.rmsnorm(h, gq, 1e-6), R, p, theta) for h in q])
+        rk = np.stack([oracle.rope_neox(oracle.rmsnorm(h, gk, 1e-6), R, p, theta) for h in k])
+        if v_mode:
+            rv = np.stack([oracle.rmsnorm(h, None, 1e-6) for h in k])
+        else:
+            rv = qkv[b, (n_q + n_kv) * d:].reshape(n_kv, d).astype(np.float64)
+        assert_close(got[b, :n_q * d], rq.reshape(-1), "rope q b=%d" % b)
+        assert_close(got[b, n_q * d:(n_q + n_kv) * d], rk.reshape(-1), "rope k b=%d" % b)
+        ek = np.array([[oracle.double_to_half_via_f32(v) for v in row] for row in rk], np.uint16)
+        ev = np.array([[oracle.double_to_half_via_f32(v) for v in row] for row in rv], np.uint16)
+        dkk = f16_ulp_diff(gk_bits[b, :, slot], ek)
+        dvv = f16_ulp_diff(gv_bits[b, :, slot], ev)
+        assert dkk.max() <= 1 and dvv.max() <= 1
+        assert (dkk > 0).mean() < 0.01 and (dvv > 0).mean() < 0.01
+        # all other slots untouched
+        mask = np.ones(cap, bool)
+        mask[slot] = False
+        assert np.array_equal(gk_bits[b][:, mask], kc[b][:, mask])
+        assert np.array_equal(gv_bits[b][:, mask], vc[b][:, mask])
+
+
+def test_rope_bad_position_flags_and_skips(gem, torch_mod):
+    t = torch_mod
+    n_q, n_kv, d, cap = 2, 1, 64, 8
+    qkv = _cu(t, gem_synth.normal_f32(8, 1, (1, (n_q + 2 * n_kv) * d)))
+    before = qkv.clone()
+    kc = t.zeros((1, n_kv, cap, d), dtype=t.int16, device="cuda")
+    vc = t.zeros_like(kc)
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    gem.rmsnorm_qknorm_rope(qkv, n_q, n_kv, d, None, None, 0, 1e-6, _cu(t, np.array([8], np.int32)), 1e6, d,
+                            kc, vc, 0, status=status)
+    t.cuda.synchronize()
+    assert int(status.item()) & gem.DEVFLAG_POS_RANGE
+    assert t.equal(qkv, before) and int(kc.abs().sum()) == 0
+
+
+# ---- attention ----------------------------------------------------------------------------------
+
+ATTN_CASES = [
+    # (n_q, n_kv, d, window, positions, cap, scale)
+    (4, 2, 64, 0, [128], 129, 0.125),
+    (4, 4, 64, 0, [0], 1, 0.125),                       # one cached position: output = V
+    (8, 1, 64, 0, [15], 16, 0.125),                     # G = 8
+    (16, 8, 128, 0, [4096], 4097, 128 ** -0.5),         # Qwen3-1.7B shape
+    (32, 8, 128, 0, [2048] * 8, 2049, 128 ** -0.5),     # Qwen3-4B shape, B = 8
+    (32, 8, 128, 0, [0, 1, 63, 64, 65, 700, 1500, 2048], 2049, 128 ** -0.5),  # ragged lengths
+    (32, 16, 256, 1024, [32768], 1024, 1.0),            # Gemma SWA ring, full ring
+    (32, 16, 256, 1024, [700], 1024, 1.0),              # ring not yet full
+    (32, 4, 512, 0, [32768], 32769, 1.0),               # Gemma full-attention shape
+    (6, 2, 256, 0, [5000], 5001, 0.0625),
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "G%d_d%d_w%d_p%d_B%d" % (c[0] // c[1], c[2], c[3], max(c[4]), len(c[4])))
+def test_attention_matches_oracle(gem, torch_mod, case):
+    t = torch_mod
+    n_q, n_kv, d, window, pos_l, cap, scale = case
+    B = len(pos_l)
+    q = gem_synth.normal_f32(9, d, (B, n_q * d))
+    kc = gem_synth.normal_f16_bits(9, 1, (B, n_kv, cap, d))
+    vc = gem_synth.normal_f16_bits(9, 2, (B, n_kv, cap, d))
+    pos = np.array(pos_l, np.int32)
+    ws_bytes = gem.gqa_decode_attn_workspace(B, n_q, n_kv, d, cap, window)
+    ws = t.empty(max(ws_bytes, 1), dtype=t.uint8, device="cuda")
+    out = t.full((B, n_q * d), float("nan"), device="cuda")
+    gem.gqa_decode_attn(_cu(t, q), _half_cache(t, kc), _half_cache(t, vc), n_q, n_kv, d, _cu(t, pos), window,
+                        scale, out, ws if ws_bytes else None)
+    t.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b in range(B):
+        ref = oracle.gqa_attention(q[b].reshape(n_q, d), kc[b], vc[b], int(pos[b]), window, scale)
+        assert_close(got[b], ref.reshape(-1), "attention b=%d p=%d" % (b, pos[b]))
+    assert gem.device_status() == 0
+
+
+def test_attention_deterministic_repeat(gem, torch_mod):
+    t = torch_mod
+    n_q, n_kv, d, cap = 32, 4, 512, 9000
+    q = _cu(t, gem_synth.normal_f32(10, 1, (1, n_q * d)))
+    kc = _half_cache(t, gem_synth.normal_f16_bits(10, 2, (1, n_kv, cap, d)))
+    vc = _half_cache(t, gem_synth.normal_f16_bits(10, 3, (1, n_kv, cap, d)))
+    pos = _cu(t, np.array([cap - 1], np.int32))
+    ws = t.empty(gem.gqa_decode_attn_workspace(1, n_q, n_kv, d, cap, 0), dtype=t.uint8, device="cuda")
+    o1 = t.empty((1, n_q * d), device="cuda")
+    o2 = t.empty((1, n_q * d), device="cuda")
+    gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o1, ws)
+    gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o2, ws)
+    t.cuda.synchronize()
+    assert t.equal(o1, o2)
+
+
+def test_attention_needs_workspace(gem, torch_mod):
+    t = torch_mod
+    n_q, n_kv, d, cap = 16, 8, 128, 4097
+    need = gem.gqa_decode_attn_workspace(1, n_q, n_kv, d, cap, 0)
+    assert need > 0
+    q = t.zeros((1, n_q * d), device="cuda")
+    kc = t.zeros((1, n_kv, cap, d), dtype=t.int16, device="cuda")
+    with pytest.raises(gem.GemError):
+        gem.gqa_decode_attn(q, kc, kc, n_q, n_kv, d, _cu(t, np.array([4096], np.int32)), 0, 1.0,
+                            t.empty((1, n_q * d), device="cuda"), t.empty(need - 256, dtype=t.uint8, device="cuda"))
+
+
+# ---- one decoder layer step ----------------------------------------------------------------------
+
+def _small_gemma(full: bool):
+    base = configs.GEMMA31_FULL if full else configs.GEMMA31_SWA
+    return replace(base, H=512, n_q=8, n_kv=2 if full else 4, d=64 if not full else 128, F=1024,
+                   rope_dim=32 if full else 64, window=0 if full else 64)
+
+
+LAYER_CASES = [
+    ("tiny", configs.TINY, 1, [128]),
+    ("qwen3-1.7b", configs.QWEN3_1_7B, 1, [4096]),
+    ("qwen3-4b-b8", configs.QWEN3_4B, 8, [2048] * 8),
+    ("qwen3-4b-ragged", configs.QWEN3_4B, 3, [0, 1000, 2048]),
+    ("gemma-small-swa", _small_gemma(False), 2, [200, 30]),
+    ("gemma-small-full", _small_gemma(True), 1, [300]),
+    ("gemma4-31b-swa", configs.GEMMA31_SWA, 1, [32768]),
+    ("gemma4-31b-full", configs.GEMMA31_FULL, 1, [32768]),
+]
+
+
+def _run_layer(gem, t, shape, B, pos_l, seed=0, layer=0):
+    pos = np.array(pos_l, np.int32)
+    cap = shape.window if shape.window else int(pos.max()) + 1
+    tens = configs.layer_tensors(shape, B, cap, seed, layer)
+    x = gem_synth.normal_f32(seed, gem_synth.tid(layer, gem_synth.ROLE_X), (B, shape.H))
+    dl = gem.DeviceLayer(shape, tens)
+    dx = _cu(t, x)
+    dk, dv = _half_cache(t, tens.k_cache), _half_cache(t, tens.v_cache)
+    ws = t.empty(gem.decode_layer_workspace(dl, B, cap), dtype=t.uint8, device="cuda")
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    gem.decode_layer(dl, dx, dk, dv, _cu(t, pos), ws, status=status)
+    t.cuda.synchronize()
+    kc, vc = tens.k_cache.copy(), tens.v_cache.copy()
+    ref = oracle.decode_layer(shape, tens, x, pos, kc, vc)
+    return dx.cpu().numpy(), ref, _bits(dk), _bits(dv), kc, vc, int(status.item()), pos
+
+
+@pytest.mark.parametrize("name,shape,B,pos_l", LAYER_CASES, ids=[c[0] for c in LAYER_CASES])
+def test_decode_layer_matches_oracle(gem, torch_mod, name, shape, B, pos_l):
+    got, ref, gk, gv, ek, ev, status, pos = _run_layer(gem, torch_mod, shape, B, pos_l)
+    assert status == 0
+    assert_close(got, ref, "layer %s" % name)
+    dk, dv = f16_ulp_diff(gk, ek), f16_ulp_diff(gv, ev)
+    assert dk.max() <= 1 and dv.max() <= 1, "appended rows differ by more than one binary16 unit"
+    assert (dk > 0).mean() < 1e-3 and (dv > 0).mean() < 1e-3
+
+
+def test_decode_layer_stack_three_layers(gem, torch_mod):
+    """Three stacked Qwen3-1.7B-shape layers, each with its own weights and cache."""
+    t = torch_mod
+    shape, B, p = configs.QWEN3_1_7B, 1, 1024
+    cap = p + 1
+    pos = np.array([p], np.int32)
+    x = gem_synth.normal_f32(0, gem_synth.tid(0, gem_synth.ROLE_X), (B, shape.H))
+    dx = _cu(t, x)
+    xr = x.astype(np.float64)
+    dpos = _cu(t, pos)
+    for layer in range(3):
+        tens = configs.layer_tensors(shape, B, cap, 11, layer)
+        dl = gem.DeviceLayer(shape, tens)
+        dk, dv = _half_cache(t, tens.k_cache), _half_cache(t, tens.v_cache)
+        ws = t.empty(gem.decode_layer_workspace(dl, B, cap), dtype=t.uint8, device="cuda")
+        gem.decode_layer(dl, dx, dk, dv, dpos, ws)
+        kc, vc = tens.k_cache.copy(), tens.v_cache.copy()
+        xr = oracle.decode_layer(shape, tens, xr, pos, kc, vc)
+    t.cuda.synchronize()
+    assert_close(dx.cpu().numpy(), xr, "3-layer stack")

@@ -75,6 +75,10 @@ def lib():
                                                   C.c_int64, p, p, p, p, p]
             L.gem_oracle_decode_layer_f64.argtypes = [C.POINTER(Layer), C.c_int, p, p, p,
                                                       C.c_int64, p, p, p, p, p]
+            L.gem_oracle_decode_layer_ex.argtypes = [C.POINTER(Layer), C.c_int, p, p, p,
+                                                     C.c_int64, p, p, p, p, p, p, p]
+            L.gem_oracle_other_half_via_f32.restype = C.c_uint16
+            L.gem_oracle_other_half_via_f32.argtypes = [C.c_double]
             L.gem_oracle_argmax.restype = C.c_int64
             L.gem_oracle_argmax.argtypes = [p, C.c_int64]
             L.gem_oracle_num_threads.restype = C.c_int
@@ -97,6 +101,10 @@ def half_to_double(h: int) -> float:
 
 def double_to_half_via_f32(v: float) -> int:
     return int(lib().gem_oracle_double_to_half_via_f32(float(v)))
+
+
+def other_half_via_f32(v: float) -> int:
+    return int(lib().gem_oracle_other_half_via_f32(float(v)))
 
 
 def q4_0_dequant(W: np.ndarray, N: int, K: int) -> np.ndarray:
@@ -203,9 +211,12 @@ def make_layer(shape, t) -> tuple:
 
 
 def decode_layer(shape, tensors, x: np.ndarray, pos: np.ndarray, k_cache: np.ndarray,
-                 v_cache: np.ndarray, stages: bool = False):
+                 v_cache: np.ndarray, stages: bool = False, flip: np.ndarray | None = None,
+                 kvnew: bool = False):
     """One layer step.  k_cache / v_cache (uint16, [B, n_kv, cap, d]) are updated in
-    place with the appended row.  Returns x_out (fp64) or (x_out, qkv, attn, h)."""
+    place with the appended row.  Returns x_out (fp64), or with stages=True the tuple
+    (x_out, qkv, attn, h); kvnew=True appends the unrounded new rows [B, 2, n_kv, d].
+    flip (int8 [B, 2, n_kv, d]) selects the other binary16 neighbour for those elements."""
     L, keep = make_layer(shape, tensors)
     B = x.shape[0]
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
@@ -215,15 +226,16 @@ def decode_layer(shape, tensors, x: np.ndarray, pos: np.ndarray, k_cache: np.nda
     qkv = np.empty((B, shape.n_qkv), dtype=np.float64) if stages else None
     att = np.empty((B, shape.n_q * shape.d), dtype=np.float64) if stages else None
     h = np.empty((B, shape.H), dtype=np.float64) if stages else None
-    if x.dtype == np.float64:
-        xx = _c(x, np.float64)
-        fn = lib().gem_oracle_decode_layer_f64
-    else:
-        xx = _c(x, np.float32)
-        fn = lib().gem_oracle_decode_layer
-    rc = fn(C.byref(L), B, _ptr(xx), _ptr(k_cache), _ptr(v_cache), cap, _ptr(pos),
-            _ptr(out), _ptr(qkv), _ptr(att), _ptr(h))
+    kvn = np.empty((B, 2, shape.n_kv, shape.d), dtype=np.float64) if kvnew else None
+    fl = _c(flip, np.int8)
+    xx = _c(x, np.float64)
+    rc = lib().gem_oracle_decode_layer_ex(C.byref(L), B, _ptr(xx), _ptr(k_cache), _ptr(v_cache),
+                                          cap, _ptr(pos), _ptr(out), _ptr(qkv), _ptr(att),
+                                          _ptr(h), _ptr(kvn), _ptr(fl))
     del keep
     if rc:
         raise ValueError("oracle decode layer failed (rc=%d)" % rc)
-    return (out, qkv, att, h) if stages else out
+    res = (out, qkv, att, h) if stages else (out,)
+    if kvnew:
+        res = res + (kvn,)
+    return res if len(res) > 1 else res[0]

@@ -57,6 +57,19 @@ uint16_t gem_oracle_double_to_half_via_f32(double v)
     return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0));
 }
 
+uint16_t gem_oracle_other_half_via_f32(double v)
+{
+    float f = (float)v;
+    uint16_t h = gem_oracle_double_to_half_via_f32(v);
+    double hv = gem_oracle_half_to_double(h);
+    if (isnan(f) || hv == (double)f)
+        return h;
+    /* binary16 codes on a monotone integer line: +x -> x, -x -> -(x & 0x7fff) */
+    int i = (h & 0x8000) ? -(int)(h & 0x7fff) : (int)h;
+    i += hv > (double)f ? -1 : 1;
+    return (uint16_t)(i < 0 ? (0x8000 | -i) : i);
+}
+
 /* ---- Q4_0 --------------------------------------------------------------------------
  * [GEM] "Verified model facts": Q4_0 matrices are rows of 32-weight blocks.  A block
  * is an 18-byte record: binary16 scale d (little endian), then 16 bytes of 4-bit
@@ -252,10 +265,11 @@ double gem_oracle_gelu_tanh(double g)
  * Gemma flags: V from the K projection by unweighted RMSNorm ([GEM] "Verified model
  * facts"); post-attention / post-FFN norms before each residual add (reading).
  */
-int gem_oracle_decode_layer_f64(const gem_oracle_layer *L, int B, const double *x_in,
-                                uint16_t *k_cache, uint16_t *v_cache, int64_t cap,
-                                const int32_t *pos, double *x_out, double *qkv_out,
-                                double *attn_out, double *h_out)
+int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x_in,
+                               uint16_t *k_cache, uint16_t *v_cache, int64_t cap,
+                               const int32_t *pos, double *x_out, double *qkv_out,
+                               double *attn_out, double *h_out, double *kvnew_out,
+                               const int8_t *flip)
 {
     const int64_t H = L->H, d = L->d, nq = L->n_q, nkv = L->n_kv, F = L->F;
     const int64_t qdim = nq * d, kdim = nkv * d;
@@ -320,8 +334,18 @@ int gem_oracle_decode_layer_f64(const gem_oracle_layer *L, int B, const double *
         }
         for (int64_t j = 0; j < nkv; ++j)
             for (int64_t i = 0; i < d; ++i) {
-                kc[(j * cap + slot) * d + i] = gem_oracle_double_to_half_via_f32(k[j * d + i]);
-                vc[(j * cap + slot) * d + i] = gem_oracle_double_to_half_via_f32(vrow[j * d + i]);
+                const int64_t fk = (((int64_t)b * 2 + 0) * nkv + j) * d + i;
+                const int64_t fv = (((int64_t)b * 2 + 1) * nkv + j) * d + i;
+                kc[(j * cap + slot) * d + i] = (flip && flip[fk])
+                    ? gem_oracle_other_half_via_f32(k[j * d + i])
+                    : gem_oracle_double_to_half_via_f32(k[j * d + i]);
+                vc[(j * cap + slot) * d + i] = (flip && flip[fv])
+                    ? gem_oracle_other_half_via_f32(vrow[j * d + i])
+                    : gem_oracle_double_to_half_via_f32(vrow[j * d + i]);
+                if (kvnew_out) {
+                    kvnew_out[fk] = k[j * d + i];
+                    kvnew_out[fv] = vrow[j * d + i];
+                }
             }
         /* a6 attention */
         rc = gem_oracle_gqa_attention(q, kc, vc, (int)nq, (int)nkv, (int)d, cap, p,
@@ -364,6 +388,15 @@ done:
     free(xn); free(qkv); free(vrow); free(tmp); free(att); free(o); free(h);
     free(g); free(u); free(a); free(dn);
     return rc;
+}
+
+int gem_oracle_decode_layer_f64(const gem_oracle_layer *L, int B, const double *x_in,
+                                uint16_t *k_cache, uint16_t *v_cache, int64_t cap,
+                                const int32_t *pos, double *x_out, double *qkv_out,
+                                double *attn_out, double *h_out)
+{
+    return gem_oracle_decode_layer_ex(L, B, x_in, k_cache, v_cache, cap, pos, x_out, qkv_out,
+                                      attn_out, h_out, NULL, NULL);
 }
 
 int gem_oracle_decode_layer(const gem_oracle_layer *L, int B, const float *x_in,

@@ -88,6 +88,23 @@ int gem_oracle_decode_layer_f64(const gem_oracle_layer *L, int B, const double *
                                 const int32_t *pos, double *x_out, double *qkv_out,
                                 double *attn_out, double *h_out);
 
+/* The step with two extra, optional arguments (nullable):
+ *   kvnew_out [B][2][n_kv][d]: the new K (index 0) and V (index 1) rows before rounding.
+ *   flip      [B][2][n_kv][d]: where non-zero, the appended binary16 code is the other
+ *             neighbour of the binary32 value (the one round-to-nearest-even did not pick);
+ *             a value that is exactly representable keeps its code.  This evaluates the
+ *             step for the other valid outcome of a rounding decision that lies within
+ *             the arithmetic's precision of a binary16 midpoint. */
+int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x_in,
+                               uint16_t *k_cache, uint16_t *v_cache, int64_t cap,
+                               const int32_t *pos, double *x_out, double *qkv_out,
+                               double *attn_out, double *h_out, double *kvnew_out,
+                               const int8_t *flip);
+
+/* The binary16 neighbour of fp32(v) on the other side from round-to-nearest-even
+ * (equal to the RNE code when fp32(v) is exactly representable). */
+uint16_t gem_oracle_other_half_via_f32(double v);
+
 /* Index of the largest value; ties go to the lowest index. */
 int64_t gem_oracle_argmax(const double *v, int64_t n);
 

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_co
             for (int j = lane; j < Ls; j += 32) m = fmaxf(m, sc[h * L + j]);
             m = warp_max(m);
             for (int j = lane; j < Ls; j += 32) {
-                const float e = __expf(sc[h * L + j] - m);
+                const float e = expf(sc[h * L + j] - m);
                 l += e;
                 __half hi, lo;
                 split_hi_lo(e, hi, lo);
@@ -318,12 +318,12 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const AttnParams P, int 
     float M = -INFINITY;
     for (int s = 0; s < nsplit; ++s) M = fmaxf(M, base[s * (D + 2) + D]);
     float den = 0.f;
-    for (int s = 0; s < nsplit; ++s) den += __expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + D + 1];
+    for (int s = 0; s < nsplit; ++s) den += expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + D + 1];
     const float inv = 1.f / den;
     float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
         float v = 0.f;
-        for (int s = 0; s < nsplit; ++s) v += __expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + i];
+        for (int s = 0; s < nsplit; ++s) v += expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + i];
         o[i] = v * inv;
     }
 }

@@ -16,12 +16,13 @@
 //
 // Arithmetic.  Each thread owns one (row, group) task per stage: it loads its 144 bytes
 // with nine 16-byte shared loads, and for each block forms the floats 1 + q/16 with one
-// byte permute per weight (exponent 0x3F8, code in mantissa bits 19..22).  Then
-//   sum_j (q_j - 8) x_j = 16 * (sum_j (1 + q_j/16) x_j - 1.5 * sum_j x_j)
-// where the per-block sum of x is computed once per CTA when the activation chunk is
-// staged.  Products accumulate in fp32 with packed f32x2 FMAs; the per-block result is
-// scaled by d in fp32.  No tensor cores: at batch 1..8 the op streams 0.5625 bytes per
-// weight and the budget is instruction issue, not math throughput.
+// byte permute per weight (exponent 0x3F8, code in mantissa bits 19..22); one packed add
+// of -1.5 turns them into the exact codes (q - 8)/16.  Products accumulate in fp32 with
+// packed f32x2 FMAs in two chains per block; the block sum is scaled by d in fp32 and the
+// factor 16 is applied once in the epilogue.  (Folding the -8 into a per-block sum of x
+// instead would save the add but cancels about two bits, which unit-scale attention
+// downstream of the QKV projection amplifies.)  No tensor cores: at batch 1..8 the op
+// streams 0.5625 bytes per weight and the budget is instruction issue, not math.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -145,12 +146,12 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
     const int per_group_tasks = nmat * p.up * kUnitRows;
     const size_t per_group_bytes = static_cast<size_t>(nmat) * p.up * kBoxBytes;
     // activation staging per group phase: raw ring (3 x (B+1) chunks), transformed x (2 x B),
-    // block sums (2 x B / 32), epilogue partials
+    // epilogue partials
     auto other_bytes = [&](int g) {
         const size_t chunk = static_cast<size_t>(g) * 256 * 4;
         const size_t red = std::max<size_t>(static_cast<size_t>(nmat) * p.up * kUnitRows * g * B * 4,
                                             static_cast<size_t>(kMaxThreads / 32) * B * 4);
-        return 3 * (B + 1) * chunk + 2 * B * chunk + 2 * B * chunk / 32 + red + 8 * 8 + 16 * 4 + 6 * 128;
+        return 3 * (B + 1) * chunk + 2 * B * chunk + red + 8 * 8 + 16 * 4 + 5 * 128;
     };
     int gps = std::max(1, std::min(p.G, kMaxThreads / per_group_tasks));
     while (gps > 1 && per_group_bytes * gps * 2 + other_bytes(gps) > kSmemBudget) --gps;
@@ -172,8 +173,6 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
     off = align_up(off + 3 * (B + 1) * chunk_bytes, 128);
     p.xs_off = static_cast<uint32_t>(off);
     off = align_up(off + 2 * B * chunk_bytes, 128);
-    p.bs_off = static_cast<uint32_t>(off);
-    off = align_up(off + 2 * B * chunk_bytes / 32, 128);
     p.rstd_off = static_cast<uint32_t>(off);
     off = align_up(off + 16 * 4, 128);
     p.red_off = static_cast<uint32_t>(off);

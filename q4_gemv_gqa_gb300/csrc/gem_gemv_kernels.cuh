@@ -33,7 +33,7 @@ struct GemvParams {
     int spp;          // stages per pass
     int tasks;        // nmat * up * 16 * gps
     uint32_t stage_bytes;
-    uint32_t bar_off, raw_off, xs_off, bs_off, rstd_off, red_off;
+    uint32_t bar_off, raw_off, xs_off, rstd_off, red_off;
     int* status;
 };
 
@@ -70,11 +70,9 @@ __device__ __forceinline__ float nib_float(uint32_t v) {
 
 // Accumulate one 144-byte group (8 blocks) of one row against BATCH activation chunks.
 //   xc: activation chunk for this group, batch b at xc + b * xstride (256 floats)
-//   cc: -1.5 * per-block sums of x, batch b at cc + b * cstride (8 floats)
 template <int BATCH, int BLK>
 __device__ __forceinline__ void dot_block(const uint32_t (&w)[36], const float* __restrict__ xc,
-                                          int xstride, const float* __restrict__ cc, int cstride,
-                                          float (&acc)[BATCH]) {
+                                          int xstride, float (&acc)[BATCH]) {
     constexpr int O = 18 * BLK;
     const uint32_t dbits = (O & 2) ? (w[O >> 2] >> 16) : (w[O >> 2] & 0xffffu);
     const float d = half_bits_to_float(dbits);
@@ -97,25 +95,30 @@ __device__ __forceinline__ void dot_block(const uint32_t (&w)[36], const float* 
         f[16 + 4 * wi + 2] = nib_float<2>(hi);
         f[16 + 4 * wi + 3] = nib_float<3>(hi);
     }
+    // (1 + q/16) - 1.5 = (q - 8)/16 exactly: every product below is of an exact weight code
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float2 e = fadd2(make_float2(f[2 * i], f[2 * i + 1]), make_float2(-1.5f, -1.5f));
+        f[2 * i] = e.x;
+        f[2 * i + 1] = e.y;
+    }
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) {
         const float4* xv = reinterpret_cast<const float4*>(xc + b * xstride + 32 * BLK);
-        float2 s = make_float2(0.f, 0.f);
+        float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
             const float4 xx = xv[q4];
-            s = ffma2(make_float2(f[4 * q4 + 0], f[4 * q4 + 1]), make_float2(xx.x, xx.y), s);
-            s = ffma2(make_float2(f[4 * q4 + 2], f[4 * q4 + 3]), make_float2(xx.z, xx.w), s);
+            s0 = ffma2(make_float2(f[4 * q4 + 0], f[4 * q4 + 1]), make_float2(xx.x, xx.y), s0);
+            s1 = ffma2(make_float2(f[4 * q4 + 2], f[4 * q4 + 3]), make_float2(xx.z, xx.w), s1);
         }
-        const float c = cc[b * cstride + BLK];
-        acc[b] = fmaf(d, (s.x + s.y) + c, acc[b]);
+        acc[b] = fmaf(d, (s0.x + s0.y) + (s1.x + s1.y), acc[b]);
     }
 }
 
 template <int BATCH>
 __device__ __forceinline__ void dot_group(const uint8_t* __restrict__ src, const float* __restrict__ xc,
-                                          int xstride, const float* __restrict__ cc, int cstride,
-                                          float (&acc)[BATCH]) {
+                                          int xstride, float (&acc)[BATCH]) {
     uint32_t w[36];
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -126,14 +129,14 @@ __device__ __forceinline__ void dot_group(const uint8_t* __restrict__ src, const
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
     }
-    dot_block<BATCH, 0>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 1>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 2>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 3>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 4>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 5>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 6>(w, xc, xstride, cc, cstride, acc);
-    dot_block<BATCH, 7>(w, xc, xstride, cc, cstride, acc);
+    dot_block<BATCH, 0>(w, xc, xstride, acc);
+    dot_block<BATCH, 1>(w, xc, xstride, acc);
+    dot_block<BATCH, 2>(w, xc, xstride, acc);
+    dot_block<BATCH, 3>(w, xc, xstride, acc);
+    dot_block<BATCH, 4>(w, xc, xstride, acc);
+    dot_block<BATCH, 5>(w, xc, xstride, acc);
+    dot_block<BATCH, 6>(w, xc, xstride, acc);
+    dot_block<BATCH, 7>(w, xc, xstride, acc);
 }
 
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
@@ -153,7 +156,6 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     float* raw = reinterpret_cast<float*>(smem + p.raw_off);   // 3 x (BATCH + 1) x chunk
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);     // 2 x BATCH x chunk
-    float* bs = reinterpret_cast<float*>(smem + p.bs_off);     // 2 x BATCH x chunk/32
     float* rstd = reinterpret_cast<float*>(smem + p.rstd_off);
     float* red = reinterpret_cast<float*>(smem + p.red_off);
     __shared__ int abort_flag;
@@ -236,11 +238,10 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
     float ssq[BATCH];
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) ssq[b] = 0.f;
-    auto transform = [&](int s) {  // raw(s) -> xs[s & 1], bs[s & 1]
+    auto transform = [&](int s) {  // raw(s) -> xs[s & 1]
         if (s >= S) return;
         const float* rd = raw + static_cast<size_t>(s % 3) * rawsz;
         float* xd = xs + static_cast<size_t>(s & 1) * BATCH * chunk;
-        float* bd = bs + static_cast<size_t>(s & 1) * BATCH * (chunk / 32);
         const bool first_pass = s < p.spp;
         for (int f = t; f < BATCH * chunk / 4; f += nthr) {
             const int b = f / (chunk / 4);
@@ -256,11 +257,6 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
                 v.x *= g.x; v.y *= g.y; v.z *= g.z; v.w *= g.w;
             }
             *reinterpret_cast<float4*>(xd + b * chunk + i) = v;
-            float sv = (v.x + v.y) + (v.z + v.w);
-            sv += __shfl_xor_sync(0xffffffffu, sv, 1);
-            sv += __shfl_xor_sync(0xffffffffu, sv, 2);
-            sv += __shfl_xor_sync(0xffffffffu, sv, 4);
-            if ((t & 7) == 0) bd[f >> 3] = -1.5f * sv;
         }
     };
 
@@ -291,8 +287,7 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
             const uint8_t* src = smem + static_cast<size_t>(slot) * p.stage_bytes +
                                  ((phi * NMAT + mat) * p.up + uu) * kBoxBytes + r * kGroupBytes;
             const float* xc = xs + static_cast<size_t>(buf) * BATCH * chunk + phi * 256;
-            const float* cc = bs + static_cast<size_t>(buf) * BATCH * (chunk / 32) + phi * 8;
-            dot_group<BATCH>(src, xc, chunk, cc, chunk / 32, acc);
+            dot_group<BATCH>(src, xc, chunk, acc);
         }
 
         if (ks == p.spp - 1) {  // end of pass: combine the group phases of every row

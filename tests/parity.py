@@ -2,6 +2,9 @@
 
 Tolerance (stated for this library's fp32-accumulating kernels against the fp64 oracle):
 max-abs error <= 2e-3 and relative L2 error <= 1e-5 on every compared output."""
+import json
+import os
+
 import numpy as np
 
 MAX_ABS = 2e-3
@@ -22,6 +25,10 @@ def errors(got, ref):
 def assert_close(got, ref, what, max_abs=MAX_ABS, rel_l2=REL_L2):
     assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), "%s: non-finite output" % what
     ma, rl = errors(got, ref)
+    log = os.environ.get("GEM_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"what": what, "max_abs": ma, "rel_l2": rl}) + "\n")
     assert ma <= max_abs and rl <= rel_l2, "%s: max_abs=%.3e rel_l2=%.3e" % (what, ma, rl)
     return ma, rl
 

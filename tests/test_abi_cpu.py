@@ -16,8 +16,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from q4_gemv_gqa_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return C.CDLL(path)
 
 

@@ -13,7 +13,7 @@ import pytest
 import gem_synth
 import oracle
 from gem_synth import configs
-from parity import assert_close, f16_ulp_diff
+from parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,16 @@ def _half_cache(t, bits):
 
 def _bits(tens):
     return tens.cpu().numpy().view(np.uint16)
+
+
+# Relative slack of a kernel's fp32 new K/V value against the oracle's fp64 value (scaled
+# by the head's RMS): a binary16 rounding decision inside this band may go either way.
+EPS_KV = 2e-6
+
+
+def _ambiguous(v, rms):
+    d = EPS_KV * max(abs(v), rms)
+    return oracle.double_to_half_via_f32(v - d) != oracle.double_to_half_via_f32(v + d)
 
 
 # ---- Q4_0 GEMV ----------------------------------------------------------------------------
@@ -207,12 +217,17 @@ def test_qknorm_rope_append(gem, torch_mod, case):
             rv = qkv[b, (n_q + n_kv) * d:].reshape(n_kv, d).astype(np.float64)
         assert_close(got[b, :n_q * d], rq.reshape(-1), "rope q b=%d" % b)
         assert_close(got[b, n_q * d:(n_q + n_kv) * d], rk.reshape(-1), "rope k b=%d" % b)
-        ek = np.array([[oracle.double_to_half_via_f32(v) for v in row] for row in rk], np.uint16)
-        ev = np.array([[oracle.double_to_half_via_f32(v) for v in row] for row in rv], np.uint16)
-        dkk = f16_ulp_diff(gk_bits[b, :, slot], ek)
-        dvv = f16_ulp_diff(gv_bits[b, :, slot], ev)
-        assert dkk.max() <= 1 and dvv.max() <= 1
-        assert (dkk > 0).mean() < 0.01 and (dvv > 0).mean() < 0.01
+        for which, gbits, vals in ((0, gk_bits, rk), (1, gv_bits, rv)):
+            g = gbits[b, :, slot]
+            nd = 0
+            for j in range(n_kv):
+                rms = float(np.sqrt(np.mean(vals[j] ** 2)))
+                for i in range(d):
+                    v = float(vals[j, i])
+                    if g[j, i] != oracle.double_to_half_via_f32(v):
+                        assert g[j, i] == oracle.other_half_via_f32(v) and _ambiguous(v, rms)
+                        nd += 1
+            assert nd <= max(2, 0.005 * n_kv * d)
         # all other slots untouched
         mask = np.ones(cap, bool)
         mask[slot] = False
@@ -303,11 +318,63 @@ def test_attention_needs_workspace(gem, torch_mod):
 
 
 # ---- one decoder layer step ----------------------------------------------------------------------
+#
+# The new token's K and V rows are rounded to binary16 from fp32 (GPU) or from fp64 via
+# fp32 (oracle).  Where the value lies within the fp32 arithmetic's precision of a binary16
+# midpoint, both codes are valid outcomes.  The test accepts a differing code only if it
+# is the other neighbour of the oracle's value and the oracle marks that value ambiguous
+# (within EPS_KV of the midpoint, relative to the head's RMS); downstream outputs are then
+# compared with the oracle evaluated for that same outcome.
 
 def _small_gemma(full: bool):
     base = configs.GEMMA31_FULL if full else configs.GEMMA31_SWA
     return replace(base, H=512, n_q=8, n_kv=2 if full else 4, d=64 if not full else 128, F=1024,
                    rope_dim=32 if full else 64, window=0 if full else 64)
+
+
+def _gpu_layer(gem, t, shape, tens, x, pos, cap):
+    B = x.shape[0]
+    dl = gem.DeviceLayer(shape, tens)
+    dx = _cu(t, np.ascontiguousarray(x, dtype=np.float32))
+    dk, dv = _half_cache(t, tens.k_cache), _half_cache(t, tens.v_cache)
+    ws = t.empty(gem.decode_layer_workspace(dl, B, cap), dtype=t.uint8, device="cuda")
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    gem.decode_layer(dl, dx, dk, dv, _cu(t, pos), ws, status=status)
+    t.cuda.synchronize()
+    return dx.cpu().numpy(), _bits(dk), _bits(dv), int(status.item())
+
+
+def _layer_parity(shape, tens, x, pos, got, gk, gv, what):
+    """Compare one GPU layer step with the oracle; returns the number of appended codes
+    on the other side of an ambiguous rounding decision."""
+    xin = np.ascontiguousarray(x, dtype=np.float32)
+    kc, vc = tens.k_cache.copy(), tens.v_cache.copy()
+    ref, kvn = oracle.decode_layer(shape, tens, xin, pos, kc, vc, kvnew=True)
+    B, n_kv, d = len(pos), shape.n_kv, shape.d
+    flip = np.zeros((B, 2, n_kv, d), np.int8)
+    for b in range(B):
+        p = int(pos[b])
+        slot = p % shape.window if shape.window else p
+        for which, gbits, obits in ((0, gk, kc), (1, gv, vc)):
+            g, o = gbits[b, :, slot], obits[b, :, slot]
+            for j, i in np.argwhere(g != o):
+                v = kvn[b, which, j, i]
+                rms = float(np.sqrt(np.mean(kvn[b, which, j] ** 2)))
+                assert g[j, i] == oracle.other_half_via_f32(v), \
+                    "%s: appended code is not a binary16 neighbour of the value" % what
+                assert _ambiguous(v, rms), "%s: appended code differs away from a midpoint" % what
+                flip[b, which, j, i] = 1
+        mask = np.ones(gk.shape[2], bool)
+        mask[slot] = False
+        assert np.array_equal(gk[b][:, mask], tens.k_cache[b][:, mask]), "%s: other K slots changed" % what
+        assert np.array_equal(gv[b][:, mask], tens.v_cache[b][:, mask]), "%s: other V slots changed" % what
+    nflip = int(flip.sum())
+    assert nflip <= max(2, 0.005 * flip.size), "%s: %d rounding decisions differ" % (what, nflip)
+    if nflip:
+        ref = oracle.decode_layer(shape, tens, xin, pos, tens.k_cache.copy(), tens.v_cache.copy(),
+                                  flip=flip)
+    assert_close(got, ref, what)
+    return nflip, ref
 
 
 LAYER_CASES = [
@@ -322,50 +389,31 @@ LAYER_CASES = [
 ]
 
 
-def _run_layer(gem, t, shape, B, pos_l, seed=0, layer=0):
-    pos = np.array(pos_l, np.int32)
-    cap = shape.window if shape.window else int(pos.max()) + 1
-    tens = configs.layer_tensors(shape, B, cap, seed, layer)
-    x = gem_synth.normal_f32(seed, gem_synth.tid(layer, gem_synth.ROLE_X), (B, shape.H))
-    dl = gem.DeviceLayer(shape, tens)
-    dx = _cu(t, x)
-    dk, dv = _half_cache(t, tens.k_cache), _half_cache(t, tens.v_cache)
-    ws = t.empty(gem.decode_layer_workspace(dl, B, cap), dtype=t.uint8, device="cuda")
-    status = t.zeros(1, dtype=t.int32, device="cuda")
-    gem.decode_layer(dl, dx, dk, dv, _cu(t, pos), ws, status=status)
-    t.cuda.synchronize()
-    kc, vc = tens.k_cache.copy(), tens.v_cache.copy()
-    ref = oracle.decode_layer(shape, tens, x, pos, kc, vc)
-    return dx.cpu().numpy(), ref, _bits(dk), _bits(dv), kc, vc, int(status.item()), pos
-
-
 @pytest.mark.parametrize("name,shape,B,pos_l", LAYER_CASES, ids=[c[0] for c in LAYER_CASES])
 def test_decode_layer_matches_oracle(gem, torch_mod, name, shape, B, pos_l):
-    got, ref, gk, gv, ek, ev, status, pos = _run_layer(gem, torch_mod, shape, B, pos_l)
-    assert status == 0
-    assert_close(got, ref, "layer %s" % name)
-    dk, dv = f16_ulp_diff(gk, ek), f16_ulp_diff(gv, ev)
-    assert dk.max() <= 1 and dv.max() <= 1, "appended rows differ by more than one binary16 unit"
-    assert (dk > 0).mean() < 1e-3 and (dv > 0).mean() < 1e-3
-
-
-def test_decode_layer_stack_three_layers(gem, torch_mod):
-    """Three stacked Qwen3-1.7B-shape layers, each with its own weights and cache."""
-    t = torch_mod
-    shape, B, p = configs.QWEN3_1_7B, 1, 1024
-    cap = p + 1
-    pos = np.array([p], np.int32)
+    pos = np.array(pos_l, np.int32)
+    cap = shape.window if shape.window else int(pos.max()) + 1
+    tens = configs.layer_tensors(shape, B, cap, 0, 0)
     x = gem_synth.normal_f32(0, gem_synth.tid(0, gem_synth.ROLE_X), (B, shape.H))
-    dx = _cu(t, x)
-    xr = x.astype(np.float64)
-    dpos = _cu(t, pos)
-    for layer in range(3):
-        tens = configs.layer_tensors(shape, B, cap, 11, layer)
-        dl = gem.DeviceLayer(shape, tens)
-        dk, dv = _half_cache(t, tens.k_cache), _half_cache(t, tens.v_cache)
-        ws = t.empty(gem.decode_layer_workspace(dl, B, cap), dtype=t.uint8, device="cuda")
-        gem.decode_layer(dl, dx, dk, dv, dpos, ws)
-        kc, vc = tens.k_cache.copy(), tens.v_cache.copy()
-        xr = oracle.decode_layer(shape, tens, xr, pos, kc, vc)
-    t.cuda.synchronize()
-    assert_close(dx.cpu().numpy(), xr, "3-layer stack")
+    got, gk, gv, status = _gpu_layer(gem, torch_mod, shape, tens, x, pos, cap)
+    assert status == 0
+    _layer_parity(shape, tens, x, pos, got, gk, gv, "layer %s" % name)
+
+
+@pytest.mark.parametrize("name,nlayers", [("qwen3-1.7b", 4), ("gemma4-31b-group", 6)])
+def test_decode_layer_stack_each_layer_from_oracle_input(gem, torch_mod, name, nlayers):
+    """Stacked layers, each with its own weights and cache.  Layer l runs on both sides
+    from the oracle's output of layer l - 1 (rounded to fp32), so error does not compound
+    through the comparison; the oracle chain itself is carried in fp64."""
+    t = torch_mod
+    wl = configs.with_layers(configs.workload(name), nlayers)
+    if name == "qwen3-1.7b":
+        wl = replace(wl, pos=1024, cache_cap=(1025,) * nlayers)
+    pos = np.full(wl.B, wl.pos, np.int32)
+    x = gem_synth.normal_f32(0, gem_synth.tid(0, gem_synth.ROLE_X), (wl.B, wl.layers[0].H)).astype(np.float64)
+    for layer, (shape, cap) in enumerate(zip(wl.layers, wl.cache_cap)):
+        tens = configs.layer_tensors(shape, wl.B, cap, 11, layer)
+        got, gk, gv, status = _gpu_layer(gem, t, shape, tens, x, pos, cap)
+        assert status == 0
+        _, ref = _layer_parity(shape, tens, x, pos, got, gk, gv, "%s layer %d" % (name, layer))
+        x = ref

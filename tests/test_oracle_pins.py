@@ -435,3 +435,37 @@ def test_layer_equals_composition_of_pinned_steps(which):
     dn = oracle.q4_0_gemv(t.w_down, s.H, s.F, a[None])[0]
     ref = h + (oracle.rmsnorm(dn, t.g_post_ffn, s.eps) if s.post_norms else dn)
     assert np.array_equal(out[0], ref)
+
+
+def test_other_half_neighbour():
+    # 1 + 2^-11 lies exactly between 1.0 (0x3c00) and 1 + 2^-10 (0x3c01): RNE picks the
+    # even code 0x3c00, the other neighbour is 0x3c01
+    assert oracle.double_to_half_via_f32(1.0 + 2.0 ** -11) == 0x3C00
+    assert oracle.other_half_via_f32(1.0 + 2.0 ** -11) == 0x3C01
+    assert oracle.other_half_via_f32(1.0) == 0x3C00                  # exact: no other code
+    assert oracle.other_half_via_f32(-(1.0 + 2.0 ** -12)) == 0xBC01   # RNE -> -1.0, other -> away
+    rng = np.random.default_rng(3)
+    for v in rng.standard_normal(2000) * 10:
+        a = oracle.double_to_half_via_f32(v)
+        o = oracle.other_half_via_f32(v)
+        fa = np.float64(np.uint16(a).view(np.float16))
+        fo = np.float64(np.uint16(o).view(np.float16))
+        vf = float(np.float32(v))
+        assert min(fa, fo) <= vf <= max(fa, fo)      # the two codes bracket the value
+        assert abs(fa - vf) <= abs(fo - vf)          # RNE is the nearer one
+
+
+def test_layer_flip_changes_only_the_flipped_code():
+    w, s, t, x = _tiny()
+    pos = np.array([w.pos], np.int32)
+    kc, vc = t.k_cache.copy(), t.v_cache.copy()
+    out0, kvn = oracle.decode_layer(s, t, x, pos, kc, vc, kvnew=True)
+    flip = np.zeros((1, 2, s.n_kv, s.d), np.int8)
+    flip[0, 1, 1, 5] = 1
+    kc2, vc2 = t.k_cache.copy(), t.v_cache.copy()
+    out1 = oracle.decode_layer(s, t, x, pos, kc2, vc2, flip=flip)
+    assert np.array_equal(kc2, kc)
+    diff = vc2 != vc
+    assert diff.sum() == 1 and diff[0, 1, w.pos, 5]
+    assert vc2[0, 1, w.pos, 5] == oracle.other_half_via_f32(kvn[0, 1, 1, 5])
+    assert not np.array_equal(out0, out1)

@@ -201,6 +201,59 @@ def time_graph(torch, g, reps, warmup=3):
 
 # ---- arms -------------------------------------------------------------------------------------
 
+def run_kernel_only(args):
+    """A single op on its own (for ncu captures): `gemv` = the 31B FFN projection
+    (K=5376, N=21504) over 8 rotated matrices at --batch; `attn` = GQA decode attention over
+    the workload's first --layers caches."""
+    import torch
+    import q4_gemv_gqa_gb300 as gem
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    res = {"kernel": args.kernel}
+    if args.kernel == "gemv":
+        B = args.batch
+        mats = [torch.from_numpy(gem_synth.q4_0_matrix(0, 5000 + i, 21504, 5376)).cuda()
+                for i in range(args.mats)]
+        x = torch.from_numpy(gem_synth.normal_f32(0, 6000, (B, 5376))).cuda()
+        y = torch.empty((B, 21504), device="cuda")
+
+        def run():
+            for W in mats:
+                gem.q4_0_gemv(W, 21504, 5376, x, y)
+        b = gemv_bytes(21504, 5376, B)
+        n = len(mats)
+    else:
+        wl = configs.workload(args.workload)
+        wl = configs.with_layers(wl, args.layers or 2)
+        s0, cap = wl.layers[0], wl.cache_cap[0]
+        kcs = [torch.from_numpy(gem_synth.normal_f16_bits(0, 100 + i, (wl.B, s0.n_kv, cap, s0.d)).view(np.int16)).cuda()
+               for i in range(len(wl.layers))]
+        q = torch.from_numpy(gem_synth.normal_f32(0, 7, (wl.B, s0.n_q * s0.d))).cuda()
+        out = torch.empty_like(q)
+        pos = torch.full((wl.B,), wl.pos, dtype=torch.int32, device="cuda")
+        ws = torch.empty(max(1, gem.gqa_decode_attn_workspace(wl.B, s0.n_q, s0.n_kv, s0.d, cap, s0.window)),
+                         dtype=torch.uint8, device="cuda")
+
+        def run():
+            for kc in kcs:
+                gem.gqa_decode_attn(q, kc, kc, s0.n_q, s0.n_kv, s0.d, pos, s0.window, float(s0.scale), out, ws)
+        T = min(wl.pos + 1, s0.window) if s0.window else wl.pos + 1
+        b = attn_bytes(s0, wl.B, T)
+        n = len(kcs)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        run()
+    e1.record(st)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (args.steps * n)
+    res.update({"us_per_launch": round(us, 3), "bytes_per_launch": b, "gbs": round(b / us / 1e3, 1)})
+    print(json.dumps(res), flush=True)
+
+
 def run_gem(args):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -438,18 +491,24 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gem", "reference"], default="gem")
     ap.add_argument("--workload", default="qwen3-1.7b",
                     choices=["tiny", "qwen3-1.7b", "qwen3-4b-b8", "gemma4-31b-group"])
     ap.add_argument("--layers", type=int, default=0, help="use only the first n layers")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--kernel", choices=["step", "gemv", "attn"], default="step",
+                    help="time one op alone (for profiler captures) instead of the step")
+    ap.add_argument("--batch", type=int, default=1, help="--kernel gemv: activation rows")
+    ap.add_argument("--mats", type=int, default=8, help="--kernel gemv: rotated matrices")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel != "step":
+        run_kernel_only(args)
     else:
         run_gem(args)
 

@@ -142,19 +142,23 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
     p.U = static_cast<int>((op.N + kUnitRows - 1) / kUnitRows);
     const int C = std::min(di.num_sms, p.U);
     const int umax = (p.U + C - 1) / C;
-    p.up = std::max(1, std::min(umax, kMaxThreads / (kUnitRows * nmat)));
-    const int per_group_tasks = nmat * p.up * kUnitRows;
+    constexpr int kParts = gemv_detail::kPartsPerGroup;
+    p.up = std::max(1, std::min(umax, kMaxThreads / (kUnitRows * nmat * kParts)));
+    const int per_group_tasks = nmat * p.up * kUnitRows * kParts;
     const size_t per_group_bytes = static_cast<size_t>(nmat) * p.up * kBoxBytes;
     // activation staging per group phase: raw ring (3 x (B+1) chunks), transformed x (2 x B),
     // epilogue partials
     auto other_bytes = [&](int g) {
         const size_t chunk = static_cast<size_t>(g) * 256 * 4;
-        const size_t red = std::max<size_t>(static_cast<size_t>(nmat) * p.up * kUnitRows * g * B * 4,
+        const size_t red = std::max<size_t>(static_cast<size_t>(per_group_tasks) * g * B * 4,
                                             static_cast<size_t>(kMaxThreads / 32) * B * 4);
         return 3 * (B + 1) * chunk + 2 * B * chunk + red + 8 * 8 + 16 * 4 + 5 * 128;
     };
+    // groups per stage: as many as the thread budget allows, but keep a stage to about a
+    // third of the budget so at least three stages are in flight
     int gps = std::max(1, std::min(p.G, kMaxThreads / per_group_tasks));
-    while (gps > 1 && per_group_bytes * gps * 2 + other_bytes(gps) > kSmemBudget) --gps;
+    while (gps > 1 && per_group_bytes * gps * 3 + other_bytes(gps) > kSmemBudget) --gps;
+    gps = (p.G + (p.G + gps - 1) / gps - 1) / ((p.G + gps - 1) / gps);  // same stage count, even split
     p.gps = gps;
     p.spp = (p.G + gps - 1) / gps;
     p.tasks = per_group_tasks * gps;
@@ -176,8 +180,7 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
     p.rstd_off = static_cast<uint32_t>(off);
     off = align_up(off + 16 * 4, 128);
     p.red_off = static_cast<uint32_t>(off);
-    off += std::max<size_t>(static_cast<size_t>(nmat) * p.up * kUnitRows * gps * B * 4,
-                            static_cast<size_t>(kMaxThreads / 32) * B * 4);
+    off += std::max<size_t>(static_cast<size_t>(p.tasks) * B * 4, static_cast<size_t>(kMaxThreads / 32) * B * 4);
     const size_t smem = align_up(off, 128);
     if (smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
 

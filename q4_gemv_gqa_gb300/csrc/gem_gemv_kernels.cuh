@@ -11,7 +11,8 @@ namespace gemv_detail {
 constexpr int kGroupBytes = 144;                 // 8 blocks, 256 weights
 constexpr int kUnitRows = 16;                    // rows per TMA box
 constexpr int kBoxBytes = kGroupBytes * kUnitRows;
-constexpr int kMaxThreads = 512;
+constexpr int kMaxThreads = 640;
+constexpr int kPartsPerGroup = 4;               // a task covers 2 of a group's 8 blocks
 constexpr size_t kSmemBudget = 112 * 1024;       // leaves room for a neighbouring kernel's CTA
 
 struct GemvParams {
@@ -31,7 +32,7 @@ struct GemvParams {
     int gps;          // groups per stage
     int ns;           // ring stages
     int spp;          // stages per pass
-    int tasks;        // nmat * up * 16 * gps
+    int tasks;        // nmat * up * 16 * gps * kPartsPerGroup
     uint32_t stage_bytes;
     uint32_t bar_off, raw_off, xs_off, rstd_off, red_off;
     int* status;
@@ -45,19 +46,19 @@ __device__ __forceinline__ float act_fn(float g, int act) {
 
 // 32-bit little-endian word of the group at byte offset OFF (OFF even, compile-time).
 template <int OFF>
-__device__ __forceinline__ uint32_t word_at(const uint32_t (&w)[36]) {
+__device__ __forceinline__ uint32_t word_at(const uint32_t (&w)[9]) {
     if constexpr ((OFF & 3) == 0) return w[OFF >> 2];
     else return __funnelshift_r(w[OFF >> 2], w[(OFF >> 2) + 1], 16);
 }
 // word_at<OFF>() << 3 and >> 1, with any bits that the 0x78 byte mask discards left as
 // they fall; only bits 3..6 of each byte are used afterwards.
 template <int OFF>
-__device__ __forceinline__ uint32_t word_shl3(const uint32_t (&w)[36]) {
+__device__ __forceinline__ uint32_t word_shl3(const uint32_t (&w)[9]) {
     if constexpr ((OFF & 3) == 0) return w[OFF >> 2] << 3;
     else return __funnelshift_r(w[OFF >> 2], w[(OFF >> 2) + 1], 13);
 }
 template <int OFF>
-__device__ __forceinline__ uint32_t word_shr1(const uint32_t (&w)[36]) {
+__device__ __forceinline__ uint32_t word_shr1(const uint32_t (&w)[9]) {
     if constexpr ((OFF & 3) == 0) return w[OFF >> 2] >> 1;
     else return __funnelshift_r(w[OFF >> 2], w[(OFF >> 2) + 1], 17);
 }
@@ -68,10 +69,11 @@ __device__ __forceinline__ float nib_float(uint32_t v) {
     return __uint_as_float(__byte_perm(v, 0x3Fu, 0x4055u | (M << 8)));
 }
 
-// Accumulate one 144-byte group (8 blocks) of one row against BATCH activation chunks.
-//   xc: activation chunk for this group, batch b at xc + b * xstride (256 floats)
+// Accumulate block BLK (0 or 1) of a 36-byte task (two Q4_0 blocks of one row, held in
+// w[0..8]) against BATCH activation chunks: xc points at the task's 64 activations, batch b
+// at xc + b * xstride.
 template <int BATCH, int BLK>
-__device__ __forceinline__ void dot_block(const uint32_t (&w)[36], const float* __restrict__ xc,
+__device__ __forceinline__ void dot_block(const uint32_t (&w)[9], const float* __restrict__ xc,
                                           int xstride, float (&acc)[BATCH]) {
     constexpr int O = 18 * BLK;
     const uint32_t dbits = (O & 2) ? (w[O >> 2] >> 16) : (w[O >> 2] & 0xffffu);
@@ -117,26 +119,14 @@ __device__ __forceinline__ void dot_block(const uint32_t (&w)[36], const float* 
 }
 
 template <int BATCH>
-__device__ __forceinline__ void dot_group(const uint8_t* __restrict__ src, const float* __restrict__ xc,
-                                          int xstride, float (&acc)[BATCH]) {
-    uint32_t w[36];
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void dot_task(const uint8_t* __restrict__ src, const float* __restrict__ xc,
+                                         int xstride, float (&acc)[BATCH]) {
+    uint32_t w[9];
+    const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
 #pragma unroll
-    for (int i = 0; i < 9; ++i) {
-        const uint4 v = s4[i];
-        w[4 * i + 0] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
-    }
+    for (int i = 0; i < 9; ++i) w[i] = s4[i];
     dot_block<BATCH, 0>(w, xc, xstride, acc);
     dot_block<BATCH, 1>(w, xc, xstride, acc);
-    dot_block<BATCH, 2>(w, xc, xstride, acc);
-    dot_block<BATCH, 3>(w, xc, xstride, acc);
-    dot_block<BATCH, 4>(w, xc, xstride, acc);
-    dot_block<BATCH, 5>(w, xc, xstride, acc);
-    dot_block<BATCH, 6>(w, xc, xstride, acc);
-    dot_block<BATCH, 7>(w, xc, xstride, acc);
 }
 
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
@@ -172,9 +162,10 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
     const int rawsz = (BATCH + 1) * chunk;             // x rows + gamma
     const int rows_in_pass = NMAT * p.up * kUnitRows;  // task slots per group phase
 
-    // task of this thread
-    const int phi = t / rows_in_pass;
-    const int rem = t - phi * rows_in_pass;
+    // task of this thread: group phase phi, part pi (blocks 2pi, 2pi+1), row slot rem
+    const int psi = t / rows_in_pass;
+    const int phi = psi / kPartsPerGroup, pi = psi % kPartsPerGroup;
+    const int rem = t - psi * rows_in_pass;
     const int mat = rem / (p.up * kUnitRows);
     const int uu = (rem >> 4) % p.up;
     const int r = rem & 15;
@@ -285,9 +276,9 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
         if (!mbar_wait(&bars[slot], static_cast<uint32_t>((s / p.ns) & 1), p.status)) abort_flag = 1;
         if (t < p.tasks && phi < ng && uu < nup) {
             const uint8_t* src = smem + static_cast<size_t>(slot) * p.stage_bytes +
-                                 ((phi * NMAT + mat) * p.up + uu) * kBoxBytes + r * kGroupBytes;
-            const float* xc = xs + static_cast<size_t>(buf) * BATCH * chunk + phi * 256;
-            dot_group<BATCH>(src, xc, chunk, acc);
+                                 ((phi * NMAT + mat) * p.up + uu) * kBoxBytes + r * kGroupBytes + pi * 36;
+            const float* xc = xs + static_cast<size_t>(buf) * BATCH * chunk + phi * 256 + pi * 64;
+            dot_task<BATCH>(src, xc, chunk, acc);
         }
 
         if (ks == p.spp - 1) {  // end of pass: combine the group phases of every row
@@ -305,9 +296,10 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
                 }
                 __syncthreads();
             }
+            const int nph = p.gps * kPartsPerGroup;
             if (t < p.tasks) {
 #pragma unroll
-                for (int b = 0; b < BATCH; ++b) red[(rem * p.gps + phi) * BATCH + b] = acc[b];
+                for (int b = 0; b < BATCH; ++b) red[(rem * nph + psi) * BATCH + b] = acc[b];
             }
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) acc[b] = 0.f;
@@ -319,14 +311,14 @@ __global__ void __launch_bounds__(kMaxThreads) q4_0_gemv_tma_kernel(const __grid
                     for (int b = 0; b < BATCH; ++b) {
                         const float scale = 16.f * (p.gamma ? rstd[b] : 1.f);
                         float v = 0.f;
-                        for (int ph = 0; ph < p.gps; ++ph) v += red[(t * p.gps + ph) * BATCH + b];
+                        for (int ph = 0; ph < nph; ++ph) v += red[(t * nph + ph) * BATCH + b];
                         v *= scale;
                         if (NMAT == 1) {
                             if (p.residual) v += p.residual[b * p.ldr + n];
                         } else {
                             float uv = 0.f;
                             const int srow = p.up * kUnitRows + t;
-                            for (int ph = 0; ph < p.gps; ++ph) uv += red[(srow * p.gps + ph) * BATCH + b];
+                            for (int ph = 0; ph < nph; ++ph) uv += red[(srow * nph + ph) * BATCH + b];
                             v = act_fn(v, p.act) * (uv * scale);
                         }
                         p.y[b * p.ldy + n] = v;

@@ -227,6 +227,8 @@ def run_kernel_only(args):
         s0, cap = wl.layers[0], wl.cache_cap[0]
         kcs = [torch.from_numpy(gem_synth.normal_f16_bits(0, 100 + i, (wl.B, s0.n_kv, cap, s0.d)).view(np.int16)).cuda()
                for i in range(len(wl.layers))]
+        vcs = [torch.from_numpy(gem_synth.normal_f16_bits(0, 200 + i, (wl.B, s0.n_kv, cap, s0.d)).view(np.int16)).cuda()
+               for i in range(len(wl.layers))]
         q = torch.from_numpy(gem_synth.normal_f32(0, 7, (wl.B, s0.n_q * s0.d))).cuda()
         out = torch.empty_like(q)
         pos = torch.full((wl.B,), wl.pos, dtype=torch.int32, device="cuda")
@@ -234,8 +236,8 @@ def run_kernel_only(args):
                          dtype=torch.uint8, device="cuda")
 
         def run():
-            for kc in kcs:
-                gem.gqa_decode_attn(q, kc, kc, s0.n_q, s0.n_kv, s0.d, pos, s0.window, float(s0.scale), out, ws)
+            for kc, vc in zip(kcs, vcs):
+                gem.gqa_decode_attn(q, kc, vc, s0.n_q, s0.n_kv, s0.d, pos, s0.window, float(s0.scale), out, ws)
         T = min(wl.pos + 1, s0.window) if s0.window else wl.pos + 1
         b = attn_bytes(s0, wl.B, T)
         n = len(kcs)

@@ -73,7 +73,7 @@ __device__ __forceinline__ void split_range(int T, int tp, int nsplit_max, int s
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                  const __grid_constant__ CUtensorMap tmV,
                                                                  const AttnParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -145,14 +145,37 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_co
     pdl_trigger();
     if (P.early) pdl_wait();
 
-    // q of this KV head's G query heads -> A operand rows (hi in rows 0..7, lo in 8..15)
-    for (int e = t; e < 16 * D; e += kAttnThreads) {
-        const int row = e / D, col = e - row * D, h = row & 7;
-        float v = 0.f;
-        if (h < P.G) v = P.q[b * P.ldq + static_cast<int64_t>(g * P.G + h) * D + col] * P.scale;
-        __half hi, lo;
-        split_hi_lo(v, hi, lo);
-        qa[row * QA + col] = row < 8 ? hi : lo;
+    // q of this KV head's G query heads -> A operand rows (hi in rows 0..7, lo in 8..15).
+    // All loads of a thread are issued before any is used: one L2 round trip in total.
+    {
+        constexpr int kMaxF4 = 8 * D / 4 / kAttnThreads;  // float4 slots per thread (G <= 8)
+        const int nf4 = P.G * D / 4;
+        const float4* qsrc = reinterpret_cast<const float4*>(P.q + b * P.ldq + static_cast<int64_t>(g) * P.G * D);
+        float4 qv[kMaxF4];
+#pragma unroll
+        for (int i = 0; i < kMaxF4; ++i) {
+            const int f = t + i * kAttnThreads;
+            qv[i] = f < nf4 ? qsrc[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxF4; ++i) {
+            const int f = t + i * kAttnThreads;
+            if (f < nf4) {
+                const int h = (f * 4) / D, col = (f * 4) % D;
+                const float v[4] = {qv[i].x * P.scale, qv[i].y * P.scale, qv[i].z * P.scale, qv[i].w * P.scale};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    __half hi, lo;
+                    split_hi_lo(v[j], hi, lo);
+                    qa[h * QA + col + j] = hi;
+                    qa[(h + 8) * QA + col + j] = lo;
+                }
+            }
+        }
+        for (int e = P.G * D + t; e < 8 * D; e += kAttnThreads) {  // unused head rows
+            qa[(e / D) * QA + e % D] = __float2half_rn(0.f);
+            qa[(e / D + 8) * QA + e % D] = __float2half_rn(0.f);
+        }
     }
     __syncthreads();
     const int pre = s_npre;
@@ -170,6 +193,16 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_co
 
     // ---- scores -----------------------------------------------------------------------------
     const int gq = lane >> 2, tq = lane & 3;
+    // q's A fragments are the same for every position tile: keep them in registers when small
+    constexpr bool kQReg = D <= 256;
+    uint32_t qf[kQReg ? D / 16 : 1][4];
+    if constexpr (kQReg) {
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16) {
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+            ldmatrix_x4(qf[k16][0], qf[k16][1], qf[k16][2], qf[k16][3], smem_u32(qa + arow * QA + acol));
+        }
+    }
     for (int kt = 0; kt < ntile; ++kt) {
         const int i = kt, slot = i % P.ns;
         uint8_t* tile = smem + static_cast<size_t>(slot) * P.tile_bytes;
@@ -179,11 +212,15 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_co
         const uint32_t tbase = smem_u32(tile);
         for (int n8 = warp; n8 < TP / 8; n8 += 4) {
             float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll
             for (int k16 = 0; k16 < D / 16; ++k16) {
                 uint32_t a0, a1, a2, a3, b0, b1;
-                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
-                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
+                if constexpr (kQReg) {
+                    a0 = qf[k16][0]; a1 = qf[k16][1]; a2 = qf[k16][2]; a3 = qf[k16][3];
+                } else {
+                    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+                    ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
+                }
                 const int brow = n8 * 8 + (lane & 7), bcol = k16 * 16 + ((lane >> 3) & 1) * 8;
                 ldmatrix_x2(b0, b1, tbase + swz(brow, bcol, TP));
                 mma_16816(c, a0, a1, a2, a3, b0, b1);
@@ -303,7 +340,16 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_split_kernel(const __grid_co
 }
 
 // Ordered merge of split states:  M = max_s m_s,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s
-__global__ void __launch_bounds__(128) gqa_merge_kernel(const AttnParams P, int D) {
+// One CTA per (sequence, query head).  The split maxima and denominators are read in one
+// parallel round, the weights kept in shared memory, and each thread's sum over splits
+// issues its loads eight at a time.
+constexpr int kMergeThreads = 128;
+constexpr int kMaxSplits = 1024;
+
+__global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const AttnParams P, int D) {
+    __shared__ float wsh[kMaxSplits];
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float s_inv;
     pdl_trigger();
     pdl_wait();
     const int bh = blockIdx.x;
@@ -314,16 +360,38 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const AttnParams P, int 
     const int nt = (T + P.tp - 1) / P.tp;
     const int nsplit = min(P.nsplit_max, nt);
     if (nsplit <= 1) return;
-    const float* base = P.part + (static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max * (D + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, base[s * (D + 2) + D]);
-    float den = 0.f;
-    for (int s = 0; s < nsplit; ++s) den += expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + D + 1];
-    const float inv = 1.f / den;
+    const int stride = D + 2;
+    const float* base = P.part + (static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max * stride;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float m = -INFINITY;
+    for (int s = tid; s < nsplit; s += kMergeThreads) m = fmaxf(m, base[s * stride + D]);
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    float M = red[0];
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+    for (int s = tid; s < nsplit; s += kMergeThreads) wsh[s] = expf(base[s * stride + D] - M);
+    __syncthreads();
+    if (warp == 0) {  // denominator in ascending split order (deterministic)
+        float den = 0.f;
+        for (int s = 0; s < nsplit; ++s) den += wsh[s] * base[s * stride + D + 1];
+        if (lane == 0) s_inv = 1.f / den;
+    }
+    __syncthreads();
+    const float inv = s_inv;
     float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    for (int i = tid; i < D; i += kMergeThreads) {
         float v = 0.f;
-        for (int s = 0; s < nsplit; ++s) v += expf(base[s * (D + 2) + D] - M) * base[s * (D + 2) + i];
+        int s = 0;
+        for (; s + 8 <= nsplit; s += 8) {
+            float a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = base[(s + u) * stride + i];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v += wsh[s + u] * a[u];
+        }
+        for (; s < nsplit; ++s) v += wsh[s] * base[s * stride + i];
         o[i] = v * inv;
     }
 }
@@ -344,6 +412,7 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
     ns = std::min(ns, nt_max);
     const int max_tiles = kMaxSplitSlots / pl.tp;
     if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
+    ns = std::min<int64_t>(ns, kMaxSplits);
     pl.nsplit_max = static_cast<int>(ns);
     pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
@@ -441,8 +510,8 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early) {
     if (pl.nsplit_max > 1) {
         int D = op.d;
         void* margs[] = {&P, &D};
-        st = launch_pdl(reinterpret_cast<const void*>(gqa_merge_kernel), dim3(op.B * op.n_q), dim3(128), 0, stream,
-                        margs);
+        st = launch_pdl(reinterpret_cast<const void*>(gqa_merge_kernel), dim3(op.B * op.n_q), dim3(kMergeThreads), 0,
+                        stream, margs);
     }
     return st;
 }

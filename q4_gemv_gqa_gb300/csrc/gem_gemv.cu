@@ -24,6 +24,7 @@
 // downstream of the QKV projection amplifies.)  No tensor cores: at batch 1..8 the op
 // streams 0.5625 bytes per weight and the budget is instruction issue, not math.
 #include <algorithm>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 
@@ -135,6 +136,12 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
         void* args[] = {&w0, &w1, &N, &K, &p};
         return launch_pdl(fn, grid, dim3(256), 0, stream, args);
     }
+
+    static const bool cuda_cores = [] {
+        const char* e = getenv("GEM_GEMV_CUDA_CORES");
+        return e && e[0] == '1';
+    }();
+    if (!cuda_cores) return gemv_enqueue_mma(op, stream, di);
 
     const int64_t rowbytes = op.K / 32 * 18;
     const int B = op.B;

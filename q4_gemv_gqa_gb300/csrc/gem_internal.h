@@ -55,6 +55,8 @@ struct GemvOp {
 };
 gem_status gemv_check(const GemvOp& op);
 gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream);
+// Tensor-core path (mma.sync) for the TMA-eligible shapes; called by gemv_enqueue.
+gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di);
 
 // ---- norms / RoPE / activation -------------------------------------------------------------
 struct RopeOp {

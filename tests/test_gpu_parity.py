@@ -78,6 +78,8 @@ GEMV_CASES = [
     (67, 256, 1), (67, 256, 2), (67, 256, 3), (67, 256, 4), (67, 256, 5), (67, 256, 6),
     (67, 256, 7), (67, 256, 8), (33, 512, 3), (16, 2048, 1), (4096, 2048, 1), (2048, 6144, 1),
     (6144, 2048, 8), (2560, 9728, 8), (1, 256, 1),
+    (40000, 512, 2), (40000, 512, 6),   # more 16-row units per CTA than one pass holds
+    (300, 21504, 3),                    # long K: several activation phases
 ]
 
 

@@ -131,7 +131,8 @@ GEM_API gem_status gem_rmsnorm_qknorm_rope(float *qkv, int64_t ldqkv, int B, int
  *   For sequence b with p = pos[b] and query head h (KV head g = h / (n_q / n_kv)):
  *     slots   S = {0 .. p} (window == 0) or {0 .. min(window, p + 1) - 1} (ring)
  *     out[b][h*d + i] = sum_{s in S} softmax_s(scale * q_h . K[b][g][s]) * V[b][g][s][i]
- *   q       [B][ldq] fp32, query heads contiguous (head h at column h*d).
+ *   q       [B][ldq] fp32, query heads contiguous (head h at column h*d); q 16-byte
+ *           aligned and ldq % 4 == 0 (else GEM_ERR_MISALIGNED).
  *   caches  [B][n_kv][cache_cap][d] binary16, must already hold the new token's row.
  *   out     [B][ldo] fp32.
  *   d       64, 128, 256 or 512.  n_q % n_kv == 0 and n_q / n_kv <= 8.

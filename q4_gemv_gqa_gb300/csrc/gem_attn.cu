@@ -339,17 +339,261 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid
     }
 }
 
+// ---- per-warp flash variant (d <= 256, G <= 4) -------------------------------------------
+// Each warp of the CTA owns every fourth 16-slot tile of the split and streams its K and V
+// tiles through a private 2-stage TMA ring.  Per tile: S^T = K Q^T on mma (positions are the
+// M rows; the N columns are (head, hi/lo) pairs of the pre-scaled query), an online softmax
+// per head held in registers (head t lives in lane quad position t), P^T through a 384-byte
+// per-warp buffer, and O^T += V^T P^T on mma (head t's hi and lo columns land in the same
+// thread and are summed at the end).  The four warps' states are merged once per CTA.
+constexpr int kFlashTile = 16;
+constexpr int kFlashWarps = 4;
+constexpr int kFlashStages = 2;
+
+struct FlashSmem {
+    static constexpr int kPbufPitch = 24;  // halves per P^T row (16 used; padding avoids bank conflicts)
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                        const __grid_constant__ CUtensorMap tmV,
+                                                                        const AttnParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr int kTileBytes = kFlashTile * D * 2;            // one K or V tile
+    constexpr int kStageBytes = 2 * kTileBytes;               // K + V
+    constexpr int kWarpRing = kFlashStages * kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFlashWarps * kWarpRing);       // [warp][stage]
+    __half* pbuf = reinterpret_cast<__half*>(smem + kFlashWarps * kWarpRing + 128);    // [warp][8][24]
+    float* comb = reinterpret_cast<float*>(smem);             // reuses the ring after the tile loop
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int t_id = threadIdx.x, lane = t_id & 31, warp = t_id >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int G = P.G;
+
+    if (!P.early) pdl_wait();
+    const int p = P.pos[b];
+    const bool bad = p < 0 || (P.window == 0 && static_cast<int64_t>(p) >= P.cap);
+    if (bad) {
+        pdl_trigger();
+        if (P.early) pdl_wait();
+        if (t_id == 0 && split == 0 && g == 0) atomicOr(P.status, GEM_DEVFLAG_POS_RANGE);
+        return;
+    }
+    const int T = P.window ? min(P.window, p + 1) : p + 1;
+    int nsplit, t0, t1;
+    split_range(T, kFlashTile, P.nsplit_max, split, nsplit, t0, t1);
+    if (split >= nsplit) {
+        pdl_trigger();
+        if (P.early) pdl_wait();
+        return;
+    }
+    const int ntile = t1 - t0;
+    const int nmy = ntile > warp ? (ntile - warp + kFlashWarps - 1) / kFlashWarps : 0;  // my tiles
+    const int slot_p = P.window ? p % P.window : p;
+    const int64_t row0 = (static_cast<int64_t>(b) * P.n_kv + g) * P.cap;
+    uint8_t* ring = smem + warp * kWarpRing;
+    uint64_t* wbar = bars + warp * kFlashStages;
+
+    if (lane == 0)
+        for (int i = 0; i < kFlashStages; ++i) mbar_init(&wbar[i], 1);
+    fence_mbar_init();
+    __syncwarp();
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int it) {  // my it-th tile into stage it % kFlashStages (lane 0)
+        const int tile = t0 + warp + it * kFlashWarps;
+        const int st = it % kFlashStages;
+        uint8_t* dst = ring + st * kStageBytes;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&wbar[st], kStageBytes);
+        const int32_t r = static_cast<int32_t>(row0 + static_cast<int64_t>(tile) * kFlashTile);
+        for (int j = 0; j < D / 64; ++j) {
+            tma_load_2d(dst + j * kFlashTile * 128, &tmK, j * 64, r, &wbar[st], policy);
+            tma_load_2d(dst + kTileBytes + j * kFlashTile * 128, &tmV, j * 64, r, &wbar[st], policy);
+        }
+    };
+    const int npre = min(kFlashStages, nmy);
+    if (lane == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        for (int it = 0; it < npre; ++it) issue(it);
+    }
+    pdl_trigger();
+    if (P.early) pdl_wait();
+
+    // Q^T B fragments: column n = 2h + hl (head h = n / 2, hi or lo), k = dims
+    uint32_t qb[D / 16][2];
+    {
+        const int h = gq >> 1, hl = gq & 1;
+        const float* qrow = P.q + b * P.ldq + static_cast<int64_t>(g * G + h) * D;
+        float2 raw[D / 16][2];
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16) {
+            if (h < G) {
+                raw[k16][0] = *reinterpret_cast<const float2*>(qrow + k16 * 16 + 2 * tq);
+                raw[k16][1] = *reinterpret_cast<const float2*>(qrow + k16 * 16 + 2 * tq + 8);
+            } else {
+                raw[k16][0] = raw[k16][1] = make_float2(0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                __half h0, l0, h1, l1;
+                split_hi_lo(raw[k16][r].x * P.scale, h0, l0);
+                split_hi_lo(raw[k16][r].y * P.scale, h1, l1);
+                const __half2 v = hl ? __halves2half2(l0, l1) : __halves2half2(h0, h1);
+                qb[k16][r] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+    }
+
+    float o[D / 16][4];
+#pragma unroll
+    for (int m = 0; m < D / 16; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    const bool head_ok = tq < G;
+    __half* pb = pbuf + warp * 8 * FlashSmem::kPbufPitch;
+    bool ok = true;
+
+    for (int it = 0; it < nmy; ++it) {
+        const int st = it % kFlashStages;
+        const int tile = t0 + warp + it * kFlashWarps;
+        uint8_t* kt = ring + st * kStageBytes;
+        uint8_t* vt = kt + kTileBytes;
+        if (ok) ok = mbar_wait(&wbar[st], static_cast<uint32_t>((it / kFlashStages) & 1), P.status);
+        const int rp = slot_p - tile * kFlashTile;
+        if (it < npre && rp >= 0 && rp < kFlashTile) {  // new row landed after this copy was requested
+            const uint16_t* ks = P.k_cache + (row0 + slot_p) * D;
+            const uint16_t* vs = P.v_cache + (row0 + slot_p) * D;
+            for (int c = lane * 8; c < D; c += 32 * 8) {
+                *reinterpret_cast<uint4*>(kt + swz(rp, c, kFlashTile)) = *reinterpret_cast<const uint4*>(ks + c);
+                *reinterpret_cast<uint4*>(vt + swz(rp, c, kFlashTile)) = *reinterpret_cast<const uint4*>(vs + c);
+            }
+        }
+        const int valid = T - tile * kFlashTile;  // rows >= valid belong to other slots
+        if (valid < kFlashTile)
+            for (int e = lane * 8; e < (kFlashTile - valid) * D; e += 32 * 8) {
+                const int r = valid + e / D, c = e % D;
+                *reinterpret_cast<uint4*>(vt + swz(r, c, kFlashTile)) = make_uint4(0, 0, 0, 0);
+            }
+        __syncwarp();
+        // S^T = K Q^T
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t kb = smem_u32(kt);
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16) {
+            uint32_t a0, a1, a2, a3;
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+            ldmatrix_x4(a0, a1, a2, a3, kb + swz(arow, acol, kFlashTile));
+            mma_16816(c, a0, a1, a2, a3, qb[k16][0], qb[k16][1]);
+        }
+        // head tq at positions gq and gq + 8
+        float s0 = c[0] + c[1], s1 = c[2] + c[3];
+        if (gq >= valid) s0 = -INFINITY;
+        if (gq + 8 >= valid) s1 = -INFINITY;
+        if (!head_ok) s0 = s1 = 0.f;
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m_run, mx);          // finite: row 0 of a tile is always valid
+        const float corr = expf(m_run - m_new);         // 0 on the first tile
+        const float p0 = expf(s0 - m_new), p1 = expf(s1 - m_new);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l_run = l_run * corr + ps;
+        m_run = m_new;
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            o[m][0] *= corr; o[m][1] *= corr; o[m][2] *= corr; o[m][3] *= corr;
+        }
+        // P^T rows: column 2*tq (hi), 2*tq + 1 (lo); positions gq and gq + 8
+        {
+            __half h0, l0, h1, l1;
+            split_hi_lo(p0, h0, l0);
+            split_hi_lo(p1, h1, l1);
+            pb[(2 * tq) * FlashSmem::kPbufPitch + gq] = h0;
+            pb[(2 * tq + 1) * FlashSmem::kPbufPitch + gq] = l0;
+            pb[(2 * tq) * FlashSmem::kPbufPitch + gq + 8] = h1;
+            pb[(2 * tq + 1) * FlashSmem::kPbufPitch + gq + 8] = l1;
+        }
+        __syncwarp();
+        uint32_t pb0, pb1;
+        {
+            const int n = lane & 7, kk = ((lane >> 3) & 1) * 8;
+            ldmatrix_x2(pb0, pb1, smem_u32(pb + n * FlashSmem::kPbufPitch + kk));
+        }
+        // O^T += V^T P^T
+        const uint32_t vb = smem_u32(vt);
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            uint32_t a0, a1, a2, a3;
+            const int vrow = (lane & 7) + (lane >> 4) * 8, vcol = m * 16 + ((lane >> 3) & 1) * 8;
+            ldmatrix_x4_trans(a0, a1, a2, a3, vb + swz(vrow, vcol, kFlashTile));
+            mma_16816(o[m], a0, a1, a2, a3, pb0, pb1);
+        }
+        __syncwarp();
+        if (lane == 0 && it + kFlashStages < nmy) issue(it + kFlashStages);
+    }
+    if (!ok && lane == 0) drain_stages(wbar, kFlashStages, max(0, nmy - kFlashStages), nmy - 1);
+
+    // ---- merge the four warps' states (ascending warp order) --------------------------------
+    __syncthreads();  // all rings idle: reuse them for the combine buffers
+    float* cm = comb;                                    // [warp][4] max
+    float* cl = comb + kFlashWarps * 4;                  // [warp][4] denominators
+    float* co = comb + 2 * kFlashWarps * 4;              // [warp][4][D] outputs
+    if (gq == 0 && head_ok) {
+        cm[warp * 4 + tq] = nmy ? m_run : -INFINITY;
+        cl[warp * 4 + tq] = nmy ? l_run : 0.f;
+    }
+    if (head_ok) {
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            co[(warp * 4 + tq) * D + m * 16 + gq] = o[m][0] + o[m][1];
+            co[(warp * 4 + tq) * D + m * 16 + gq + 8] = o[m][2] + o[m][3];
+        }
+    }
+    __syncthreads();
+    for (int e = t_id; e < G * D; e += kFlashWarps * 32) {
+        const int h = e / D, i = e - h * D;
+        float M = -INFINITY;
+        for (int w = 0; w < kFlashWarps; ++w) M = fmaxf(M, cm[w * 4 + h]);
+        float L = 0.f, O = 0.f;
+        for (int w = 0; w < kFlashWarps; ++w) {
+            const float f = expf(cm[w * 4 + h] - M);   // warps without tiles: e^-inf = 0
+            L += f * cl[w * 4 + h];
+            O += f * co[(w * 4 + h) * D + i];
+        }
+        const int hg = g * G + h;
+        if (nsplit == 1) {
+            P.out[b * P.ldo + static_cast<int64_t>(hg) * D + i] = O / L;
+        } else {
+            float* dst = P.part + ((static_cast<int64_t>(b) * P.n_q + hg) * P.nsplit_max + split) * (D + 2);
+            dst[i] = O;
+            if (i == 0) {
+                dst[D] = M;
+                dst[D + 1] = L;
+            }
+        }
+    }
+}
+
 // Ordered merge of split states:  M = max_s m_s,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s
-// One CTA per (sequence, query head).  The split maxima and denominators are read in one
-// parallel round, the weights kept in shared memory, and each thread's sum over splits
-// issues its loads eight at a time.
-constexpr int kMergeThreads = 128;
+// One CTA per (sequence, query head).  Every global load is issued in one parallel round:
+// split maxima and denominators into shared memory, then the split sums of the outputs,
+// spread over kMergeGroups thread groups (each summing every kMergeGroups-th split in
+// ascending order) and combined in a fixed order, so the result is deterministic.
+constexpr int kMergeThreads = 512;
 constexpr int kMaxSplits = 1024;
 
 __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const AttnParams P, int D) {
-    __shared__ float wsh[kMaxSplits];
+    __shared__ float wsh[kMaxSplits], lsh[kMaxSplits];
+    __shared__ float psum[kMergeThreads];
     __shared__ float red[kMergeThreads / 32];
-    __shared__ float s_inv;
     pdl_trigger();
     pdl_wait();
     const int bh = blockIdx.x;
@@ -364,57 +608,80 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const AttnPara
     const float* base = P.part + (static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max * stride;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float m = -INFINITY;
-    for (int s = tid; s < nsplit; s += kMergeThreads) m = fmaxf(m, base[s * stride + D]);
+    for (int s = tid; s < nsplit; s += kMergeThreads) {
+        const float ms = base[s * stride + D];
+        wsh[s] = ms;
+        lsh[s] = base[s * stride + D + 1];
+        m = fmaxf(m, ms);
+    }
     m = warp_max(m);
     if (lane == 0) red[warp] = m;
     __syncthreads();
     float M = red[0];
     for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+    for (int s = tid; s < nsplit; s += kMergeThreads) wsh[s] = expf(wsh[s] - M);
     __syncthreads();
-    for (int s = tid; s < nsplit; s += kMergeThreads) wsh[s] = expf(base[s * stride + D] - M);
-    __syncthreads();
-    if (warp == 0) {  // denominator in ascending split order (deterministic)
-        float den = 0.f;
-        for (int s = 0; s < nsplit; ++s) den += wsh[s] * base[s * stride + D + 1];
-        if (lane == 0) s_inv = 1.f / den;
-    }
-    __syncthreads();
-    const float inv = s_inv;
-    float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
-    for (int i = tid; i < D; i += kMergeThreads) {
-        float v = 0.f;
-        int s = 0;
-        for (; s + 8 <= nsplit; s += 8) {
+    // output partial sums: group q handles splits q, q + ngroups, ... for dims i < D
+    const int ngroups = kMergeThreads / D;  // D <= 512
+    const int q = tid / D, i = tid - q * D;
+    float v = 0.f;
+    if (q < ngroups) {
+        int s = q;
+        for (; s + 7 * ngroups < nsplit; s += 8 * ngroups) {
             float a[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) a[u] = base[(s + u) * stride + i];
+            for (int u = 0; u < 8; ++u) a[u] = base[(s + u * ngroups) * stride + i];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v += wsh[s + u] * a[u];
+            for (int u = 0; u < 8; ++u) v += wsh[s + u * ngroups] * a[u];
         }
-        for (; s < nsplit; ++s) v += wsh[s] * base[s * stride + i];
-        o[i] = v * inv;
+        for (; s < nsplit; s += ngroups) v += wsh[s] * base[s * stride + i];
+    }
+    psum[tid] = v;
+    if (warp == 0) {  // denominator in ascending split order
+        float den = 0.f;
+        for (int s = lane; s < nsplit; s += 32) den += wsh[s] * lsh[s];
+        den = warp_sum(den);
+        if (lane == 0) red[0] = den;
+    }
+    __syncthreads();
+    if (tid < D) {
+        float o = 0.f;
+        for (int g2 = 0; g2 < ngroups; ++g2) o += psum[g2 * D + tid];
+        P.out[b * P.ldo + static_cast<int64_t>(h) * D + tid] = o / red[0];
     }
 }
 
 struct Plan {
+    bool flash;
     int tp, nsplit_max, ltile, ns;
     uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off;
     size_t smem, ws;
 };
 
+bool use_flash(int n_q, int n_kv, int d) { return d <= 256 && n_q / n_kv <= 4; }
+
 Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num_sms) {
     Plan pl{};
-    pl.tp = tile_slots(d);
+    pl.flash = use_flash(n_q, n_kv, d);
+    pl.tp = pl.flash ? kFlashTile : tile_slots(d);
     const int64_t tmax = window ? std::min<int64_t>(window, cap) : cap;
     const int64_t nt_max = std::max<int64_t>(1, (tmax + pl.tp - 1) / pl.tp);
     const int64_t target = 2LL * num_sms;
     int64_t ns = std::max<int64_t>(1, (target + static_cast<int64_t>(B) * n_kv - 1) / (static_cast<int64_t>(B) * n_kv));
     ns = std::min(ns, nt_max);
-    const int max_tiles = kMaxSplitSlots / pl.tp;
-    if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
+    if (!pl.flash) {
+        const int max_tiles = kMaxSplitSlots / pl.tp;
+        if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
+    }
     ns = std::min<int64_t>(ns, kMaxSplits);
     pl.nsplit_max = static_cast<int>(ns);
     pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
+    pl.ws = static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
+    if (pl.flash) {
+        const size_t ring = static_cast<size_t>(kFlashWarps) * kFlashStages * 2 * kFlashTile * d * 2;
+        pl.smem = align_up(ring + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2, 1024) + 1024;
+        return pl;
+    }
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
     pl.ns = d >= 512 ? 3 : 4;
     pl.ns = static_cast<int>(std::min<int64_t>(pl.ns, 2 * pl.ltile));
@@ -432,12 +699,18 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
     pl.st_off = static_cast<uint32_t>(off);
     off += 16 * 4;
     pl.smem = align_up(off, 1024) + 1024;
-    pl.ws = static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
     return pl;
 }
 
 using SplitKernel = void (*)(CUtensorMap, CUtensorMap, AttnParams);
-SplitKernel pick(int d) {
+SplitKernel pick(int d, bool flash) {
+    if (flash) {
+        switch (d) {
+            case 64: return gqa_flash_kernel<64>;
+            case 128: return gqa_flash_kernel<128>;
+            default: return gqa_flash_kernel<256>;
+        }
+    }
     switch (d) {
         case 64: return gqa_split_kernel<64>;
         case 128: return gqa_split_kernel<128>;
@@ -502,11 +775,12 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early) {
     if ((st = make_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, op.v_cache, op.d, rows,
                                  static_cast<uint64_t>(op.d) * 2, 64, pl.tp, CU_TENSOR_MAP_SWIZZLE_128B)) != GEM_OK)
         return st;
-    const void* fn = reinterpret_cast<const void*>(pick(op.d));
+    const void* fn = reinterpret_cast<const void*>(pick(op.d, pl.flash));
     if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
     dim3 grid(pl.nsplit_max, op.n_kv, op.B);
     void* args[] = {&tmK, &tmV, &P};
-    if ((st = launch_pdl(fn, grid, dim3(kAttnThreads), pl.smem, stream, args)) != GEM_OK) return st;
+    if ((st = launch_pdl(fn, grid, dim3(pl.flash ? kFlashWarps * 32 : kAttnThreads), pl.smem, stream, args)) != GEM_OK)
+        return st;
     if (pl.nsplit_max > 1) {
         int D = op.d;
         void* margs[] = {&P, &D};
@@ -538,6 +812,7 @@ gem_status attn_check(const AttnOp& op) {
         return GEM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(op.k_cache) | reinterpret_cast<uintptr_t>(op.v_cache)) & 15)
         return GEM_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(op.q) & 15) || (op.ldq & 3)) return GEM_ERR_MISALIGNED;  // vector loads of q
     if (static_cast<uint64_t>(op.B) * op.n_kv * op.cache_cap >= (1ull << 31)) return GEM_ERR_UNSUPPORTED_SHAPE;
     return GEM_OK;
 }

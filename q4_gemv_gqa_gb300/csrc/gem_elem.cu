@@ -2,6 +2,8 @@
 // per-head QK-norm + NeoX/partial RoPE + binary16 KV append, the gated FFN activation and
 // the post-norm residual add.  All are memory-trivial (a few KB per token); they exist as
 // separate launches only where a grid-wide reduction separates them from a matvec.
+#include <cmath>
+
 #include "gem_device.cuh"
 
 namespace gem {
@@ -71,22 +73,50 @@ __global__ void swiglu_kernel(const float* __restrict__ gate, const float* __res
 constexpr int kRopeWarps = 4;
 constexpr int kMaxHeadDim = 512;
 
-__global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const RopeOp op) {
+// Rotation frequencies theta^(-2i/R), i < R/2, computed on the host in fp64.
+struct RopeFreq {
+    double w[kMaxHeadDim / 2];
+};
+
+// cos and sin of p * w in fp32 from an fp64 angle: the angle is reduced to [-pi, pi] with a
+// two-part 2*pi (Cody and Waite's additive argument reduction), which keeps the reduced
+// angle exact to ~1e-13 for the positions of a decode cache; fp32 sincosf is then accurate.
+__device__ __forceinline__ void rope_cos_sin(double ang, float& c, float& s) {
+    const double two_pi_hi = 6.283185307179586;        // 2*pi rounded to double
+    const double two_pi_lo = 2.4492935982947064e-16;   // 2*pi - two_pi_hi
+    const double k = rint(ang * 0.15915494309189535);  // ang / (2*pi)
+    double r = fma(-k, two_pi_hi, ang);
+    r = fma(-k, two_pi_lo, r);
+    sincosf(static_cast<float>(r), &s, &c);
+}
+
+__global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const RopeOp op, const RopeFreq fr, int early) {
     __shared__ float buf[kRopeWarps][kMaxHeadDim];
+    __shared__ float cs_tab[kMaxHeadDim / 2], sn_tab[kMaxHeadDim / 2];
     pdl_trigger();
-    pdl_wait();
+    if (!early) pdl_wait();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int b = blockIdx.y;
-    const int head = blockIdx.x * kRopeWarps + w;
-    const int nheads = op.n_q + op.n_kv;
-    if (head >= nheads) return;
     const int d = op.d;
     const int p = op.pos[b];
     const bool bad = p < 0 || (op.window == 0 && static_cast<int64_t>(p) >= op.cache_cap);
     if (bad) {
-        if (lane == 0 && head == 0) atomicOr(op.status, GEM_DEVFLAG_POS_RANGE);
+        if (early) pdl_wait();
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(op.status, GEM_DEVFLAG_POS_RANGE);
         return;
     }
+    const int R = op.rope_dim, half = R / 2;
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        float c, s;
+        rope_cos_sin(static_cast<double>(p) * fr.w[i], c, s);
+        cs_tab[i] = c;
+        sn_tab[i] = s;
+    }
+    if (early) pdl_wait();  // q/k/v rows come from the preceding projection
+    __syncthreads();
+    const int head = blockIdx.x * kRopeWarps + w;
+    const int nheads = op.n_q + op.n_kv;
+    if (head >= nheads) return;
     const bool is_q = head < op.n_q;
     const int j = is_q ? head : head - op.n_q;  // KV head index
     float* row = op.qkv + b * op.ldqkv + static_cast<int64_t>(head) * d;
@@ -117,16 +147,11 @@ __global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const Rope
         for (int e = lane; e < d; e += 32) sb[e] = sb[e] * r * gamma[e];
     }
     __syncwarp();
-    const int R = op.rope_dim, half = R / 2;
-    const double ln_theta = log(static_cast<double>(op.theta));
     for (int e = lane; e < d; e += 32) {
         float v = sb[e];
         if (e < R) {
             const int i = e < half ? e : e - half;
-            const double ang = static_cast<double>(p) * exp(-2.0 * static_cast<double>(i) / R * ln_theta);
-            double sn, cs;
-            sincos(ang, &sn, &cs);
-            const float c = static_cast<float>(cs), s = static_cast<float>(sn);
+            const float c = cs_tab[i], s = sn_tab[i];
             v = e < half ? fmaf(sb[e], c, -sb[e + half] * s) : fmaf(sb[e - half], s, sb[e] * c);
         }
         row[e] = v;
@@ -180,7 +205,8 @@ gem_status rope_check(const RopeOp& op) {
     return GEM_OK;
 }
 
-gem_status rope_enqueue(const RopeOp& op_in, cudaStream_t stream) {
+namespace {
+gem_status rope_launch(const RopeOp& op_in, cudaStream_t stream, int early) {
     gem_status st = rope_check(op_in);
     if (st != GEM_OK || op_in.B == 0 || op_in.n_q + op_in.n_kv == 0) return st;
     RopeOp op = op_in;
@@ -189,11 +215,18 @@ gem_status rope_enqueue(const RopeOp& op_in, cudaStream_t stream) {
         if ((st = device_info(&di)) != GEM_OK) return st;
         op.status = di.status_word;
     }
+    RopeFreq fr{};
+    for (int i = 0; i < op.rope_dim / 2; ++i)
+        fr.w[i] = std::pow(static_cast<double>(op.theta), -2.0 * i / op.rope_dim);
     dim3 grid((op.n_q + op.n_kv + kRopeWarps - 1) / kRopeWarps, op.B);
-    void* args[] = {&op};
+    void* args[] = {&op, &fr, &early};
     return launch_pdl(reinterpret_cast<const void*>(qknorm_rope_kernel), grid, dim3(kRopeWarps * 32), 0, stream,
                       args);
 }
+}  // namespace
+
+gem_status rope_enqueue(const RopeOp& op, cudaStream_t stream) { return rope_launch(op, stream, 0); }
+gem_status rope_enqueue_in_chain(const RopeOp& op, cudaStream_t stream) { return rope_launch(op, stream, 1); }
 
 }  // namespace gem
 

@@ -75,6 +75,9 @@ struct RopeOp {
 };
 gem_status rope_check(const RopeOp& op);
 gem_status rope_enqueue(const RopeOp& op, cudaStream_t stream);
+// Same, inside a layer chain: positions are read before griddepcontrol.wait (the preceding
+// kernel does not write them), so the rotation table is built while it still runs.
+gem_status rope_enqueue_in_chain(const RopeOp& op, cudaStream_t stream);
 
 gem_status rmsnorm_enqueue(const float* x, int B, int64_t H, const float* gamma, float eps, float* out,
                            cudaStream_t stream);

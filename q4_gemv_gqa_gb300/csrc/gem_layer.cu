@@ -134,7 +134,7 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
         return st;
 
     if ((st = gemv_enqueue(qkv, stream)) != GEM_OK) return st;
-    if ((st = rope_enqueue(rope, stream)) != GEM_OK) return st;
+    if ((st = rope_enqueue_in_chain(rope, stream)) != GEM_OK) return st;
     if ((st = attn_enqueue_in_chain(attn, stream)) != GEM_OK) return st;
     if ((st = gemv_enqueue(oproj, stream)) != GEM_OK) return st;
     if (L->post_norms && (st = postnorm_residual_enqueue(x, w.tmp, B, H, L->g_post_attn, L->eps, stream)) != GEM_OK)

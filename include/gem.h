@@ -150,6 +150,38 @@ GEM_API gem_status gem_gqa_decode_attn(const float *q, int64_t ldq, const uint16
                                int32_t *status, void *stream);
 
 /*
+ * gem_gqa_decode_attn without a caller-supplied workspace: the split partials live in a
+ * fixed array inside the library, so the call allocates no device memory at all (no
+ * cudaMalloc/cudaFree, no allocating library routine).  The decode-attention pages have no
+ * counterpart of this entry point; it exists for callers that cannot allocate:
+ *   - programs that have handed all device memory to their own arena (weights plus a KV cache
+ *     sized to fill HBM), where a new allocation could fail in the middle of decoding;
+ *   - serving loops that must not call cudaMalloc/cudaFree per step, since those calls can
+ *     synchronise the device and stall the other streams;
+ *   - plain C callers that have no device allocator of their own for a scratch buffer.
+ * Arguments, results and errors are those of gem_gqa_decode_attn (same kernels, same split
+ * plan, so the output is bit-identical to that call's), except:
+ *   - the split partials need gem_gqa_decode_attn_workspace() bytes for the same shape; when
+ *     that exceeds GEM_ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) the call launches nothing and
+ *     returns GEM_ERR_WORKSPACE.  (On a 152-SM GPU every supported shape with
+ *     B * n_kv <= 152 fits; the largest such need is about 7.5 MB.)
+ *   - the array exists once per device and every call on that device shares it.  Calls issued
+ *     in order on one stream are safe; two calls that can run at the same time on one device
+ *     (different streams, or different host threads with different streams) race on the
+ *     array and corrupt each other's outputs.  No part of the array has to start at zero.
+ *   - the first call on each device (with that device current) does the set-up: it looks up
+ *     the array's device address and sets the kernels' shared-memory limit.  Make that first
+ *     call before any stream capture begins.
+ */
+#define GEM_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+GEM_API gem_status gem_gqa_decode_attn_noalloc(const float *q, int64_t ldq,
+                                               const uint16_t *k_cache, const uint16_t *v_cache,
+                                               int B, int n_q, int n_kv, int d,
+                                               int64_t cache_cap, const int32_t *pos, int window,
+                                               float scale, float *out, int64_t ldo,
+                                               int32_t *status, void *stream);
+
+/*
  * Gated FFN activation  [GELO] 04/05 (Qwen3 SwiGLU; Gemma gelu_pytorch_tanh).
  *   out = act(gate) * up,  act 0: silu(g) = g / (1 + e^-g);
  *                          act 1: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).

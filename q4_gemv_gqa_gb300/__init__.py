@@ -134,6 +134,29 @@ def gqa_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     return out
 
 
+NOALLOC_SCRATCH_BYTES = 8 << 20  # GEM_ATTN_NOALLOC_SCRATCH_BYTES
+
+
+def gqa_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            n_q: int, n_kv: int, d: int, pos: torch.Tensor, window: int,
+                            scale: float, out: torch.Tensor, status: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """gqa_decode_attn with the split partials in the library's own per-device array.
+
+    For callers that must not allocate device memory while decoding.  Allocates nothing;
+    calls that may run concurrently on one device race on the shared array; shapes whose
+    partials exceed NOALLOC_SCRATCH_BYTES raise GemError (GEM_ERR_WORKSPACE)."""
+    B = q.shape[0]
+    cap = k_cache.shape[2]
+    st = lib.gem_gqa_decode_attn_noalloc(
+        _dev(q, torch.float32, "q"), q.shape[-1], _dev(k_cache, _HALF_BITS, "k_cache"),
+        _dev(v_cache, _HALF_BITS, "v_cache"), B, n_q, n_kv, d, cap,
+        _dev(pos, torch.int32, "pos"), window, scale, _dev(out, torch.float32, "out"),
+        out.shape[-1], _dev(status, torch.int32, "status"), _stream(stream))
+    _check(st, "gem_gqa_decode_attn_noalloc")
+    return out
+
+
 def swiglu(gate: torch.Tensor, up: torch.Tensor, act: int, out: torch.Tensor,
            stream=None) -> torch.Tensor:
     B = gate.shape[0] if gate.dim() == 2 else 1

@@ -39,6 +39,8 @@ PROTOTYPES = {
     "gem_gqa_decode_attn_workspace": (C.c_size_t, [i32, i32, i32, i32, i64, i32]),
     "gem_gqa_decode_attn": (i32, [p, i64, p, p, i32, i32, i32, i32, i64, p, i32, C.c_float,
                                   p, i64, p, C.c_size_t, p, p]),
+    "gem_gqa_decode_attn_noalloc": (i32, [p, i64, p, p, i32, i32, i32, i32, i64, p, i32,
+                                          C.c_float, p, i64, p, p]),
     "gem_swiglu": (i32, [p, p, i32, i64, i32, p, p]),
     "gem_decode_layer_workspace": (C.c_size_t, [C.POINTER(LayerDesc), i32, i64]),
     "gem_decode_layer": (i32, [C.POINTER(LayerDesc), i32, p, p, p, i64, p, p, C.c_size_t, p, p]),

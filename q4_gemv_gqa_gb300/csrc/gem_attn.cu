@@ -820,6 +820,36 @@ gem_status attn_check(const AttnOp& op) {
 gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, false); }
 gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true); }
 
+// ---- split-partial scratch owned by the library (gem_gqa_decode_attn_noalloc) --------------
+// One fixed array per device (a module-scope __device__ variable exists once in every device
+// context), shared by all calls on that device.  The split kernels write every partial state
+// that the merge kernel then reads, so no part of it has to start at zero.
+static __device__ __align__(256) float g_attn_noalloc_scratch[GEM_ATTN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoallocMaxDevices];
+}  // namespace
+
+// Device address of the current device's scratch array, looked up on the first call made
+// with that device current (the look-up is the only set-up; it allocates nothing).
+gem_status noalloc_scratch(void** out) {
+    int dev = 0;
+    GEM_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kNoallocMaxDevices) return GEM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (!p) return cuda_fail(cudaErrorInvalidSymbol);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return GEM_OK;
+}
+
 }  // namespace gem
 
 extern "C" {
@@ -850,6 +880,37 @@ gem_status gem_gqa_decode_attn(const float* q, int64_t ldq, const uint16_t* k_ca
     op.workspace = workspace;
     op.ws_bytes = ws_bytes;
     op.status = status;
+    return gem::attn_enqueue(op, static_cast<cudaStream_t>(stream));
+}
+
+gem_status gem_gqa_decode_attn_noalloc(const float* q, int64_t ldq, const uint16_t* k_cache,
+                                       const uint16_t* v_cache, int B, int n_q, int n_kv, int d,
+                                       int64_t cache_cap, const int32_t* pos, int window, float scale,
+                                       float* out, int64_t ldo, int32_t* status, void* stream) {
+    gem::AttnOp op{};
+    op.q = q;
+    op.ldq = ldq;
+    op.k_cache = k_cache;
+    op.v_cache = v_cache;
+    op.B = B;
+    op.n_q = n_q;
+    op.n_kv = n_kv;
+    op.d = d;
+    op.cache_cap = cache_cap;
+    op.pos = pos;
+    op.window = window;
+    op.scale = scale;
+    op.out = out;
+    op.ldo = ldo;
+    op.status = status;
+    gem_status st = gem::attn_check(op);
+    if (st != GEM_OK || B == 0 || n_q == 0) return st;
+    void* scratch = nullptr;
+    if ((st = gem::noalloc_scratch(&scratch)) != GEM_OK) return st;
+    const size_t need = gem::attn_workspace_bytes(B, n_q, n_kv, d, cache_cap, window);
+    if (need > GEM_ATTN_NOALLOC_SCRATCH_BYTES) return GEM_ERR_WORKSPACE;
+    op.workspace = scratch;
+    op.ws_bytes = GEM_ATTN_NOALLOC_SCRATCH_BYTES;
     return gem::attn_enqueue(op, static_cast<cudaStream_t>(stream));
 }
 

@@ -10,8 +10,6 @@ namespace {
 
 using namespace gemv_mma;
 
-constexpr size_t kXfMax = 48 * 1024;   // activation fragments of one K-phase
-
 const void* pick(bool packed, int nmat) {
     if (packed) return nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_mma_kernel<true, 2>)
                                  : reinterpret_cast<const void*>(q4_0_gemv_mma_kernel<true, 1>);
@@ -54,53 +52,72 @@ gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceI
     p.U = static_cast<int>((op.N + kUnitRows - 1) / kUnitRows);
     const int C = std::min(di.num_sms, p.U);
     const int umax = (p.U + C - 1) / C;
-    p.up = std::max(1, std::min(umax, kMaxConsumerWarps / (2 * nmat)));
-    int gps = std::max(1, std::min(p.G, kMaxConsumerWarps / (2 * nmat * p.up)));
-    const int stages_for = (p.G + gps - 1) / gps;
-    gps = (p.G + stages_for - 1) / stages_for;   // same stage count, even split
-    p.gps = gps;
-    p.spp = (p.G + gps - 1) / gps;
-    p.ncw = 2 * nmat * p.up * gps;
-    p.stage_bytes = static_cast<uint32_t>(nmat) * p.up * gps * kBoxBytes;
-    const int nct = p.ncw * 32;
-    // K-phase: as much of K as the fragment area and the register prefetch hold
-    const int step = 256 * gps;
-    const int64_t cap_xf = static_cast<int64_t>(kXfMax) / (4 * B);
-    const int64_t cap_pf = static_cast<int64_t>(kPrefetchF4) * nct * 4 / B;
-    int64_t kp = std::min<int64_t>({cap_xf, cap_pf, static_cast<int64_t>(p.spp) * step});
-    kp = std::max<int64_t>(step, kp / step * step);
-    p.kp = static_cast<int>(kp);
-    p.nphase = static_cast<int>((static_cast<int64_t>(p.spp) * step + kp - 1) / kp);
-    const int nph = 2 * gps;
-    const int rows_in_pass = nmat * p.up * kUnitRows;
-    const size_t xf_bytes = 4ull * B * p.kp;
-    const size_t xsc_bytes = static_cast<size_t>(p.kp / 128) * B * 4;
+
+    // Shared memory for phases of gps groups, `up` units per pass and ns ring slots.
     const size_t ssq_bytes = static_cast<size_t>(B) * 2 * p.G * 4;
-    const size_t red_bytes = static_cast<size_t>(rows_in_pass) * nph * B * 4;
-    const size_t other = align_up(xf_bytes, 128) + align_up(xsc_bytes, 128) + align_up(ssq_bytes, 128) +
-                         align_up(red_bytes, 128) + 128 + 2 * 8 * 8 + 128;
-    const int total_stages = ((umax + p.up - 1) / p.up) * p.spp;
-    int ns = static_cast<int>((kSmemBudget > other ? kSmemBudget - other : 0) / p.stage_bytes);
-    ns = std::max(2, std::min(ns, std::min(total_stages, 8)));
-    ns = std::min(ns, total_stages);
-    p.ns = std::max(1, ns);
-    size_t off = align_up(static_cast<size_t>(p.ns) * p.stage_bytes, 128);
-    p.full_off = static_cast<uint32_t>(off);
-    off += 8 * 8;
-    p.empty_off = static_cast<uint32_t>(off);
-    off = align_up(off + 8 * 8, 128);
-    p.xf_off = static_cast<uint32_t>(off);
-    off = align_up(off + xf_bytes, 128);
-    p.xsc_off = static_cast<uint32_t>(off);
-    off = align_up(off + xsc_bytes, 128);
-    p.ssq_off = static_cast<uint32_t>(off);
-    off = align_up(off + ssq_bytes, 128);
-    p.red_off = static_cast<uint32_t>(off);
-    off = align_up(off + red_bytes, 128);
-    p.rstd_off = static_cast<uint32_t>(off);
-    off += 8 * 4;
-    const size_t smem = align_up(off, 128);
-    if (smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
+    // Activation fragments of every phase stay resident when they are small (4 B * K bytes).
+    const bool resident = 4ull * B * p.G * 256 <= kResidentX;
+    auto nbuf_of = [&](int gps) { return resident ? (p.G + gps - 1) / gps : 2; };
+    auto layout = [&](int gps, int up, int ns, bool commit) -> size_t {
+        const size_t stage = static_cast<size_t>(gps) * kBoxBytes;
+        const size_t xf = 4ull * B * gps * 256;
+        const size_t xsc = static_cast<size_t>(gps) * 2 * B * 4;
+        const int nbuf = nbuf_of(gps);
+        const size_t red = static_cast<size_t>(nmat) * up * kUnitRows * (2 * gps) * B * 4;
+        size_t off = align_up(static_cast<size_t>(ns) * stage, 128);
+        const size_t full_off = off;
+        off += kMaxSlots * 8;
+        const size_t empty_off = off;
+        off = align_up(off + kMaxSlots * 8, 128);
+        const size_t xf_off = off;
+        off = align_up(off + nbuf * xf, 128);
+        const size_t xsc_off = off;
+        off = align_up(off + nbuf * xsc, 128);
+        const size_t ssq_off = off;
+        off = align_up(off + ssq_bytes, 128);
+        const size_t red_off = off;
+        off = align_up(off + red, 128);
+        const size_t rstd_off = off;
+        off += 8 * 4;
+        if (commit) {
+            p.stage_bytes = static_cast<uint32_t>(stage);
+            p.full_off = static_cast<uint32_t>(full_off);
+            p.empty_off = static_cast<uint32_t>(empty_off);
+            p.xf_off = static_cast<uint32_t>(xf_off);
+            p.xf_bytes = static_cast<uint32_t>(xf);
+            p.xsc_off = static_cast<uint32_t>(xsc_off);
+            p.ssq_off = static_cast<uint32_t>(ssq_off);
+            p.red_off = static_cast<uint32_t>(red_off);
+            p.rstd_off = static_cast<uint32_t>(rstd_off);
+        }
+        return align_up(off, 128);
+    };
+    // Phase width: up to kMaxConsumerWarps / 2 groups (one consumer warp per half group), as
+    // wide as possible for long contiguous runs per row, split evenly over K.  Then all of a
+    // CTA's units in one pass if the partial-sum area allows, and as many ring slots as fit
+    // (at least min(4, stages)).
+    const size_t budget = std::min<size_t>(kSmemBudget, di.smem_optin);
+    const int nphase = (p.G + kMaxConsumerWarps / 2 - 1) / (kMaxConsumerWarps / 2);
+    int gps = (p.G + nphase - 1) / nphase;
+    int up = umax, ns = 0;
+    for (;; ) {
+        const int stages = std::max(1, nmat * std::min(up, umax) * ((p.G + gps - 1) / gps));
+        const int want = std::min(4, stages);
+        ns = 0;
+        for (int n = std::min(kMaxSlots, stages); n >= want && !ns; --n)
+            if (layout(gps, up, n, false) <= budget) ns = n;
+        if (ns) break;
+        if (up > 1) up = (up + 1) / 2;
+        else if (gps > 1) --gps;
+        else return GEM_ERR_UNSUPPORTED_SHAPE;
+    }
+    p.up = up;
+    p.gps = gps;
+    p.nphase = (p.G + gps - 1) / gps;
+    p.ns = ns;
+    p.ncw = 2 * gps;
+    p.nbuf = nbuf_of(gps);
+    const size_t smem = layout(gps, up, ns, true);
 
     const int64_t rowbytes = op.K / 32 * 18;
     CUtensorMap tm0, tm1;

@@ -9,12 +9,18 @@
 // binary16 pairs (two columns of B, or two mma per k-step for B > 4), scaled per 128
 // elements by a power of two so any fp32 range is safe, so products keep ~22 bits.
 //
-// Work split.  A CTA owns 16-row units; a consumer warp owns one (group phase, matrix,
-// unit, half group) task: 16 rows x 4 blocks (128 weights) of every stage.  A producer warp
-// streams 16-row x 144-byte TMA boxes into a ring guarded by full / empty mbarriers, so
-// consumer warps never wait on each other except at the (few) activation-phase switches.
-// Activations for a K-phase are converted once per CTA into mma B fragments in shared
-// memory; the next phase's raw activations are prefetched into registers meanwhile.
+// Work split.  A CTA owns a contiguous range of 16-row units; one matrix's 16 rows of one
+// unit form a "row block".  K is walked in phases of `gps` groups (gps * 256 weights).  A
+// ring stage holds one row block's `gps` consecutive groups (gps TMA boxes of 16 rows x
+// 144 bytes): every row is read in runs of gps * 144 bytes (about 1 KB), which the HBM
+// streams near its copy rate, where runs of 144 bytes per row reach less than half of it.
+// The producer warp issues stages in (pass, phase, unit, matrix) order into a circular
+// ring of `ns` slots.  Consumer warp w owns half group w of every stage (group w / 2,
+// half w % 2: 16 rows x 128 weights), so all 2 * gps consumer warps walk the ring in
+// order, and it adds its two per-row partial sums into a shared-memory slot of its own
+// after each stage.  Activations of a phase are converted once per CTA into mma B
+// fragments, double-buffered: phase ph + 1 is converted while phase ph's stages stream,
+// so the warps meet at one barrier per phase.
 #pragma once
 
 #include "gem_device.cuh"
@@ -25,10 +31,12 @@ namespace gemv_mma {
 constexpr int kGroupBytes = 144;
 constexpr int kUnitRows = 16;
 constexpr int kBoxBytes = kGroupBytes * kUnitRows;
-constexpr int kMaxConsumerWarps = 20;
+constexpr int kMaxConsumerWarps = 18;
+constexpr int kMaxSlots = 32;                     // ring slots
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kPrefetchF4 = 2;                    // raw activation float4s per thread per phase
-constexpr size_t kSmemBudget = 112 * 1024;
+constexpr size_t kSmemBudget = 220 * 1024;
+constexpr size_t kResidentX = 48 * 1024;         // activation fragments kept for all of K up to this size
 
 struct Params {
     int64_t N;
@@ -43,12 +51,15 @@ struct Params {
     const float* gamma;
     float eps;
     int act;
-    int U, up, gps, ns, spp;
-    int nphase;          // K-phases per pass
-    int kp;              // activations per phase (multiple of 256 * gps)
-    int ncw;             // consumer warps = gps * NMAT * up * 2
+    int U;               // 16-row units
+    int up;              // units per pass (row blocks per pass = NMAT * up)
+    int gps;             // groups per phase (one stage = one row block x gps groups)
+    int nphase;          // phases per pass = ceil(G / gps)
+    int ns;              // ring slots
+    int ncw;             // consumer warps = 2 * gps
+    int nbuf;            // activation fragment buffers: nphase (all resident) or 2 (double-buffered)
     uint32_t stage_bytes;
-    uint32_t full_off, empty_off, xf_off, xsc_off, rstd_off, red_off, ssq_off;
+    uint32_t full_off, empty_off, xf_off, xf_bytes, xsc_off, rstd_off, red_off, ssq_off;
     int* status;
 };
 
@@ -64,24 +75,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-    uint16_t v;
-    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
 }
 
 __device__ __forceinline__ uint32_t lop3_mask_or(uint32_t a, uint32_t mask, uint32_t orv) {
@@ -102,13 +95,14 @@ __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t 
     return d;
 }
 
-// The 4-byte code word t (qs bytes 4t .. 4t+3) of block jj of a row starting at `row`
-// (shared address).  Block jj starts at byte 18 * jj; its codes at 18 * jj + 2.
+// The 4-byte code word t (qs bytes 4t .. 4t+3) of block jj of a row starting at `row` in
+// shared memory.  Block jj starts at byte 18 * jj; its codes at 18 * jj + 2.
 template <int JPAR>
-__device__ __forceinline__ uint32_t code_word(uint32_t row, int jj, int t) {
-    const uint32_t off = 18u * jj + 2u + 4u * t;
-    if constexpr (JPAR == 1) return lds32(row + off);        // odd block: 4-byte aligned
-    else return __funnelshift_r(lds32(row + off - 2), lds32(row + off + 2), 16);
+__device__ __forceinline__ uint32_t code_word(const uint8_t* row, int jj, int t) {
+    const int off = 18 * jj + 2 + 4 * t;
+    if constexpr (JPAR == 1) return *reinterpret_cast<const uint32_t*>(row + off);  // odd block: 4-byte aligned
+    else return __funnelshift_r(*reinterpret_cast<const uint32_t*>(row + off - 2),
+                                *reinterpret_cast<const uint32_t*>(row + off + 2), 16);
 }
 
 // A fragments (tile 0: low nibbles = elements 0..15, tile 1: high nibbles = 16..31) of one
@@ -143,12 +137,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + p.empty_off);
-    float* xsc = reinterpret_cast<float*>(smem + p.xsc_off);   // [hg][B] scale back (2^e)
     float* rstd = reinterpret_cast<float*>(smem + p.rstd_off);
-    float* red = reinterpret_cast<float*>(smem + p.red_off);
+    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [row of pass][warp][B]
     float* ssqb = reinterpret_cast<float*>(smem + p.ssq_off);  // [B][K/128] sums of x^2
-    const uint32_t xf = smem_u32(smem + p.xf_off);
-    const uint32_t ring = smem_u32(smem);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ncw = p.ncw, nct = ncw * 32;
@@ -156,10 +147,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
     const int u0 = static_cast<int>((static_cast<int64_t>(c) * p.U) / C);
     const int u1 = static_cast<int>((static_cast<int64_t>(c + 1) * p.U) / C);
     const int npass = (u1 - u0 + p.up - 1) / p.up;
-    const int S = npass * p.spp;
     const int B = p.B;
 
+    __shared__ int any_failed;
     if (tid == 0) {
+        any_failed = 0;
         for (int i = 0; i < p.ns; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], ncw);
@@ -171,33 +163,42 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
     __syncthreads();
 
     // ---------------- producer warp ----------------
+    // Stage s (order: pass, phase, unit, matrix) goes to slot s % ns.
     if (warp == ncw) {
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            auto issue = [&](int s) {
-                const int pass = s / p.spp, ks = s - pass * p.spp;
+            bool ok = true;
+            int s = 0, slot = 0;
+            uint32_t par = 1;   // parity of the empty-barrier phase to wait for (from the second lap)
+            for (int pass = 0; pass < npass && ok; ++pass) {
                 const int ub = u0 + pass * p.up;
                 const int nup = min(p.up, u1 - ub);
-                const int g0 = ks * p.gps;
-                const int ng = min(p.gps, p.G - g0);
-                const int slot = s % p.ns;
-                uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage_bytes;
-                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(NMAT * nup * ng * kBoxBytes));
-                for (int ph = 0; ph < ng; ++ph)
-                    for (int m = 0; m < NMAT; ++m)
-                        for (int u = 0; u < nup; ++u)
-                            tma_load_2d(dst + ((ph * NMAT + m) * p.up + u) * kBoxBytes, m ? &tm1 : &tm0,
-                                        (g0 + ph) * kGroupBytes, (ub + u) * kUnitRows, &full[slot], policy);
-            };
-            const int pre = min(p.ns, S);
-            for (int s = 0; s < pre; ++s) issue(s);  // weights only: before the dependency wait
-            pdl_trigger();
-            bool ok = true;
-            for (int s = pre; s < S && ok; ++s) {
-                const int slot = s % p.ns;
-                ok = mbar_wait(&empty[slot], static_cast<uint32_t>(((s / p.ns) + 1) & 1), p.status);
-                if (ok) issue(s);
+                for (int ph = 0; ph < p.nphase && ok; ++ph) {
+                    const int g0 = ph * p.gps;
+                    const int ng = min(p.gps, p.G - g0);
+                    for (int ul = 0; ul < nup && ok; ++ul) {
+                        for (int m = 0; m < NMAT; ++m) {
+                            if (s == p.ns) pdl_trigger();   // ring filled once: weights only so far
+                            if (s >= p.ns) {
+                                ok = mbar_wait(&empty[slot], par, p.status);
+                                if (!ok) break;
+                            }
+                            uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage_bytes;
+                            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ng * kBoxBytes));
+                            for (int j = 0; j < ng; ++j)
+                                tma_load_2d(dst + j * kBoxBytes, m ? &tm1 : &tm0, (g0 + j) * kGroupBytes,
+                                            (ub + ul) * kUnitRows, &full[slot], policy);
+                            ++s;
+                            if (++slot == p.ns) {
+                                slot = 0;
+                                par ^= 1u;
+                            }
+                        }
+                    }
+                }
             }
+            if (s <= p.ns) pdl_trigger();
+            if (!ok) drain_stages(full, p.ns, max(0, s - p.ns), s - 1);
         } else {
             pdl_trigger();
         }
@@ -209,26 +210,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
     pdl_wait();  // activations and residual come from the previous kernel
 
     const int g = lane >> 2, t = lane & 3;
-    const int rows_in_pass = NMAT * p.up * kUnitRows;
-    // task: (phase phi, matrix, unit uu, half group eta)
-    const int eta = warp & 1;
-    const int tw = warp >> 1;
-    const int uu = tw % p.up;
-    const int mat = (tw / p.up) % NMAT;
-    const int phi = tw / (p.up * NMAT);
-    const int nph = 2 * p.gps;  // partial sums per row
-    const int psi = phi * 2 + eta;
+    const int jg = warp >> 1, eta = warp & 1;   // my half group inside every stage
     const bool col_ok = PACKED ? (g < 2 * B) : (g < B);
+    const int kp = p.gps * 256;          // activations per phase
+    const int nhg = kp / 128;            // half groups per phase
+    const int hg = jg * 2 + eta;         // my half group inside the phase
 
-    // Raw activations of a K-phase: slot f covers float4 e4 of batch row b (f = b * kp4 + e4).
+    // Raw activations of a phase: slot f covers float4 e4 of batch row b (f = b * kp4 + e4).
     // Thread tid owns slots tid + i * nct; the first kPrefetchF4 are prefetched into
-    // registers (with the matching norm weights) during the previous phase's compute.
-    const int kp4 = p.kp / 4;
+    // registers (with the matching norm weights) ahead of their conversion.
+    const int kp4 = kp / 4;
     const int nslots = B * kp4;
     float4 pf[kPrefetchF4], pg[kPrefetchF4];
     auto load_slot = [&](int phase, int f, float4& xv, float4& gv) {
-        const int k0 = phase * p.kp;
-        const int lim = min(p.kp, p.G * 256 - k0);
+        const int k0 = phase * kp;
+        const int lim = min(kp, p.G * 256 - k0);
         const int b = f / kp4, e = (f - b * kp4) * 4;
         xv = make_float4(0.f, 0.f, 0.f, 0.f);
         gv = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -244,13 +240,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
             if (f < nslots) load_slot(phase, f, pf[i], pg[i]);
         }
     };
-    // One slot -> binary16 hi/lo B fragments.  The 32 lanes of a warp hold one 128-element
-    // half group of one row (nslots, kp4 and nct are multiples of 32), so the power-of-two
+    // One slot -> binary16 hi/lo B fragments in buffer `buf`.  The 32 lanes of a warp hold
+    // one 128-element half group of one row (kp4 is a multiple of 32), so the power-of-two
     // scale and the sum of squares are warp reductions.
-    auto convert_slot = [&](int phase, int f, float4 v, float4 gm, bool first_pass) {
+    auto convert_slot = [&](int phase, int buf, int f, float4 v, float4 gm, bool first_pass) {
         const int b = f / kp4, e4 = f - b * kp4;
         if (p.gamma) {
-            const int hgk = (phase * p.kp) / 128 + (e4 >> 5);   // half group inside the row
+            const int hgk = phase * nhg + (e4 >> 5);   // half group inside the row
             if (first_pass && hgk < 2 * p.G) {  // one fixed slot per (row, half group)
                 const float ps = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
                 if (lane == 0) ssqb[b * (2 * p.G) + hgk] = ps;
@@ -263,7 +259,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
         if (m > 0.f) ex = ((__float_as_int(m) >> 23) & 0xff) - 127 - 13;  // m * 2^-ex in [2^13, 2^14)
         ex = max(-100, min(100, ex));
         const float sc = __int_as_float((127 - ex) << 23);
-        const int hg = e4 >> 5, ln = e4 & 31;
+        const int hgi = e4 >> 5, ln = e4 & 31;
         const int j = ln >> 3, tile = (ln >> 2) & 1, tt = ln & 3;
         __half h0, l0, h1, l1, h2, l2, h3, l3;
         split_hi_lo(v.x * sc, h0, l0);
@@ -274,115 +270,175 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
         const __half2 lb0 = __halves2half2(l0, l2), lb1 = __halves2half2(l1, l3);  // b1 = {x1, x3}
         const uint2 hv = make_uint2(*reinterpret_cast<const uint32_t*>(&hb0), *reinterpret_cast<const uint32_t*>(&hb1));
         const uint2 lv = make_uint2(*reinterpret_cast<const uint32_t*>(&lb0), *reinterpret_cast<const uint32_t*>(&lb1));
-        uint8_t* xfp = smem + p.xf_off;
+        uint8_t* xfp = smem + p.xf_off + buf * p.xf_bytes;
         if constexpr (PACKED) {
-            *reinterpret_cast<uint2*>(xfp + xf_entry<true>(hg, j, tt, 2 * b, B) + tile * 8) = hv;
-            *reinterpret_cast<uint2*>(xfp + xf_entry<true>(hg, j, tt, 2 * b + 1, B) + tile * 8) = lv;
+            *reinterpret_cast<uint2*>(xfp + xf_entry<true>(hgi, j, tt, 2 * b, B) + tile * 8) = hv;
+            *reinterpret_cast<uint2*>(xfp + xf_entry<true>(hgi, j, tt, 2 * b + 1, B) + tile * 8) = lv;
         } else {
-            uint8_t* base = xfp + xf_entry<false>(hg, j, tt, b, B);
+            uint8_t* base = xfp + xf_entry<false>(hgi, j, tt, b, B);
             *reinterpret_cast<uint2*>(base + tile * 8) = hv;
             *reinterpret_cast<uint2*>(base + 16 + tile * 8) = lv;
         }
-        if (lane == 0) xsc[hg * B + b] = __int_as_float((127 + ex) << 23);
+        float* xsc = reinterpret_cast<float*>(smem + p.xsc_off) + buf * nhg * B;
+        if (lane == 0) xsc[hgi * B + b] = __int_as_float((127 + ex) << 23);
     };
-    auto convert = [&](int phase, bool first_pass) {
+    auto convert = [&](int phase, int buf, bool first_pass) {
 #pragma unroll
         for (int i = 0; i < kPrefetchF4; ++i) {
             const int f = tid + i * nct;
-            if (f < nslots) convert_slot(phase, f, pf[i], pg[i], first_pass);
+            if (f < nslots) convert_slot(phase, buf, f, pf[i], pg[i], first_pass);
         }
         for (int f = tid + kPrefetchF4 * nct; f < nslots; f += nct) {  // beyond the prefetch
             float4 xv, gv;
             load_slot(phase, f, xv, gv);
-            convert_slot(phase, f, xv, gv, first_pass);
+            convert_slot(phase, buf, f, xv, gv, first_pass);
         }
     };
 
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // PACKED: [row g, row g+8] of batch t; else [g: 2t, 2t+1; g+8: 2t, 2t+1]
-    int s = 0;
+    // All phases at once (resident fragments, converted in pass 0 only): my slots
+    // f = tid + i * nct over (phase, row, float4), loaded two at a time before converting.
+    auto convert_all = [&]() {
+        const int per_phase = B * kp4;
+        const int total = p.nphase * per_phase;
+        for (int f0 = tid; f0 < total; f0 += 2 * nct) {
+            float4 xv[2], gv[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int f = f0 + i * nct;
+                if (f < total) load_slot(f / per_phase, f % per_phase, xv[i], gv[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int f = f0 + i * nct;
+                if (f < total) convert_slot(f / per_phase, f / per_phase, f % per_phase, xv[i], gv[i], true);
+            }
+        }
+    };
+
     bool ok = true;
-    prefetch(0);
+    int s = 0, slot = 0;
+    uint32_t par = 0;                      // parity of the full-barrier phase to wait for
+    const bool resident = p.nbuf == p.nphase;
+    const int nq = npass * p.nphase;       // phases over all passes (the same activations each pass)
+    if (!resident) prefetch(0);
     // Every consumer warp runs the same sequence of named barriers whatever happens: after a
     // timed-out wait (ok == false) the remaining waits are skipped, never the barriers.
     for (int pass = 0; pass < npass; ++pass) {
         const int ub = u0 + pass * p.up;
         const int nup = min(p.up, u1 - ub);
+        const int q0 = pass * p.nphase;
+        consumer_sync(nct);                 // the previous pass is done with the buffers
+        if (resident) {
+            if (pass == 0) convert_all();
+        } else {
+            convert(0, q0 & 1, pass == 0);
+            if (q0 + 1 < nq) prefetch((q0 + 1) % p.nphase);
+        }
+        consumer_sync(nct);                 // fragments published
         for (int ph = 0; ph < p.nphase; ++ph) {
-            consumer_sync(nct);                 // previous phase's fragments are no longer read
-            convert(ph, pass == 0);
-            const int nxt = ph + 1 < p.nphase ? ph + 1 : (pass + 1 < npass ? 0 : -1);
-            consumer_sync(nct);                 // fragments (and scales) published
-            if (nxt >= 0) prefetch(nxt);
-            const int st_lo = ph * (p.kp / (256 * p.gps));
-            const int st_hi = min(p.spp, st_lo + p.kp / (256 * p.gps));
-            for (int ks = st_lo; ks < st_hi; ++ks, ++s) {
-                const int slot = s % p.ns;
-                if (ok) ok = mbar_wait(&full[slot], static_cast<uint32_t>((s / p.ns) & 1), p.status);
-                const int gidx = ks * p.gps + phi;          // group index of this task
-                if (gidx < p.G && uu < nup) {
-                    const uint32_t box = ring + slot * p.stage_bytes + ((phi * NMAT + mat) * p.up + uu) * kBoxBytes;
-                    const uint32_t rg = box + g * kGroupBytes, rg8 = box + (g + 8) * kGroupBytes;
-                    const int hg = (gidx * 256 - ph * p.kp) / 128 + eta;   // half group inside the phase
-                    float blk[4] = {0.f, 0.f, 0.f, 0.f};
+            const int q = q0 + ph;
+            if (!resident && ph + 1 < p.nphase) {   // next phase into the other buffer
+                convert(ph + 1, (q + 1) & 1, pass == 0);
+                if (q + 2 < nq) prefetch((q + 2) % p.nphase);
+            }
+            const int buf = resident ? ph : (q & 1);
+            const int ng = min(p.gps, p.G - ph * p.gps);
+            const bool mine = jg < ng;
+            const uint8_t* xfb = smem + p.xf_off + buf * p.xf_bytes;
+            const float* xsc = reinterpret_cast<const float*>(smem + p.xsc_off) + buf * nhg * B;
+            float sc0 = 0.f, sc1 = 0.f;     // power-of-two activation scales of my half group
+            if constexpr (PACKED) {
+                sc0 = t < B ? xsc[hg * B + t] : 0.f;
+            } else {
+                sc0 = 2 * t < B ? xsc[hg * B + 2 * t] : 0.f;
+                sc1 = 2 * t + 1 < B ? xsc[hg * B + 2 * t + 1] : 0.f;
+            }
+            uint4 xh[4];                    // B <= 4: my activation fragments, the same for every stage
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int jj = eta * 4 + j;
-                        uint32_t wg, wg8;
-                        if (j & 1) {
-                            wg = code_word<1>(rg, jj, t);
-                            wg8 = code_word<1>(rg8, jj, t);
-                        } else {
-                            wg = code_word<0>(rg, jj, t);
-                            wg8 = code_word<0>(rg8, jj, t);
-                        }
-                        const float dg = half_bits_to_float(lds16(rg + 18u * jj));
-                        const float dg8 = half_bits_to_float(lds16(rg8 + 18u * jj));
-                        uint32_t a0, a2, a4, a6, a1, a3, a5, a7;
-                        dequant_word(wg, a0, a2, a4, a6);
-                        dequant_word(wg8, a1, a3, a5, a7);
-                        float cf[4] = {0.f, 0.f, 0.f, 0.f};
-                        if constexpr (PACKED) {
-                            uint4 bx = make_uint4(0, 0, 0, 0);
-                            if (col_ok) bx = lds128(xf + xf_entry<true>(hg, j, t, g, B));
-                            mma_16816(cf, a0, a1, a2, a3, bx.x, bx.y);
-                            mma_16816(cf, a4, a5, a6, a7, bx.z, bx.w);
-                            blk[0] = fmaf(dg, cf[0] + cf[1], blk[0]);
-                            blk[1] = fmaf(dg8, cf[2] + cf[3], blk[1]);
-                        } else {
-                            uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
-                            if (col_ok) {
-                                bh = lds128(xf + xf_entry<false>(hg, j, t, g, B));
-                                bl = lds128(xf + xf_entry<false>(hg, j, t, g, B) + 16);
+            for (int j = 0; j < 4; ++j) {
+                xh[j] = make_uint4(0, 0, 0, 0);
+                if (PACKED && col_ok) xh[j] = *reinterpret_cast<const uint4*>(xfb + xf_entry<true>(hg, j, t, g, B));
+            }
+            float* rr = red + (g * ncw + warp) * B;   // my partial-sum slots, row g of row block 0
+            for (int ul = 0; ul < nup; ++ul) {
+                for (int m = 0; m < NMAT; ++m, rr += kUnitRows * ncw * B) {
+                    if (ok) ok = mbar_wait(&full[slot], par, p.status);
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (mine) {
+                        const uint8_t* rg = smem + static_cast<size_t>(slot) * p.stage_bytes + jg * kBoxBytes +
+                                            g * kGroupBytes;
+                        const uint8_t* rg8 = rg + 8 * kGroupBytes;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int jj = eta * 4 + j;
+                            uint32_t wg, wg8;
+                            if (j & 1) {
+                                wg = code_word<1>(rg, jj, t);
+                                wg8 = code_word<1>(rg8, jj, t);
+                            } else {
+                                wg = code_word<0>(rg, jj, t);
+                                wg8 = code_word<0>(rg8, jj, t);
                             }
-                            mma_16816(cf, a0, a1, a2, a3, bh.x, bh.y);
-                            mma_16816(cf, a4, a5, a6, a7, bh.z, bh.w);
-                            mma_16816(cf, a0, a1, a2, a3, bl.x, bl.y);
-                            mma_16816(cf, a4, a5, a6, a7, bl.z, bl.w);
-                            blk[0] = fmaf(dg, cf[0], blk[0]);
-                            blk[1] = fmaf(dg, cf[1], blk[1]);
-                            blk[2] = fmaf(dg8, cf[2], blk[2]);
-                            blk[3] = fmaf(dg8, cf[3], blk[3]);
+                            const float dg = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rg + 18 * jj));
+                            const float dg8 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rg8 + 18 * jj));
+                            uint32_t a0, a2, a4, a6, a1, a3, a5, a7;
+                            dequant_word(wg, a0, a2, a4, a6);
+                            dequant_word(wg8, a1, a3, a5, a7);
+                            float cf[4] = {0.f, 0.f, 0.f, 0.f};
+                            if constexpr (PACKED) {
+                                mma_16816(cf, a0, a1, a2, a3, xh[j].x, xh[j].y);
+                                mma_16816(cf, a4, a5, a6, a7, xh[j].z, xh[j].w);
+                                acc[0] = fmaf(dg, cf[0] + cf[1], acc[0]);
+                                acc[1] = fmaf(dg8, cf[2] + cf[3], acc[1]);
+                            } else {
+                                uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
+                                if (col_ok) {
+                                    bh = *reinterpret_cast<const uint4*>(xfb + xf_entry<false>(hg, j, t, g, B));
+                                    bl = *reinterpret_cast<const uint4*>(xfb + xf_entry<false>(hg, j, t, g, B) + 16);
+                                }
+                                mma_16816(cf, a0, a1, a2, a3, bh.x, bh.y);
+                                mma_16816(cf, a4, a5, a6, a7, bh.z, bh.w);
+                                mma_16816(cf, a0, a1, a2, a3, bl.x, bl.y);
+                                mma_16816(cf, a4, a5, a6, a7, bl.z, bl.w);
+                                acc[0] = fmaf(dg, cf[0], acc[0]);
+                                acc[1] = fmaf(dg, cf[1], acc[1]);
+                                acc[2] = fmaf(dg8, cf[2], acc[2]);
+                                acc[3] = fmaf(dg8, cf[3], acc[3]);
+                            }
                         }
                     }
-                    if constexpr (PACKED) {
-                        const float sc = t < B ? xsc[hg * B + t] : 0.f;
-                        acc[0] = fmaf(sc, blk[0], acc[0]);
-                        acc[1] = fmaf(sc, blk[1], acc[1]);
-                    } else {
-                        const float sc0 = 2 * t < B ? xsc[hg * B + 2 * t] : 0.f;
-                        const float sc1 = 2 * t + 1 < B ? xsc[hg * B + 2 * t + 1] : 0.f;
-                        acc[0] = fmaf(sc0, blk[0], acc[0]);
-                        acc[1] = fmaf(sc1, blk[1], acc[1]);
-                        acc[2] = fmaf(sc0, blk[2], acc[2]);
-                        acc[3] = fmaf(sc1, blk[3], acc[3]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[slot]);
+                    if (++slot == p.ns) {
+                        slot = 0;
+                        par ^= 1u;
+                    }
+                    ++s;
+                    // my partial sums of this row block: red[(row * ncw + warp) * B + b]
+                    if (mine) {
+                        float* rr8 = rr + 8 * ncw * B;
+                        if constexpr (PACKED) {
+                            if (t < B) {
+                                rr[t] = (ph ? rr[t] : 0.f) + sc0 * acc[0];
+                                rr8[t] = (ph ? rr8[t] : 0.f) + sc0 * acc[1];
+                            }
+                        } else {
+                            if (2 * t < B) {
+                                rr[2 * t] = (ph ? rr[2 * t] : 0.f) + sc0 * acc[0];
+                                rr8[2 * t] = (ph ? rr8[2 * t] : 0.f) + sc0 * acc[2];
+                            }
+                            if (2 * t + 1 < B) {
+                                rr[2 * t + 1] = (ph ? rr[2 * t + 1] : 0.f) + sc1 * acc[1];
+                                rr8[2 * t + 1] = (ph ? rr8[2 * t + 1] : 0.f) + sc1 * acc[3];
+                            }
+                        }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
             }
+            if (!resident) consumer_sync(nct);   // next buffer published; this one free again
         }
-        // ---- end of pass: combine the 2 * gps partial sums of every row, write outputs ----
-        consumer_sync(nct);
+        if (resident) consumer_sync(nct);        // every partial sum written
+        // ---- end of pass: combine the per-warp partial sums of every row, write outputs ----
         if (pass == 0 && p.gamma) {   // 1 / rms of every activation row (pass 0 saw all of K)
             if (tid < B) {
                 float sum = 0.f;
@@ -391,59 +447,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
             }
             consumer_sync(nct);
         }
-        {
-            // partial sums: red[(slotrow * nph + psi) * B + b]
-            const int slotrow = (mat * p.up + uu) * kUnitRows;
-            if (uu < nup) {
-                if constexpr (PACKED) {
-                    if (t < B) {
-                        red[((slotrow + g) * nph + psi) * B + t] = acc[0];
-                        red[((slotrow + g + 8) * nph + psi) * B + t] = acc[1];
-                    }
-                } else {
-                    if (2 * t < B) {
-                        red[((slotrow + g) * nph + psi) * B + 2 * t] = acc[0];
-                        red[((slotrow + g + 8) * nph + psi) * B + 2 * t] = acc[2];
-                    }
-                    if (2 * t + 1 < B) {
-                        red[((slotrow + g) * nph + psi) * B + 2 * t + 1] = acc[1];
-                        red[((slotrow + g + 8) * nph + psi) * B + 2 * t + 1] = acc[3];
-                    }
-                }
+        // warps that own no half group of the first phase never wrote their slots
+        const int nw = min(ncw, 2 * min(p.gps, p.G));
+        const int rows_in_pass = nup * NMAT * kUnitRows;
+        for (int idx = tid; idx < rows_in_pass * B; idx += nct) {
+            const int row = idx / B, b = idx - row * B;
+            const int rb = row / kUnitRows, r16 = row - rb * kUnitRows;
+            const int u = rb / NMAT, m = rb - u * NMAT;
+            const int64_t n = static_cast<int64_t>(ub + u) * kUnitRows + r16;
+            if (NMAT == 2 && m == 1) continue;
+            if (n >= p.N) continue;
+            float v = 0.f;
+            for (int w = 0; w < nw; ++w) v += red[(row * ncw + w) * B + b];
+            if (p.gamma) v *= rstd[b];
+            if (NMAT == 1) {
+                if (p.residual) v += p.residual[b * p.ldr + n];
+            } else {
+                float uv = 0.f;
+                const int urow = row + kUnitRows;   // same unit, matrix 1
+                for (int w = 0; w < nw; ++w) uv += red[(urow * ncw + w) * B + b];
+                if (p.gamma) uv *= rstd[b];
+                v = act_fn(v, p.act) * uv;
             }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            consumer_sync(nct);
-            for (int idx = tid; idx < rows_in_pass * B; idx += nct) {
-                const int row = idx / B, b = idx - row * B;
-                const int m = row / (p.up * kUnitRows);
-                const int rr = row - m * p.up * kUnitRows;
-                const int64_t n = static_cast<int64_t>(ub) * kUnitRows + rr;
-                if (NMAT == 2 && m == 1) continue;
-                if (rr / kUnitRows >= nup || n >= p.N) continue;
-                float v = 0.f;
-                for (int q = 0; q < nph; ++q) v += red[(row * nph + q) * B + b];
-                if (p.gamma) v *= rstd[b];
-                if (NMAT == 1) {
-                    if (p.residual) v += p.residual[b * p.ldr + n];
-                } else {
-                    float uv = 0.f;
-                    const int urow = p.up * kUnitRows + rr;
-                    for (int q = 0; q < nph; ++q) uv += red[(urow * nph + q) * B + b];
-                    if (p.gamma) uv *= rstd[b];
-                    v = act_fn(v, p.act) * uv;
-                }
-                p.y[b * p.ldy + n] = v;
-            }
+            p.y[b * p.ldy + n] = v;
         }
     }
-    // a copy never landed: give whatever the producer still had in flight a bounded chance to
-    // land before the CTA exits
-    __shared__ int any_failed;
-    if (tid == 0) any_failed = 0;
-    consumer_sync(nct);
+    // a copy never landed: give the copies the producer may still have in flight a bounded
+    // chance to land before the CTA exits
     if (!ok) atomicOr(&any_failed, 1);
     consumer_sync(nct);
-    if (any_failed && tid == 0) drain_stages(full, p.ns, max(0, S - p.ns), S - 1);
+    if (any_failed && tid == 0) drain_stages(full, p.ns, max(0, s - p.ns), s - 1);
 }
 
 }  // namespace gemv_mma

@@ -227,6 +227,40 @@ GEM_API gem_status gem_decode_layer(const gem_layer_desc *L, int B, float *x, ui
                             void *workspace, size_t ws_bytes, int32_t *status,
                             void *stream);
 
+/*
+ * A whole decode step (every layer, one new token per sequence) as ONE persistent launch.
+ *   Same arithmetic and results as calling gem_decode_layer for layer 0, 1, ... in order
+ *   (within the library's tolerance; summation orders differ).  One CTA per SM: a producer
+ *   warp streams every stage of the CTA's weights and cached K/V rows by TMA through a
+ *   shared-memory ring, running ahead across layer phases; consumer warps compute the
+ *   phases (QKV, attention with QK-norm/RoPE/KV append fused, O, gate/up, down) separated
+ *   by grid-wide barriers.  Every device-side wait is bounded: a wait that runs out sets
+ *   GEM_DEVFLAG_TIMEOUT and makes every CTA leave the step (x is then unspecified).
+ *
+ *   gem_step_plan_create  validates the layers and prepares device-resident descriptors
+ *            (tensor maps of every weight matrix and cache) and the step's scratch.  It
+ *            allocates device memory and synchronises the device: call it once, outside any
+ *            stream capture.  layers [nlayers] as for gem_decode_layer; k_caches[l],
+ *            v_caches[l]: layer l's caches [B][n_kv][cache_caps[l]][d] binary16 (device
+ *            pointers in host arrays; the plan keeps the pointers, not the arrays).
+ *            Supported: every layer with the same head_dim d in {64, 128, 256},
+ *            n_q / n_kv <= 4, no post_norms, no v_from_k, H, F and n_q * d multiples of
+ *            256, B in 1..4, 16-byte aligned weights and caches; otherwise
+ *            GEM_ERR_UNSUPPORTED_SHAPE (use gem_decode_layer for those layers).
+ *   gem_decode_step  enqueues the step: x [B][H] fp32 in/out (16-byte aligned), pos [B]
+ *            int32 device.  The plan's scratch (including grid-barrier and merge counters)
+ *            is shared by every call with that plan: calls with one plan must not overlap
+ *            (issue them in order on one stream).  Allocates nothing.
+ *   gem_step_plan_destroy  frees the plan (after its last step has completed).
+ */
+typedef struct gem_step_plan gem_step_plan;
+GEM_API gem_status gem_step_plan_create(const gem_layer_desc *layers, int nlayers, int B,
+                                        uint16_t *const *k_caches, uint16_t *const *v_caches,
+                                        const int64_t *cache_caps, gem_step_plan **plan);
+GEM_API gem_status gem_decode_step(const gem_step_plan *plan, float *x, const int32_t *pos,
+                                   int32_t *status, void *stream);
+GEM_API void gem_step_plan_destroy(gem_step_plan *plan);
+
 #ifdef __cplusplus
 }
 #endif

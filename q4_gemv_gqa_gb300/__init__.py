@@ -217,3 +217,41 @@ def decode_layer(layer: DeviceLayer, x: torch.Tensor, k_cache: torch.Tensor,
                               _stream(stream))
     _check(st, "gem_decode_layer")
     return x
+
+
+class StepPlan:
+    """Every layer of a decode step in one persistent launch (gem_step_plan).
+
+    layers: DeviceLayer list; k_caches, v_caches: per-layer uint16 [B, n_kv, cap, d]
+    tensors, kept referenced by the plan."""
+
+    def __init__(self, layers, B: int, k_caches, v_caches):
+        n = len(layers)
+        self._keep = (list(layers), list(k_caches), list(v_caches))
+        descs = (LayerDesc * n)(*[dl.desc for dl in layers])
+        kp = (C.c_void_p * n)(*[_dev(k, _HALF_BITS, "k_cache") for k in k_caches])
+        vp = (C.c_void_p * n)(*[_dev(v, _HALF_BITS, "v_cache") for v in v_caches])
+        caps = (C.c_int64 * n)(*[int(k.shape[2]) for k in k_caches])
+        h = C.c_void_p()
+        st = lib.gem_step_plan_create(descs, n, B, kp, vp, caps, C.byref(h))
+        _check(st, "gem_step_plan_create")
+        self._h = h
+        self.B = B
+
+    def step(self, x: torch.Tensor, pos: torch.Tensor, status: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+        st = lib.gem_decode_step(self._h, _dev(x, torch.float32, "x"), _dev(pos, torch.int32, "pos"),
+                                 _dev(status, torch.int32, "status"), _stream(stream))
+        _check(st, "gem_decode_step")
+        return x
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib.gem_step_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

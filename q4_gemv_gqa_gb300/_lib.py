@@ -44,6 +44,10 @@ PROTOTYPES = {
     "gem_swiglu": (i32, [p, p, i32, i64, i32, p, p]),
     "gem_decode_layer_workspace": (C.c_size_t, [C.POINTER(LayerDesc), i32, i64]),
     "gem_decode_layer": (i32, [C.POINTER(LayerDesc), i32, p, p, p, i64, p, p, C.c_size_t, p, p]),
+    "gem_step_plan_create": (i32, [C.POINTER(LayerDesc), i32, i32, C.POINTER(p), C.POINTER(p),
+                                   C.POINTER(i64), C.POINTER(p)]),
+    "gem_decode_step": (i32, [p, p, p, p, p]),
+    "gem_step_plan_destroy": (None, [p]),
 }
 
 _lib = None

@@ -58,13 +58,6 @@ struct AttnParams {
 
 __host__ __device__ __forceinline__ int tile_slots(int d) { return d <= 64 ? 128 : (d <= 128 ? 64 : 32); }
 
-// byte offset of (row r, element c) inside a tile stored as D/64 boxes of [TP][64] with the
-// 128-byte swizzle (16-byte chunk index XOR row mod 8)
-__device__ __forceinline__ uint32_t swz(int r, int c, int tp) {
-    const int box = c >> 6, cc = c & 63;
-    return static_cast<uint32_t>(box * tp * 128 + r * 128 + ((((cc >> 3) ^ r) & 7) << 4) + ((cc & 7) << 1));
-}
-
 __device__ __forceinline__ void split_range(int T, int tp, int nsplit_max, int s, int& nsplit, int& t0, int& t1) {
     const int nt = (T + tp - 1) / tp;
     nsplit = min(nsplit_max, nt);

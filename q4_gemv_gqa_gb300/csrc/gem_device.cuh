@@ -183,4 +183,24 @@ __device__ __forceinline__ void split_hi_lo(float x, __half& hi, __half& lo) {
     lo = __float2half_rn(x - __half2float(hi));
 }
 
+// ---- shared by the RoPE and attention paths ----------------------------------------------
+// cos and sin of an fp64 angle in fp32: the angle is reduced to [-pi, pi] with a two-part
+// 2*pi (Cody and Waite's additive argument reduction), which keeps the reduced angle exact
+// to ~1e-13 for the positions of a decode cache; fp32 sincosf is then accurate.
+__device__ __forceinline__ void rope_cos_sin(double ang, float& c, float& s) {
+    const double two_pi_hi = 6.283185307179586;        // 2*pi rounded to double
+    const double two_pi_lo = 2.4492935982947064e-16;   // 2*pi - two_pi_hi
+    const double k = rint(ang * 0.15915494309189535);  // ang / (2*pi)
+    double r = fma(-k, two_pi_hi, ang);
+    r = fma(-k, two_pi_lo, r);
+    sincosf(static_cast<float>(r), &s, &c);
+}
+
+// Byte offset of (row r, element c) of a binary16 tile stored by TMA as D/64 boxes of
+// [tp rows][64 elements] with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t swz(int r, int c, int tp) {
+    const int box = c >> 6, cc = c & 63;
+    return static_cast<uint32_t>(box * tp * 128 + r * 128 + ((((cc >> 3) ^ r) & 7) << 4) + ((cc & 7) << 1));
+}
+
 }  // namespace gem

@@ -78,18 +78,6 @@ struct RopeFreq {
     double w[kMaxHeadDim / 2];
 };
 
-// cos and sin of p * w in fp32 from an fp64 angle: the angle is reduced to [-pi, pi] with a
-// two-part 2*pi (Cody and Waite's additive argument reduction), which keeps the reduced
-// angle exact to ~1e-13 for the positions of a decode cache; fp32 sincosf is then accurate.
-__device__ __forceinline__ void rope_cos_sin(double ang, float& c, float& s) {
-    const double two_pi_hi = 6.283185307179586;        // 2*pi rounded to double
-    const double two_pi_lo = 2.4492935982947064e-16;   // 2*pi - two_pi_hi
-    const double k = rint(ang * 0.15915494309189535);  // ang / (2*pi)
-    double r = fma(-k, two_pi_hi, ang);
-    r = fma(-k, two_pi_lo, r);
-    sincosf(static_cast<float>(r), &s, &c);
-}
-
 __global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const RopeOp op, const RopeFreq fr, int early) {
     __shared__ float buf[kRopeWarps][kMaxHeadDim];
     __shared__ float cs_tab[kMaxHeadDim / 2], sn_tab[kMaxHeadDim / 2];

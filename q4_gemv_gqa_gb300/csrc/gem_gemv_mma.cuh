@@ -95,14 +95,26 @@ __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t 
     return d;
 }
 
-// The 4-byte code word t (qs bytes 4t .. 4t+3) of block jj of a row starting at `row` in
-// shared memory.  Block jj starts at byte 18 * jj; its codes at 18 * jj + 2.
+// Shared-memory loads at 32-bit shared addresses (the ring is read only after its full
+// barrier, whose wait is a volatile asm with a memory clobber, so these stay after it).
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// The 4-byte code word of a block whose codes for this lane start at shared address `ca`
+// (block start + 2 + 4t): 4-byte aligned in odd blocks, two aligned words and a funnel
+// shift in even ones (blocks are 18 bytes).
 template <int JPAR>
-__device__ __forceinline__ uint32_t code_word(const uint8_t* row, int jj, int t) {
-    const int off = 18 * jj + 2 + 4 * t;
-    if constexpr (JPAR == 1) return *reinterpret_cast<const uint32_t*>(row + off);  // odd block: 4-byte aligned
-    else return __funnelshift_r(*reinterpret_cast<const uint32_t*>(row + off - 2),
-                                *reinterpret_cast<const uint32_t*>(row + off + 2), 16);
+__device__ __forceinline__ uint32_t code_word(uint32_t ca) {
+    if constexpr (JPAR == 1) return lds32(ca);
+    else return __funnelshift_r(lds32(ca - 2), lds32(ca + 2), 16);
 }
 
 // A fragments (tile 0: low nibbles = elements 0..15, tile 1: high nibbles = 16..31) of one
@@ -360,27 +372,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
                 if (PACKED && col_ok) xh[j] = *reinterpret_cast<const uint4*>(xfb + xf_entry<true>(hg, j, t, g, B));
             }
             float* rr = red + (g * ncw + warp) * B;   // my partial-sum slots, row g of row block 0
+            // my half group inside a stage: row g, blocks 4 eta .. 4 eta + 3 of group jg
+            const uint32_t soff = static_cast<uint32_t>(jg * kBoxBytes + g * kGroupBytes + eta * 72);
+            const uint32_t ring0 = smem_u32(smem);
             for (int ul = 0; ul < nup; ++ul) {
                 for (int m = 0; m < NMAT; ++m, rr += kUnitRows * ncw * B) {
                     if (ok) ok = mbar_wait(&full[slot], par, p.status);
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
                     if (mine) {
-                        const uint8_t* rg = smem + static_cast<size_t>(slot) * p.stage_bytes + jg * kBoxBytes +
-                                            g * kGroupBytes;
-                        const uint8_t* rg8 = rg + 8 * kGroupBytes;
+                        const uint32_t sa = ring0 + static_cast<uint32_t>(slot) * p.stage_bytes + soff;  // scales
+                        const uint32_t ca = sa + 2 + 4 * t;                                               // codes
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int jj = eta * 4 + j;
                             uint32_t wg, wg8;
-                            if (j & 1) {
-                                wg = code_word<1>(rg, jj, t);
-                                wg8 = code_word<1>(rg8, jj, t);
+                            if (((eta * 4 + j) & 1) != 0) {   // eta * 4 is even: parity of j
+                                wg = code_word<1>(ca + 18 * j);
+                                wg8 = code_word<1>(ca + 18 * j + 8 * kGroupBytes);
                             } else {
-                                wg = code_word<0>(rg, jj, t);
-                                wg8 = code_word<0>(rg8, jj, t);
+                                wg = code_word<0>(ca + 18 * j);
+                                wg8 = code_word<0>(ca + 18 * j + 8 * kGroupBytes);
                             }
-                            const float dg = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rg + 18 * jj));
-                            const float dg8 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rg8 + 18 * jj));
+                            const float dg = half_bits_to_float(lds16(sa + 18 * j));
+                            const float dg8 = half_bits_to_float(lds16(sa + 18 * j + 8 * kGroupBytes));
                             uint32_t a0, a2, a4, a6, a1, a3, a5, a7;
                             dequant_word(wg, a0, a2, a4, a6);
                             dequant_word(wg8, a1, a3, a5, a7);

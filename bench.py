@@ -165,7 +165,8 @@ class Model:
     def launches_per_step(self):
         n = 0
         for s, cap in zip(self.wl.layers, self.wl.cache_cap):
-            n += 6 + (2 if s.post_norms else 0)
+            fused = s.d <= 256 and s.n_q // s.n_kv <= 4   # QK-norm/RoPE/append inside attention
+            n += (5 if fused else 6) + (2 if s.post_norms else 0)
             if self.gem.gqa_decode_attn_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.window) > 0:
                 n += 1
         return n

@@ -23,6 +23,7 @@
 // writes (max, denominator, unnormalised output) and a merge kernel combines splits in
 // ascending order.  A split that has the whole range writes the final output directly.
 #include <algorithm>
+#include <cmath>
 #include <map>
 #include <mutex>
 
@@ -54,6 +55,12 @@ struct AttnParams {
     const uint16_t* v_cache;
     uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off;
     int* status;
+    // fused QK-norm / RoPE / append (flash kernel only): q rows are the raw projections
+    int fuse;
+    const float *g_q, *g_k;
+    float eps;
+    int rope_dim, v_mode;
+    uint16_t *k_out, *v_out;
 };
 
 __host__ __device__ __forceinline__ int tile_slots(int d) { return d <= 64 ? 128 : (d <= 128 ? 64 : 32); }
@@ -350,7 +357,8 @@ struct FlashSmem {
 template <int D>
 __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                         const __grid_constant__ CUtensorMap tmV,
-                                                                        const AttnParams P) {
+                                                                        const AttnParams P,
+                                                                        const __grid_constant__ RopeFreq fr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     constexpr int kTileBytes = kFlashTile * D * 2;            // one K or V tile
@@ -359,6 +367,13 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFlashWarps * kWarpRing);       // [warp][stage]
     __half* pbuf = reinterpret_cast<__half*>(smem + kFlashWarps * kWarpRing + 128);    // [warp][8][24]
     float* comb = reinterpret_cast<float*>(smem);             // reuses the ring after the tile loop
+    // fused path: rotated query heads [4][D], cos / sin of the rotated pairs, new K / V rows
+    float* qs = reinterpret_cast<float*>(smem + kFlashWarps * kWarpRing + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2);
+    float* kbuf = qs + 4 * D;
+    float* cs = kbuf + D;
+    float* sn = cs + D / 2;
+    uint16_t* knew = reinterpret_cast<uint16_t*>(sn + D / 2);
+    uint16_t* vnew = knew + D;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int t_id = threadIdx.x, lane = t_id & 31, warp = t_id >> 5;
@@ -412,14 +427,91 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
         prefetch_tensormap(&tmV);
         for (int it = 0; it < npre; ++it) issue(it);
     }
+    const int R = P.rope_dim, half = R / 2;
+    if (P.fuse)   // positions are not written by the preceding kernel: build the table now
+        for (int i = t_id; i < half; i += kFlashWarps * 32) {
+            float c, s;
+            rope_cos_sin(static_cast<double>(p) * fr.w[i], c, s);
+            cs[i] = c;
+            sn[i] = s;
+        }
     pdl_trigger();
     if (P.early) pdl_wait();
+
+    const bool owner = slot_p >= t0 * kFlashTile && slot_p < t1 * kFlashTile;
+    if (P.fuse) {
+        // QK-norm + RoPE of a raw head row (warp-wide), result in sb[0..D)
+        auto rotate = [&](const float* src, const float* gamma, float* sb) {
+            float v[D / 32];
+            float ss = 0.f;
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+                v[k] = src[lane + 32 * k];
+                ss = fmaf(v[k], v[k], ss);
+            }
+            ss = warp_sum(ss);
+            if (gamma) {
+                const float r = rsqrtf(ss / static_cast<float>(D) + P.eps);
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) v[k] = v[k] * r * gamma[lane + 32 * k];
+            }
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) sb[lane + 32 * k] = v[k];
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+                const int e = lane + 32 * k;
+                if (e < R) {
+                    const int i = e < half ? e : e - half;
+                    v[k] = e < half ? fmaf(sb[e], cs[i], -sb[e + half] * sn[i]) : fmaf(sb[e - half], sn[i], sb[e] * cs[i]);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) sb[lane + 32 * k] = v[k];
+            __syncwarp();
+        };
+        __syncthreads();   // rotation table complete
+        const float* qrow0 = P.q + b * P.ldq;
+        if (warp < G) rotate(qrow0 + static_cast<int64_t>(g * G + warp) * D, P.g_q, qs + warp * D);
+        if (owner) {   // the new token's K and V rows: into the cache and into shared memory
+            const int64_t crow = (row0 + slot_p) * D;
+            const float* krow = qrow0 + static_cast<int64_t>(P.n_q + g) * D;
+            if (warp == 0) {
+                rotate(krow, P.g_k, kbuf);
+                for (int e = lane; e < D; e += 32) {
+                    const uint16_t h = __half_as_ushort(__float2half_rn(kbuf[e]));
+                    knew[e] = h;
+                    P.k_out[crow + e] = h;
+                }
+            } else if (warp == 1) {
+                if (P.v_mode == 1) {   // V = unweighted RMSNorm of the raw K row
+                    float ss = 0.f;
+                    for (int e = lane; e < D; e += 32) ss = fmaf(krow[e], krow[e], ss);
+                    const float r = rsqrtf(warp_sum(ss) / static_cast<float>(D) + P.eps);
+                    for (int e = lane; e < D; e += 32) {
+                        const uint16_t h = __half_as_ushort(__float2half_rn(krow[e] * r));
+                        vnew[e] = h;
+                        P.v_out[crow + e] = h;
+                    }
+                } else {
+                    const float* vrow = qrow0 + static_cast<int64_t>(P.n_q + P.n_kv + g) * D;
+                    for (int e = lane; e < D; e += 32) {
+                        const uint16_t h = __half_as_ushort(__float2half_rn(vrow[e]));
+                        vnew[e] = h;
+                        P.v_out[crow + e] = h;
+                    }
+                }
+            }
+        }
+        __syncthreads();   // rotated query heads and the new rows visible to every warp
+    }
 
     // Q^T B fragments: column n = 2h + hl (head h = n / 2, hi or lo), k = dims
     uint32_t qb[D / 16][2];
     {
         const int h = gq >> 1, hl = gq & 1;
-        const float* qrow = P.q + b * P.ldq + static_cast<int64_t>(g * G + h) * D;
+        const float* qrow = P.fuse ? qs + h * D : P.q + b * P.ldq + static_cast<int64_t>(g * G + h) * D;
         float2 raw[D / 16][2];
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16) {
@@ -457,9 +549,9 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
         uint8_t* vt = kt + kTileBytes;
         if (ok) ok = mbar_wait(&wbar[st], static_cast<uint32_t>((it / kFlashStages) & 1), P.status);
         const int rp = slot_p - tile * kFlashTile;
-        if (it < npre && rp >= 0 && rp < kFlashTile) {  // new row landed after this copy was requested
-            const uint16_t* ks = P.k_cache + (row0 + slot_p) * D;
-            const uint16_t* vs = P.v_cache + (row0 + slot_p) * D;
+        if ((P.fuse || it < npre) && rp >= 0 && rp < kFlashTile) {  // the new row: staged before it was written
+            const uint16_t* ks = P.fuse ? knew : P.k_cache + (row0 + slot_p) * D;
+            const uint16_t* vs = P.fuse ? vnew : P.v_cache + (row0 + slot_p) * D;
             for (int c = lane * 8; c < D; c += 32 * 8) {
                 *reinterpret_cast<uint4*>(kt + swz(rp, c, kFlashTile)) = *reinterpret_cast<const uint4*>(ks + c);
                 *reinterpret_cast<uint4*>(vt + swz(rp, c, kFlashTile)) = *reinterpret_cast<const uint4*>(vs + c);
@@ -672,7 +764,8 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
     pl.ws = static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
     if (pl.flash) {
         const size_t ring = static_cast<size_t>(kFlashWarps) * kFlashStages * 2 * kFlashTile * d * 2;
-        pl.smem = align_up(ring + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2, 1024) + 1024;
+        // + the fused path's rotated query heads, K row, rotation table and new K/V rows (28 d bytes)
+        pl.smem = align_up(ring + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2 + 28ull * d, 1024) + 1024;
         return pl;
     }
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
@@ -695,20 +788,19 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
     return pl;
 }
 
-using SplitKernel = void (*)(CUtensorMap, CUtensorMap, AttnParams);
-SplitKernel pick(int d, bool flash) {
+const void* pick(int d, bool flash) {
     if (flash) {
         switch (d) {
-            case 64: return gqa_flash_kernel<64>;
-            case 128: return gqa_flash_kernel<128>;
-            default: return gqa_flash_kernel<256>;
+            case 64: return reinterpret_cast<const void*>(gqa_flash_kernel<64>);
+            case 128: return reinterpret_cast<const void*>(gqa_flash_kernel<128>);
+            default: return reinterpret_cast<const void*>(gqa_flash_kernel<256>);
         }
     }
     switch (d) {
-        case 64: return gqa_split_kernel<64>;
-        case 128: return gqa_split_kernel<128>;
-        case 256: return gqa_split_kernel<256>;
-        default: return gqa_split_kernel<512>;
+        case 64: return reinterpret_cast<const void*>(gqa_split_kernel<64>);
+        case 128: return reinterpret_cast<const void*>(gqa_split_kernel<128>);
+        case 256: return reinterpret_cast<const void*>(gqa_split_kernel<256>);
+        default: return reinterpret_cast<const void*>(gqa_split_kernel<512>);
     }
 }
 
@@ -723,7 +815,7 @@ gem_status ensure_smem_attn(const void* fn, int device, size_t bytes) {
     return GEM_OK;
 }
 
-gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early) {
+gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool fuse) {
     gem_status st = attn_check(op);
     if (st != GEM_OK || op.B == 0 || op.n_q == 0) return st;
     DeviceInfo di;
@@ -759,6 +851,25 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early) {
     P.pa_off = pl.pa_off;
     P.st_off = pl.st_off;
     P.status = op.status ? op.status : di.status_word;
+    RopeFreq fr{};
+    if (fuse) {
+        if (!pl.flash) return GEM_ERR_UNSUPPORTED_SHAPE;
+        if (op.rope_dim < 2 || op.rope_dim > op.d || (op.rope_dim & 1) || !(op.theta > 0.f) || op.v_mode < 0 ||
+            op.v_mode > 1 || !op.k_out || !op.v_out)
+            return GEM_ERR_INVALID_ARG;
+        if (op.ldq < static_cast<int64_t>(op.n_q + op.n_kv + (op.v_mode ? 0 : op.n_kv)) * op.d)
+            return GEM_ERR_INVALID_ARG;
+        P.fuse = 1;
+        P.g_q = op.gamma_q;
+        P.g_k = op.gamma_k;
+        P.eps = op.eps;
+        P.rope_dim = op.rope_dim;
+        P.v_mode = op.v_mode;
+        P.k_out = op.k_out;
+        P.v_out = op.v_out;
+        for (int i = 0; i < op.rope_dim / 2; ++i)
+            fr.w[i] = std::pow(static_cast<double>(op.theta), -2.0 * i / op.rope_dim);
+    }
 
     const uint64_t rows = static_cast<uint64_t>(op.B) * op.n_kv * op.cache_cap;
     CUtensorMap tmK, tmV;
@@ -768,10 +879,10 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early) {
     if ((st = make_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, op.v_cache, op.d, rows,
                                  static_cast<uint64_t>(op.d) * 2, 64, pl.tp, CU_TENSOR_MAP_SWIZZLE_128B)) != GEM_OK)
         return st;
-    const void* fn = reinterpret_cast<const void*>(pick(op.d, pl.flash));
+    const void* fn = pick(op.d, pl.flash);
     if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
     dim3 grid(pl.nsplit_max, op.n_kv, op.B);
-    void* args[] = {&tmK, &tmV, &P};
+    void* args[] = {&tmK, &tmV, &P, &fr};   // the split kernel takes the first three
     if ((st = launch_pdl(fn, grid, dim3(pl.flash ? kFlashWarps * 32 : kAttnThreads), pl.smem, stream, args)) != GEM_OK)
         return st;
     if (pl.nsplit_max > 1) {
@@ -810,8 +921,10 @@ gem_status attn_check(const AttnOp& op) {
     return GEM_OK;
 }
 
-gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, false); }
-gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true); }
+gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, false, false); }
+gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, false); }
+bool attn_fusable(int n_q, int n_kv, int d) { return n_kv > 0 && n_q % n_kv == 0 && use_flash(n_q, n_kv, d); }
+gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, true); }
 
 // ---- split-partial scratch owned by the library (gem_gqa_decode_attn_noalloc) --------------
 // One fixed array per device (a module-scope __device__ variable exists once in every device

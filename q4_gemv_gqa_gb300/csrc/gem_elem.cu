@@ -71,13 +71,6 @@ __global__ void swiglu_kernel(const float* __restrict__ gate, const float* __res
 // rotates the first rope_dim dims.  "gem" research record: NeoX pairing (i, i + R/2); on
 // full-attention layers V is the unweighted RMSNorm of the raw K projection.
 constexpr int kRopeWarps = 4;
-constexpr int kMaxHeadDim = 512;
-
-// Rotation frequencies theta^(-2i/R), i < R/2, computed on the host in fp64.
-struct RopeFreq {
-    double w[kMaxHeadDim / 2];
-};
-
 __global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const RopeOp op, const RopeFreq fr, int early) {
     __shared__ float buf[kRopeWarps][kMaxHeadDim];
     __shared__ float cs_tab[kMaxHeadDim / 2], sn_tab[kMaxHeadDim / 2];

@@ -99,6 +99,18 @@ struct AttnOp {
     float* out; int64_t ldo;
     void* workspace; size_t ws_bytes;
     int32_t* status;
+    // Fused QK-norm / RoPE / KV append (attn_enqueue_fused): q points at the raw QKV
+    // projection row (Q heads, K heads, then V heads unless v_mode == 1).
+    const float *gamma_q, *gamma_k;   // nullable
+    float eps, theta;
+    int rope_dim, v_mode;
+    uint16_t *k_out, *v_out;           // the same caches, written at the new slot
+};
+
+// Rotation frequencies theta^(-2i/R), i < R/2, computed on the host in fp64.
+constexpr int kMaxHeadDim = 512;
+struct RopeFreq {
+    double w[kMaxHeadDim / 2];
 };
 size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window);
 gem_status attn_check(const AttnOp& op);
@@ -107,6 +119,11 @@ gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream);
 // cached rows are read before griddepcontrol.wait (the preceding kernel writes neither,
 // except the new token's row, which is re-read after the wait).
 gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream);
+// Inside a layer chain, right after the QKV projection: the attention kernel itself applies
+// QK-norm and RoPE to its query heads and appends the new K/V row (no separate RoPE launch).
+// Only for shapes that attn_fusable() accepts.
+bool attn_fusable(int n_q, int n_kv, int d);
+gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -7,7 +7,7 @@
 // of the K projection.
 //
 //   1  QKV GEMV, pre-attention RMSNorm fused into its activation staging
-//   2  QK-norm + RoPE + binary16 KV append
+//   2  QK-norm + RoPE + binary16 KV append (head_dim <= 256 and n_q / n_kv <= 4: inside 3)
 //   3  split-K GQA attention (+ ordered merge launch when the range is split)
 //   4  O GEMV with the residual add fused (post_norms: O GEMV, then norm + residual)
 //   5  gate/up GEMV pair, pre-FFN RMSNorm fused in, gated activation in the epilogue
@@ -128,14 +128,30 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
     attn.workspace = w.attn_ws;
     attn.ws_bytes = w.attn_ws_bytes;
     attn.status = status;
+    // flash-eligible shapes: QK-norm, RoPE and the KV append run inside the attention kernel
+    const bool fused = attn_fusable(static_cast<int>(nq), static_cast<int>(nkv), static_cast<int>(d));
+    if (fused) {
+        attn.gamma_q = rope.gamma_q;
+        attn.gamma_k = rope.gamma_k;
+        attn.eps = L->eps;
+        attn.theta = L->theta;
+        attn.rope_dim = L->rope_dim;
+        attn.v_mode = rope.v_mode;
+        attn.k_out = k_cache;
+        attn.v_out = v_cache;
+    }
     if ((st = gemv_check(qkv)) != GEM_OK || (st = gemv_check(oproj)) != GEM_OK ||
         (st = gemv_check(gateup)) != GEM_OK || (st = gemv_check(down)) != GEM_OK ||
         (st = rope_check(rope)) != GEM_OK || (st = attn_check(attn)) != GEM_OK)
         return st;
 
     if ((st = gemv_enqueue(qkv, stream)) != GEM_OK) return st;
-    if ((st = rope_enqueue_in_chain(rope, stream)) != GEM_OK) return st;
-    if ((st = attn_enqueue_in_chain(attn, stream)) != GEM_OK) return st;
+    if (fused) {
+        if ((st = attn_enqueue_fused(attn, stream)) != GEM_OK) return st;
+    } else {
+        if ((st = rope_enqueue_in_chain(rope, stream)) != GEM_OK) return st;
+        if ((st = attn_enqueue_in_chain(attn, stream)) != GEM_OK) return st;
+    }
     if ((st = gemv_enqueue(oproj, stream)) != GEM_OK) return st;
     if (L->post_norms && (st = postnorm_residual_enqueue(x, w.tmp, B, H, L->g_post_attn, L->eps, stream)) != GEM_OK)
         return st;

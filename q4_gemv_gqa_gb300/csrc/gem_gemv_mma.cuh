@@ -185,27 +185,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
             for (int pass = 0; pass < npass && ok; ++pass) {
                 const int ub = u0 + pass * p.up;
                 const int nup = min(p.up, u1 - ub);
-                for (int ph = 0; ph < p.nphase && ok; ++ph) {
+                // resident activations: row-block-major (every K-phase of a row block in turn);
+                // otherwise phase-major, as the consumers convert one K-phase at a time
+                const bool rbmajor = p.nbuf == p.nphase;
+                const int nrb = nup * NMAT;
+                for (int i = 0; i < p.nphase * nrb && ok; ++i) {
+                    const int ph = rbmajor ? i % p.nphase : i / nrb;
+                    const int rb = rbmajor ? i / p.nphase : i % nrb;
+                    const int ul = rb / NMAT, m = rb % NMAT;
                     const int g0 = ph * p.gps;
                     const int ng = min(p.gps, p.G - g0);
-                    for (int ul = 0; ul < nup && ok; ++ul) {
-                        for (int m = 0; m < NMAT; ++m) {
-                            if (s == p.ns) pdl_trigger();   // ring filled once: weights only so far
-                            if (s >= p.ns) {
-                                ok = mbar_wait(&empty[slot], par, p.status);
-                                if (!ok) break;
-                            }
-                            uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage_bytes;
-                            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ng * kBoxBytes));
-                            for (int j = 0; j < ng; ++j)
-                                tma_load_2d(dst + j * kBoxBytes, m ? &tm1 : &tm0, (g0 + j) * kGroupBytes,
-                                            (ub + ul) * kUnitRows, &full[slot], policy);
-                            ++s;
-                            if (++slot == p.ns) {
-                                slot = 0;
-                                par ^= 1u;
-                            }
-                        }
+                    if (s == p.ns) pdl_trigger();   // ring filled once: weights only so far
+                    if (s >= p.ns) {
+                        ok = mbar_wait(&empty[slot], par, p.status);
+                        if (!ok) break;
+                    }
+                    uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage_bytes;
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ng * kBoxBytes));
+                    for (int j = 0; j < ng; ++j)
+                        tma_load_2d(dst + j * kBoxBytes, m ? &tm1 : &tm0, (g0 + j) * kGroupBytes,
+                                    (ub + ul) * kUnitRows, &full[slot], policy);
+                    ++s;
+                    if (++slot == p.ns) {
+                        slot = 0;
+                        par ^= 1u;
                     }
                 }
             }
@@ -347,7 +350,106 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
             if (q0 + 1 < nq) prefetch((q0 + 1) % p.nphase);
         }
         consumer_sync(nct);                 // fragments published
-        for (int ph = 0; ph < p.nphase; ++ph) {
+        if (resident) {
+            // Row-block-major: all K-phases of one row block in turn, running sums in registers,
+            // one store per row block (no read-modify-write of shared partial sums per stage).
+            const uint32_t soff = static_cast<uint32_t>(jg * kBoxBytes + g * kGroupBytes + eta * 72);
+            const uint32_t ring0 = smem_u32(smem);
+            const int nrb = nup * NMAT;
+            for (int rb = 0; rb < nrb; ++rb) {
+                float tot[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int ph = 0; ph < p.nphase; ++ph) {
+                    const int ng = min(p.gps, p.G - ph * p.gps);
+                    const bool mine = jg < ng;
+                    if (ok) ok = mbar_wait(&full[slot], par, p.status);
+                    if (mine) {
+                        const uint8_t* xfb = smem + p.xf_off + ph * p.xf_bytes;
+                        const float* xsc = reinterpret_cast<const float*>(smem + p.xsc_off) + ph * nhg * B;
+                        float sc0, sc1 = 0.f;
+                        if constexpr (PACKED) {
+                            sc0 = t < B ? xsc[hg * B + t] : 0.f;
+                        } else {
+                            sc0 = 2 * t < B ? xsc[hg * B + 2 * t] : 0.f;
+                            sc1 = 2 * t + 1 < B ? xsc[hg * B + 2 * t + 1] : 0.f;
+                        }
+                        const uint32_t sa = ring0 + static_cast<uint32_t>(slot) * p.stage_bytes + soff;  // scales
+                        const uint32_t ca = sa + 2 + 4 * t;                                               // codes
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
+                            if (col_ok) {
+                                bh = *reinterpret_cast<const uint4*>(xfb + xf_entry<PACKED>(hg, j, t, g, B));
+                                if constexpr (!PACKED) bl = *reinterpret_cast<const uint4*>(xfb + xf_entry<false>(hg, j, t, g, B) + 16);
+                            }
+                            uint32_t wg, wg8;
+                            if ((j & 1) != 0) {
+                                wg = code_word<1>(ca + 18 * j);
+                                wg8 = code_word<1>(ca + 18 * j + 8 * kGroupBytes);
+                            } else {
+                                wg = code_word<0>(ca + 18 * j);
+                                wg8 = code_word<0>(ca + 18 * j + 8 * kGroupBytes);
+                            }
+                            const float dg = half_bits_to_float(lds16(sa + 18 * j));
+                            const float dg8 = half_bits_to_float(lds16(sa + 18 * j + 8 * kGroupBytes));
+                            uint32_t a0, a2, a4, a6, a1, a3, a5, a7;
+                            dequant_word(wg, a0, a2, a4, a6);
+                            dequant_word(wg8, a1, a3, a5, a7);
+                            float cf[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_16816(cf, a0, a1, a2, a3, bh.x, bh.y);
+                            mma_16816(cf, a4, a5, a6, a7, bh.z, bh.w);
+                            if constexpr (PACKED) {
+                                acc[0] = fmaf(dg, cf[0] + cf[1], acc[0]);
+                                acc[1] = fmaf(dg8, cf[2] + cf[3], acc[1]);
+                            } else {
+                                mma_16816(cf, a0, a1, a2, a3, bl.x, bl.y);
+                                mma_16816(cf, a4, a5, a6, a7, bl.z, bl.w);
+                                acc[0] = fmaf(dg, cf[0], acc[0]);
+                                acc[1] = fmaf(dg, cf[1], acc[1]);
+                                acc[2] = fmaf(dg8, cf[2], acc[2]);
+                                acc[3] = fmaf(dg8, cf[3], acc[3]);
+                            }
+                        }
+                        if constexpr (PACKED) {
+                            tot[0] = fmaf(sc0, acc[0], tot[0]);
+                            tot[1] = fmaf(sc0, acc[1], tot[1]);
+                        } else {
+                            tot[0] = fmaf(sc0, acc[0], tot[0]);
+                            tot[1] = fmaf(sc1, acc[1], tot[1]);
+                            tot[2] = fmaf(sc0, acc[2], tot[2]);
+                            tot[3] = fmaf(sc1, acc[3], tot[3]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[slot]);
+                    if (++slot == p.ns) {
+                        slot = 0;
+                        par ^= 1u;
+                    }
+                    ++s;
+                }
+                if (jg < min(p.gps, p.G)) {   // owned a half group in phase 0: my slots of this row block
+                    float* rr = red + ((rb * kUnitRows + g) * ncw + warp) * B;
+                    float* rr8 = rr + 8 * ncw * B;
+                    if constexpr (PACKED) {
+                        if (t < B) {
+                            rr[t] = tot[0];
+                            rr8[t] = tot[1];
+                        }
+                    } else {
+                        if (2 * t < B) {
+                            rr[2 * t] = tot[0];
+                            rr8[2 * t] = tot[2];
+                        }
+                        if (2 * t + 1 < B) {
+                            rr[2 * t + 1] = tot[1];
+                            rr8[2 * t + 1] = tot[3];
+                        }
+                    }
+                }
+            }
+        }
+        for (int ph = 0; ph < (resident ? 0 : p.nphase); ++ph) {
             const int q = q0 + ph;
             if (!resident && ph + 1 < p.nphase) {   // next phase into the other buffer
                 convert(ph + 1, (q + 1) & 1, pass == 0);

@@ -137,6 +137,20 @@ def traffic_record(kernel_key: str):
     return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
 
 
+# ---- replicas (N > 1): one independent step per rank, max-over-ranks timing -------------------
+
+def max_over_ranks(dist, torch, ms: float, device) -> float:
+    """The slowest rank's step time: every rank contributes its own, all receive the max."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes: int, world: int, ms: float) -> float:
+    """Aggregate algorithmic GB/s of `world` replicas, each streaming step_bytes per step."""
+    return step_bytes * world / (ms * 1e-3) / 1e9
+
+
 # ---- device setup -----------------------------------------------------------------------------
 
 class Model:
@@ -295,9 +309,7 @@ def run_gem(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     if dist:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(dist, torch, ms, "cuda")
         dist.barrier()
     flags = gem.device_status()
 
@@ -393,7 +405,7 @@ def run_gem(args):
     dk = kern[dom]
 
     tokens = wl.B * world
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms)
     if rank == 0:
         cpu = cpu_baseline(wl, args) if world == 1 else None
         line = {

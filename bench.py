@@ -338,8 +338,11 @@ def run_gem(args):
     e2e_ms = e2.elapsed_time(e3) / args.steps
     e2e_wall_ms = (time.perf_counter() - t0) * 1e3 / args.steps
 
-    # per-kernel roofline: each op of the layer timed alone over all layers' data
+    # per-kernel roofline: each op of the layer timed alone over the data of every layer that
+    # has the first layer's shape and cache capacity (a mixed stack's other layers differ)
     shape0, cap0 = wl.layers[0], wl.cache_cap[0]
+    same = [i for i in range(nL) if wl.layers[i] == shape0 and wl.cache_cap[i] == cap0]
+    nS = len(same)
     kern = {}
     q = torch.randn((wl.B, shape0.n_q * shape0.d), device="cuda")
     out = torch.empty_like(q)
@@ -347,21 +350,23 @@ def run_gem(args):
                                                            shape0.window)), dtype=torch.uint8, device="cuda")
 
     def attn_all():
-        for k, v in zip(model.kc, model.vc):
+        for i in same:
+            k, v = model.kc[i], model.vc[i]
             gem.gqa_decode_attn(q, k, v, shape0.n_q, shape0.n_kv, shape0.d, model.pos, shape0.window,
                                 float(shape0.scale), out, aws)
     ga = capture(torch, attn_all)
-    ms_a = time_graph(torch, ga, max(5, args.steps)) / nL
+    ms_a = time_graph(torch, ga, max(5, args.steps)) / nS
     Ta = min(T, shape0.window) if shape0.window else T
     kern["gqa_decode_attn"] = {"us": ms_a * 1e3, "bytes": attn_bytes(shape0, wl.B, Ta)}
 
     xin = torch.randn((wl.B, max(shape0.H, shape0.F, shape0.n_q * shape0.d)), device="cuda")
-    gate_up = [torch.cat([dl.w_gate, dl.w_up]) for dl in model.layers]
+    layers0 = [model.layers[i] for i in same]
+    gate_up = [torch.cat([dl.w_gate, dl.w_up]) for dl in layers0]
     yb = torch.empty((wl.B, 2 * shape0.F), device="cuda")
     for name, mats, N, K in [("q4_0_gemv_gate_up", gate_up, 2 * shape0.F, shape0.H),
-                             ("q4_0_gemv_qkv", [dl.w_qkv for dl in model.layers], shape0.n_qkv, shape0.H),
-                             ("q4_0_gemv_down", [dl.w_down for dl in model.layers], shape0.H, shape0.F),
-                             ("q4_0_gemv_o", [dl.w_o for dl in model.layers], shape0.H, shape0.n_q * shape0.d)]:
+                             ("q4_0_gemv_qkv", [dl.w_qkv for dl in layers0], shape0.n_qkv, shape0.H),
+                             ("q4_0_gemv_down", [dl.w_down for dl in layers0], shape0.H, shape0.F),
+                             ("q4_0_gemv_o", [dl.w_o for dl in layers0], shape0.H, shape0.n_q * shape0.d)]:
         xk = xin[:, :K].contiguous()
         yk = torch.empty((wl.B, N), device="cuda")
 
@@ -369,7 +374,7 @@ def run_gem(args):
             for W in mats:
                 gem.q4_0_gemv(W, N, K, xk, yk)
         gg = capture(torch, gemv_all)
-        ms_g = time_graph(torch, gg, max(5, args.steps)) / nL
+        ms_g = time_graph(torch, gg, max(5, args.steps)) / nS
         kern[name] = {"us": ms_g * 1e3, "bytes": gemv_bytes(N, K, wl.B)}
     del gate_up, yb
 
@@ -388,6 +393,17 @@ def run_gem(args):
         b = gemv_bytes(21504, 5376, B)
         gemv31["b%d" % B] = {"us": us, "gbs": b / us / 1e3}
     del W31
+
+    # the same step as one persistent launch (gem_decode_step), where the layers allow it
+    persistent = None
+    try:
+        plan = gem.StepPlan(model.layers, wl.B, model.kc, model.vc)
+        gp = capture(torch, lambda: plan.step(model.x, model.pos))
+        ms_p = time_graph(torch, gp, max(5, args.steps))
+        persistent = {"ms_per_step": round(ms_p, 4), "us_per_layer": round(ms_p * 1e3 / nL, 3)}
+        plan.close()
+    except gem.GemError as e:
+        persistent = {"unsupported": str(e)}
 
     peak, peak_kind = measured_peaks()
     for k in kern.values():
@@ -428,6 +444,8 @@ def run_gem(args):
                          "us_per_launch": round(dk["us"], 3)},
             "kernels": {k: {"us": round(v["us"], 3), "gbs": round(v["gbs"], 1), "frac": round(v["frac"], 4)}
                         for k, v in kern.items()},
+            "kernels_layers": "the %d of %d layers shaped like the first" % (nS, nL),
+            "persistent_step_kernel": persistent,
             "gemv_k5376_n21504": {k: {"us": round(v["us"], 3), "gbs": round(v["gbs"], 1),
                                       "frac": round(v["frac"], 4)} for k, v in gemv31.items()},
             "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,

@@ -63,6 +63,22 @@ def _dev(t: torch.Tensor | None, dtype, name: str):
     return t.data_ptr()
 
 
+def _cache_shape(k: torch.Tensor, v: torch.Tensor, B: int, n_kv: int, d: int) -> int:
+    """Caches must be [B, n_kv, cap, d] (the kernels address them from these sizes)."""
+    for name, c in (("k_cache", k), ("v_cache", v)):
+        if c.dim() != 4 or c.shape[0] != B or c.shape[1] != n_kv or c.shape[3] != d:
+            raise ValueError("%s must be [B=%d, n_kv=%d, cap, d=%d], got %s" % (name, B, n_kv, d, tuple(c.shape)))
+    if v.shape != k.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    return int(k.shape[2])
+
+
+def _q4_bytes(W: torch.Tensor, N: int, K: int) -> None:
+    # K % 32 != 0 is left to the library, which rejects it with GEM_ERR_BAD_SHAPE
+    if K % 32 == 0 and W.numel() < N * (K // 32) * 18:
+        raise ValueError("W must hold N x K Q4_0 weights (%d bytes), has %d" % (N * (K // 32) * 18, W.numel()))
+
+
 def version() -> int:
     return lib.gem_version()
 
@@ -77,6 +93,9 @@ def q4_0_gemv(W: torch.Tensor, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
               residual: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y[b] = deq(W) @ x[b] (+ residual[b]).  x: [B, >=K] fp32, y: [B, >=N] fp32."""
     B = x.shape[0] if x.dim() == 2 else 1
+    _q4_bytes(W, N, K)
+    if x.shape[-1] < K or y.shape[-1] < N:
+        raise ValueError("x must have >= K columns and y >= N")
     st = lib.gem_q4_0_gemv(_dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"),
                            x.shape[-1], B, _dev(y, torch.float32, "y"), y.shape[-1],
                            _dev(residual, torch.float32, "residual"), _stream(stream))
@@ -101,7 +120,7 @@ def rmsnorm_qknorm_rope(qkv: torch.Tensor, n_q: int, n_kv: int, d: int,
                         status: torch.Tensor | None = None, stream=None) -> None:
     """qkv [B, ldqkv] fp32 in place; caches binary16 bits (int16/uint16) [B, n_kv, cap, d]; pos int32 [B]."""
     B = qkv.shape[0]
-    cap = k_cache.shape[2]
+    cap = _cache_shape(k_cache, v_cache, B, n_kv, d)
     st = lib.gem_rmsnorm_qknorm_rope(
         _dev(qkv, torch.float32, "qkv"), qkv.shape[-1], B, n_q, n_kv, d,
         _dev(gamma_q, torch.float32, "gamma_q"), _dev(gamma_k, torch.float32, "gamma_k"),
@@ -122,7 +141,7 @@ def gqa_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                     status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """q [B, ldq] fp32 (head h at column h*d); caches uint16 [B, n_kv, cap, d]."""
     B = q.shape[0]
-    cap = k_cache.shape[2]
+    cap = _cache_shape(k_cache, v_cache, B, n_kv, d)
     ws_ptr = _dev(workspace, torch.uint8, "workspace")
     ws_bytes = workspace.numel() if workspace is not None else 0
     st = lib.gem_gqa_decode_attn(
@@ -147,7 +166,7 @@ def gqa_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     calls that may run concurrently on one device race on the shared array; shapes whose
     partials exceed NOALLOC_SCRATCH_BYTES raise GemError (GEM_ERR_WORKSPACE)."""
     B = q.shape[0]
-    cap = k_cache.shape[2]
+    cap = _cache_shape(k_cache, v_cache, B, n_kv, d)
     st = lib.gem_gqa_decode_attn_noalloc(
         _dev(q, torch.float32, "q"), q.shape[-1], _dev(k_cache, _HALF_BITS, "k_cache"),
         _dev(v_cache, _HALF_BITS, "v_cache"), B, n_q, n_kv, d, cap,
@@ -209,9 +228,13 @@ def decode_layer(layer: DeviceLayer, x: torch.Tensor, k_cache: torch.Tensor,
                  status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """One layer step, in place on x [B, H] fp32; caches uint16 [B, n_kv, cap, d]."""
     B = x.shape[0]
+    s = layer.shape
+    cap = _cache_shape(k_cache, v_cache, B, s.n_kv, s.d)
+    if x.dim() != 2 or x.shape[1] != s.H:
+        raise ValueError("x must be [B, H=%d], got %s" % (s.H, tuple(x.shape)))
     st = lib.gem_decode_layer(C.byref(layer.desc), B, _dev(x, torch.float32, "x"),
                               _dev(k_cache, _HALF_BITS, "k_cache"),
-                              _dev(v_cache, _HALF_BITS, "v_cache"), k_cache.shape[2],
+                              _dev(v_cache, _HALF_BITS, "v_cache"), cap,
                               _dev(pos, torch.int32, "pos"), _dev(workspace, torch.uint8, "workspace"),
                               workspace.numel(), _dev(status, torch.int32, "status"),
                               _stream(stream))
@@ -227,6 +250,10 @@ class StepPlan:
 
     def __init__(self, layers, B: int, k_caches, v_caches):
         n = len(layers)
+        if len(k_caches) != n or len(v_caches) != n:
+            raise ValueError("one K and one V cache per layer")
+        for dl, k, v in zip(layers, k_caches, v_caches):
+            _cache_shape(k, v, B, dl.shape.n_kv, dl.shape.d)
         self._keep = (list(layers), list(k_caches), list(v_caches))
         descs = (LayerDesc * n)(*[dl.desc for dl in layers])
         kp = (C.c_void_p * n)(*[_dev(k, _HALF_BITS, "k_cache") for k in k_caches])
@@ -240,6 +267,11 @@ class StepPlan:
 
     def step(self, x: torch.Tensor, pos: torch.Tensor, status: torch.Tensor | None = None,
              stream=None) -> torch.Tensor:
+        H = self._keep[0][0].shape.H
+        if x.dim() != 2 or x.shape[0] != self.B or x.shape[1] != H:
+            raise ValueError("x must be [B=%d, H=%d], got %s" % (self.B, H, tuple(x.shape)))
+        if pos.numel() < self.B:
+            raise ValueError("pos must hold B positions")
         st = lib.gem_decode_step(self._h, _dev(x, torch.float32, "x"), _dev(pos, torch.int32, "pos"),
                                  _dev(status, torch.int32, "status"), _stream(stream))
         _check(st, "gem_decode_step")

@@ -57,6 +57,9 @@ gem_status gemv_check(const GemvOp& op);
 gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream);
 // Tensor-core path (mma.sync) for the TMA-eligible shapes; called by gemv_enqueue.
 gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di);
+// One-row (B = 1) tensor-core kernel; *planned = false when K is too long for its shared-memory
+// layout (nothing launched).
+gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, bool* planned);
 
 // ---- norms / RoPE / activation -------------------------------------------------------------
 struct RopeOp {

@@ -56,10 +56,13 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
             gps = c;
         }
     }
+    // Stages hold two row blocks (sharing the activation operand) unless no CTA has two.
+    const int rps = umax * nmat >= 2 ? 2 : 1;
+    p.rps = rps;
     const size_t budget = std::min<size_t>(gemv_mma::kSmemBudget, di.smem_optin);
     const size_t xf = static_cast<size_t>(2 * p.G) * kRecBytes + kZeroBytes;
     auto layout = [&](int up, int ns, bool commit) -> size_t {
-        const size_t stage = static_cast<size_t>(gps) * kBoxBytes;
+        const size_t stage = static_cast<size_t>(rps * gps) * kBoxBytes;
         const size_t red = static_cast<size_t>(nmat) * up * kUnitRows * (2 * gps) * 4;
         size_t off = align_up(static_cast<size_t>(ns) * stage, 128);
         const size_t full_off = off;
@@ -85,7 +88,7 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
     const int nphase = (p.G + gps - 1) / gps;
     int up = umax, ns = 0;
     for (;;) {
-        const int stages = nmat * up * nphase;
+        const int stages = (nmat * up + rps - 1) / rps * nphase;
         const int want = std::min(4, stages);
         ns = 0;
         for (int n = std::min(kMaxSlots, stages); n >= want && !ns; --n)

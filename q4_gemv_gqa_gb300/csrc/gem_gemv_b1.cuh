@@ -25,6 +25,8 @@
 
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "gem_gemv_mma.cuh"
 
 namespace gem {
@@ -38,7 +40,7 @@ using gemv_mma::kUnitRows;
 constexpr int kMaxConsumerWarps = 18;
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kRecBytes = 512;   // activation record of one half group: 8 columns x 8 tiles x 8 B
-constexpr int kZeroBytes = 64;   // the operand of lanes off the block diagonal
+constexpr int kZeroBytes = 96;   // the operand of lanes off the block diagonal (bytes 32..95)
 
 struct Params {
     int64_t N;
@@ -51,7 +53,8 @@ struct Params {
     int act;
     int U;               // 16-row units
     int up;              // units per pass
-    int gps;             // groups per phase (stage = one row block x gps groups)
+    int gps;             // groups per phase (stage = rps row blocks x gps groups)
+    int rps;             // row blocks per stage: 2, or 1 when no CTA has two
     int nphase;
     int ns;
     int ncw;             // consumer warps = 2 * gps
@@ -67,55 +70,68 @@ __device__ __forceinline__ int code_byte(bool odd, int i, int j) {
     return 4 * i - 2 + j;
 }
 
-// One task: rows g and g + 8 of one block per lane, 8 mma over the block's 32 weights.
-// a = shared offset of the lane's 5 words in row g (row g + 8 is 8 rows further); xr = shared
-// offset of the lane's 64-byte activation operand (its column or the zero block).
-template <bool ODD>
-__device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t xr, float& t0, float& t1) {
-    const uint32_t* wa = reinterpret_cast<const uint32_t*>(smem + a);
-    const uint32_t* wb = reinterpret_cast<const uint32_t*>(smem + a + 8 * kGroupBytes);
-    uint32_t ra[5], rb[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        ra[i] = wa[i];
-        rb[i] = wb[i];
-    }
+// One task: rows g and g + 8 of one block per lane in each of NR row blocks (the same K range,
+// so they share the activation operand), 8 mma per row block.  a = shared offset of the lane's
+// 5 words in row g of row block 0 (row g + 8 is 8 rows further, row block r is r * rstride
+// further); xr = shared offset of the lane's 64-byte activation operand.
+template <bool ODD, int NR>
+__device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t rstride, uint32_t xr,
+                                     float (&t0)[2], float (&t1)[2]) {
     const uint4* xp = reinterpret_cast<const uint4*>(smem + xr);
     uint4 xb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) xb[i] = xp[i];
-    uint32_t ca[4], cb[4];
-    float da, db;
-    if constexpr (ODD) {
+    uint32_t ca[NR][4], cb[NR][4];
+    float da[NR], db[NR];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ca[i] = ra[i + 1];
-            cb[i] = rb[i + 1];
-        }
-        da = __high2float(*reinterpret_cast<const __half2*>(&ra[0]));
-        db = __high2float(*reinterpret_cast<const __half2*>(&rb[0]));
-    } else {
-        ca[0] = __byte_perm(ra[0], ra[4], 0x5432);
-        cb[0] = __byte_perm(rb[0], rb[4], 0x5432);
+    for (int r = 0; r < NR; ++r) {
+        const uint32_t* wa = reinterpret_cast<const uint32_t*>(smem + a + r * rstride);
+        const uint32_t* wb = reinterpret_cast<const uint32_t*>(smem + a + r * rstride + 8 * kGroupBytes);
+        uint32_t ra[5], rb[5];
 #pragma unroll
-        for (int i = 1; i < 4; ++i) {
-            ca[i] = ra[i];
-            cb[i] = rb[i];
+        for (int i = 0; i < 5; ++i) {
+            ra[i] = wa[i];
+            rb[i] = wb[i];
         }
-        da = __low2float(*reinterpret_cast<const __half2*>(&ra[0]));
-        db = __low2float(*reinterpret_cast<const __half2*>(&rb[0]));
+        if constexpr (ODD) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ca[r][i] = ra[i + 1];
+                cb[r][i] = rb[i + 1];
+            }
+            da[r] = __high2float(*reinterpret_cast<const __half2*>(&ra[0]));
+            db[r] = __high2float(*reinterpret_cast<const __half2*>(&rb[0]));
+        } else {
+            ca[r][0] = __byte_perm(ra[0], ra[4], 0x5432);
+            cb[r][0] = __byte_perm(rb[0], rb[4], 0x5432);
+#pragma unroll
+            for (int i = 1; i < 4; ++i) {
+                ca[r][i] = ra[i];
+                cb[r][i] = rb[i];
+            }
+            da[r] = __low2float(*reinterpret_cast<const __half2*>(&ra[0]));
+            db[r] = __low2float(*reinterpret_cast<const __half2*>(&rb[0]));
+        }
     }
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float d[NR][4];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) d[r][0] = d[r][1] = d[r][2] = d[r][3] = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        uint32_t l02, l13, h02, h13, m02, m13, n02, n13;
-        gemv_mma::dequant_word(ca[i], l02, l13, h02, h13);   // row g: low nibbles (b0,b2) (b1,b3), high nibbles
-        gemv_mma::dequant_word(cb[i], m02, m13, n02, n13);   // row g + 8
-        mma_16816(d, l02, m02, l13, m13, xb[i].x, xb[i].y);  // k-tile 2i: low nibbles of word i
-        mma_16816(d, h02, n02, h13, n13, xb[i].z, xb[i].w);  // k-tile 2i + 1: high nibbles
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            uint32_t l02, l13, h02, h13, m02, m13, n02, n13;
+            gemv_mma::dequant_word(ca[r][i], l02, l13, h02, h13);   // row g: low nibbles (b0,b2) (b1,b3), high nibbles
+            gemv_mma::dequant_word(cb[r][i], m02, m13, n02, n13);   // row g + 8
+            mma_16816(d[r], l02, m02, l13, m13, xb[i].x, xb[i].y);  // k-tile 2i: low nibbles of word i
+            mma_16816(d[r], h02, n02, h13, n13, xb[i].z, xb[i].w);  // k-tile 2i + 1: high nibbles
+        }
     }
-    t0 = fmaf(da, d[0] + d[1], t0);
-    t1 = fmaf(db, d[2] + d[3], t1);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        t0[r] = fmaf(da[r], d[r][0] + d[r][1], t0[r]);
+        t1[r] = fmaf(db[r], d[r][2] + d[r][3], t1[r]);
+    }
 }
 
 template <int NMAT>
@@ -126,10 +142,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + p.empty_off);
     float* red = reinterpret_cast<float*>(smem + p.red_off);    // [row of pass][warp]
-    float* misc = reinterpret_cast<float*>(smem + p.misc_off);  // [0, 2 ncw): reductions; [64]: out scale
+    float* misc = reinterpret_cast<float*>(smem + p.misc_off);  // [0, 2 ncw): reductions; [64], [65]: scales
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ncw = p.ncw, nct = ncw * 32;
+    const int G = p.G, gps = p.gps, nphase = p.nphase, ns = p.ns, rps = p.rps;
+    const uint32_t stage_bytes = p.stage_bytes;
+    const uint32_t rstride = static_cast<uint32_t>(gps * kBoxBytes);   // second row block of a stage
     const int C = gridDim.x, c = blockIdx.x;
     const int u0 = static_cast<int>((static_cast<int64_t>(c) * p.U) / C);
     const int u1 = static_cast<int>((static_cast<int64_t>(c + 1) * p.U) / C);
@@ -138,7 +157,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     __shared__ int any_failed;
     if (tid == 0) {
         any_failed = 0;
-        for (int i = 0; i < p.ns; ++i) {
+        for (int i = 0; i < ns; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], ncw);
         }
@@ -148,7 +167,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     }
     __syncthreads();
 
-    // ---------------- producer warp: stages (pass, row block, phase) ----------------
+    // ---------------- producer warp: stages (pass, row-block tuple, phase) ----------------
+    // Row blocks of a pass: rb = unit * NMAT + matrix; stage v holds rb v * rps .. v * rps + rps - 1
+    // (those that exist) x the phase's groups.
     if (warp == ncw) {
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
@@ -158,31 +179,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
             for (int pass = 0; pass < npass && ok; ++pass) {
                 const int ub = u0 + pass * p.up;
                 const int nrb = min(p.up, u1 - ub) * NMAT;
-                for (int rb = 0; rb < nrb && ok; ++rb) {
-                    const int row0 = (ub + rb / NMAT) * kUnitRows;
-                    const CUtensorMap* tm = (NMAT == 2 && (rb & 1)) ? &tm1 : &tm0;
-                    for (int ph = 0; ph < p.nphase; ++ph) {
-                        const int g0 = ph * p.gps;
-                        const int ng = min(p.gps, p.G - g0);
-                        if (s == p.ns) pdl_trigger();   // ring filled once
-                        if (s >= p.ns) {
+                for (int v = 0; v * rps < nrb && ok; ++v) {
+                    const int nr = min(rps, nrb - v * rps);
+                    for (int ph = 0; ph < nphase; ++ph) {
+                        const int g0 = ph * gps;
+                        const int ng = min(gps, G - g0);
+                        if (s == ns) pdl_trigger();   // ring filled once
+                        if (s >= ns) {
                             ok = mbar_wait(&empty[slot], par, p.status);
                             if (!ok) break;
                         }
-                        uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage_bytes;
-                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ng * kBoxBytes));
-                        for (int j = 0; j < ng; ++j)
-                            tma_load_2d(dst + j * kBoxBytes, tm, (g0 + j) * kGroupBytes, row0, &full[slot], policy);
+                        uint8_t* dst = smem + static_cast<size_t>(slot) * stage_bytes;
+                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nr * ng * kBoxBytes));
+                        for (int r = 0; r < nr; ++r) {
+                            const int rb = v * rps + r;
+                            const int row0 = (ub + rb / NMAT) * kUnitRows;
+                            const CUtensorMap* tm = (NMAT == 2 && (rb & 1)) ? &tm1 : &tm0;
+                            for (int j = 0; j < ng; ++j)
+                                tma_load_2d(dst + r * rstride + j * kBoxBytes, tm, (g0 + j) * kGroupBytes, row0,
+                                            &full[slot], policy);
+                        }
                         ++s;
-                        if (++slot == p.ns) {
+                        if (++slot == ns) {
                             slot = 0;
                             par ^= 1u;
                         }
                     }
                 }
             }
-            if (s <= p.ns) pdl_trigger();
-            if (!ok) drain_stages(full, p.ns, max(0, s - p.ns), s - 1);
+            if (s <= ns) pdl_trigger();
+            if (!ok) drain_stages(full, ns, max(0, s - ns), s - 1);
         } else {
             pdl_trigger();
         }
@@ -193,17 +219,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     pdl_trigger();
     pdl_wait();   // the activations (and residual) come from the previous kernel
 
-    const int K = p.G * 256;
+    const int K = G * 256;
     // 1. largest |gamma * x| and sum of x^2 over the row
     {
         float mx = 0.f, ss = 0.f;
         const float4* x4 = reinterpret_cast<const float4*>(p.x);
         const float4* g4 = reinterpret_cast<const float4*>(p.gamma);
+#pragma unroll 4
         for (int i = tid; i < K / 4; i += nct) {
-            float4 v = x4[i];
+            float4 v = __ldg(x4 + i);
             ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             if (p.gamma) {
-                const float4 gm = g4[i];
+                const float4 gm = __ldg(g4 + i);
                 v.x *= gm.x; v.y *= gm.y; v.z *= gm.z; v.w *= gm.w;
             }
             mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
@@ -235,105 +262,135 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     // 2. activation records: record (hg, column 2t + h), tile tau, register r holds the h part of
     // the two elements of block 2t + (hg & 1) of group hg / 2 that lane t's k-slots of that register
     // meet in the A operand (bytes j = r and r + 2 of code word tau / 2, nibble tau & 1).
+    // Four registers per thread and round, their loads issued before any conversion.
     {
         const float sc = misc[64];
         uint8_t* xf = smem + p.xf_off;
-        const int nreg = 2 * p.G * 64;   // (hg, t, tau, r)
-        for (int i = tid; i < nreg; i += nct) {
-            const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
-            const bool odd = hg & 1;
-            const int base = (hg >> 1) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
-            const int k0 = base + code_byte(odd, tau >> 1, r);
-            const int k1 = base + code_byte(odd, tau >> 1, r + 2);
-            float v0 = p.x[k0], v1 = p.x[k1];
-            if (p.gamma) {
-                v0 *= p.gamma[k0];
-                v1 *= p.gamma[k1];
+        const int nreg = 2 * G * 64;   // (hg, t, tau, r)
+        for (int i0 = tid; i0 < nreg; i0 += 4 * nct) {
+            float v0[4], v1[4];
+            uint32_t off[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * nct;
+                v0[u] = v1[u] = 0.f;
+                off[u] = 0;
+                if (i < nreg) {
+                    const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
+                    const bool odd = hg & 1;
+                    const int base = (hg >> 1) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
+                    const int k0 = base + code_byte(odd, tau >> 1, r);
+                    const int k1 = base + code_byte(odd, tau >> 1, r + 2);
+                    v0[u] = __ldg(p.x + k0);
+                    v1[u] = __ldg(p.x + k1);
+                    if (p.gamma) {
+                        v0[u] *= __ldg(p.gamma + k0);
+                        v1[u] *= __ldg(p.gamma + k1);
+                    }
+                    off[u] = static_cast<uint32_t>(hg * kRecBytes + (2 * t) * 64 + tau * 8 + r * 4);
+                }
             }
-            v0 *= sc;
-            v1 *= sc;
-            __half h0, l0, h1, l1;
-            split_hi_lo(v0, h0, l0);
-            split_hi_lo(v1, h1, l1);
-            const __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
-            const uint32_t off = static_cast<uint32_t>(hg * kRecBytes + (2 * t) * 64 + tau * 8 + r * 4);
-            *reinterpret_cast<__half2*>(xf + off) = hh;
-            *reinterpret_cast<__half2*>(xf + off + 64) = ll;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + u * nct < nreg) {
+                    __half h0, l0, h1, l1;
+                    split_hi_lo(v0[u] * sc, h0, l0);
+                    split_hi_lo(v1[u] * sc, h1, l1);
+                    *reinterpret_cast<__half2*>(xf + off[u]) = __halves2half2(h0, h1);
+                    *reinterpret_cast<__half2*>(xf + off[u] + 64) = __halves2half2(l0, l1);
+                }
+            }
         }
-        if (tid < kZeroBytes / 4) reinterpret_cast<uint32_t*>(xf + 2 * p.G * kRecBytes)[tid] = 0u;
+        if (tid < kZeroBytes / 4) reinterpret_cast<uint32_t*>(xf + 2 * G * kRecBytes)[tid] = 0u;
         gemv_mma::consumer_sync(nct);
     }
 
     const int g = lane >> 2, t = lane & 3;
     const int jg = warp >> 1;
     const bool odd = warp & 1;
-    // my 5 words of row g inside a stage (group jg, block 2t (+1)); my activation operand
+    // my 5 words of row g inside a stage (group jg, block 2t (+1)); my activation operand (the
+    // zero block, 32 bytes past its start, sits on other banks than the records read with it)
     const uint32_t aoff = static_cast<uint32_t>(jg * kBoxBytes + g * kGroupBytes + 36 * t + (odd ? 16 : 0));
     const bool diag = (g >> 1) == t;
     const uint32_t xbase = diag ? p.xf_off + static_cast<uint32_t>(warp * kRecBytes + g * 64)
-                                : p.xf_off + static_cast<uint32_t>(2 * p.G * kRecBytes);
-    const uint32_t xstep = diag ? static_cast<uint32_t>(2 * p.gps * kRecBytes) : 0u;   // per phase
+                                : p.xf_off + static_cast<uint32_t>(2 * G * kRecBytes + 32);
+    const uint32_t xstep = diag ? static_cast<uint32_t>(2 * gps * kRecBytes) : 0u;   // per phase
 
     bool ok = true;
     int s = 0, slot = 0;
     uint32_t par = 0;
-    for (int pass = 0; pass < npass; ++pass) {
-        const int ub = u0 + pass * p.up;
-        const int nrb = min(p.up, u1 - ub) * NMAT;
-        gemv_mma::consumer_sync(nct);   // the previous pass has read `red`
-        for (int rb = 0; rb < nrb; ++rb) {
-            float t0 = 0.f, t1 = 0.f;
-            uint32_t xr = xbase;
-            for (int ph = 0; ph < p.nphase; ++ph, xr += xstep) {
-                const bool mine = jg < min(p.gps, p.G - ph * p.gps);
-                if (ok) ok = mbar_wait(&full[slot], par, p.status);
-                if (mine && ok) {
-                    const uint32_t a = static_cast<uint32_t>(slot) * p.stage_bytes + aoff;
-                    if (odd) task<true>(smem, a, xr, t0, t1);
-                    else task<false>(smem, a, xr, t0, t1);
+    auto run = [&](auto odd_tag) {
+        constexpr bool ODD = decltype(odd_tag)::value;
+        for (int pass = 0; pass < npass; ++pass) {
+            const int ub = u0 + pass * p.up;
+            const int nrb = min(p.up, u1 - ub) * NMAT;
+            gemv_mma::consumer_sync(nct);   // the previous pass has read `red`
+            for (int v = 0; v * rps < nrb; ++v) {
+                const bool two = rps == 2 && 2 * v + 1 < nrb;
+                float t0[2] = {0.f, 0.f}, t1[2] = {0.f, 0.f};
+                uint32_t xr = xbase;
+                for (int ph = 0; ph < nphase; ++ph, xr += xstep) {
+                    const bool mine = jg < min(gps, G - ph * gps);
+                    if (ok) ok = mbar_wait(&full[slot], par, p.status);
+                    if (mine && ok) {
+                        const uint32_t a = static_cast<uint32_t>(slot) * stage_bytes + aoff;
+                        if (two) task<ODD, 2>(smem, a, rstride, xr, t0, t1);
+                        else task<ODD, 1>(smem, a, rstride, xr, t0, t1);
+                    }
+                    __syncwarp();
+                    if (lane == 0) gemv_mma::mbar_arrive(&empty[slot]);
+                    ++s;
+                    if (++slot == ns) {
+                        slot = 0;
+                        par ^= 1u;
+                    }
                 }
-                __syncwarp();
-                if (lane == 0) gemv_mma::mbar_arrive(&empty[slot]);
-                ++s;
-                if (++slot == p.ns) {
-                    slot = 0;
-                    par ^= 1u;
+                // rows g and g + 8 of the stage's row blocks: sum the quad's four blocks, one
+                // value per (row, warp)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    t0[r] += __shfl_xor_sync(0xffffffffu, t0[r], 1);
+                    t1[r] += __shfl_xor_sync(0xffffffffu, t1[r], 1);
+                    t0[r] += __shfl_xor_sync(0xffffffffu, t0[r], 2);
+                    t1[r] += __shfl_xor_sync(0xffffffffu, t1[r], 2);
+                }
+                if (t == 0) {
+                    const int rb = v * rps;
+                    red[(rb * kUnitRows + g) * ncw + warp] = t0[0];
+                    red[(rb * kUnitRows + g + 8) * ncw + warp] = t1[0];
+                    if (two) {
+                        red[((rb + 1) * kUnitRows + g) * ncw + warp] = t0[1];
+                        red[((rb + 1) * kUnitRows + g + 8) * ncw + warp] = t1[1];
+                    }
                 }
             }
-            // rows g and g + 8: sum the quad's four blocks, one value per (row, warp)
-            t0 += __shfl_xor_sync(0xffffffffu, t0, 1);
-            t1 += __shfl_xor_sync(0xffffffffu, t1, 1);
-            t0 += __shfl_xor_sync(0xffffffffu, t0, 2);
-            t1 += __shfl_xor_sync(0xffffffffu, t1, 2);
-            if (t == 0) {
-                red[(rb * kUnitRows + g) * ncw + warp] = t0;
-                red[(rb * kUnitRows + g + 8) * ncw + warp] = t1;
+            gemv_mma::consumer_sync(nct);   // every partial sum of the pass written
+            const float out = misc[65];
+            const int rows_in_pass = nrb * kUnitRows;
+            for (int row = tid; row < rows_in_pass; row += nct) {
+                const int rb = row / kUnitRows, r16 = row - rb * kUnitRows;
+                if (NMAT == 2 && (rb & 1)) continue;
+                const int64_t n = static_cast<int64_t>(ub + rb / NMAT) * kUnitRows + r16;
+                if (n >= p.N) continue;
+                float v = 0.f;
+                for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
+                v *= out;
+                if (NMAT == 1) {
+                    if (p.residual) v += p.residual[n];
+                } else {
+                    float uv = 0.f;
+                    for (int w = 0; w < ncw; ++w) uv += red[(row + kUnitRows) * ncw + w];
+                    v = gemv_mma::act_fn(v, p.act) * (uv * out);
+                }
+                p.y[n] = v;
             }
         }
-        gemv_mma::consumer_sync(nct);   // every partial sum of the pass written
-        const float out = misc[65];
-        const int rows_in_pass = nrb * kUnitRows;
-        for (int row = tid; row < rows_in_pass; row += nct) {
-            const int rb = row / kUnitRows, r16 = row - rb * kUnitRows;
-            if (NMAT == 2 && (rb & 1)) continue;
-            const int64_t n = static_cast<int64_t>(ub + rb / NMAT) * kUnitRows + r16;
-            if (n >= p.N) continue;
-            float v = 0.f;
-            for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
-            v *= out;
-            if (NMAT == 1) {
-                if (p.residual) v += p.residual[n];
-            } else {
-                float uv = 0.f;
-                for (int w = 0; w < ncw; ++w) uv += red[(row + kUnitRows) * ncw + w];
-                v = gemv_mma::act_fn(v, p.act) * (uv * out);
-            }
-            p.y[n] = v;
-        }
-    }
+    };
+    if (odd) run(std::true_type{});
+    else run(std::false_type{});
     if (!ok) atomicOr(&any_failed, 1);
     gemv_mma::consumer_sync(nct);
-    if (any_failed && tid == 0) drain_stages(full, p.ns, max(0, s - p.ns), s - 1);
+    if (any_failed && tid == 0) drain_stages(full, ns, max(0, s - ns), s - 1);
 }
 
 }  // namespace gemv_b1

@@ -3,6 +3,8 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "gem_internal.h"
 
@@ -80,6 +82,19 @@ gem_status make_tensor_map_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const 
 
 gem_status launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                       void** args) {
+    // Every kernel of the library asks for the largest shared-memory carveout, so consecutive
+    // launches never need the SM's L1/shared split changed (which would keep a dependent launch
+    // from starting on an SM until the previous kernel has drained from it).
+    {
+        static std::mutex mu;
+        static std::set<std::pair<int, const void*>> done;
+        int dev = 0;
+        GEM_CUDA_TRY(cudaGetDevice(&dev));
+        std::lock_guard<std::mutex> lk(mu);
+        if (done.insert({dev, kernel}).second)
+            GEM_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                              cudaSharedmemCarveoutMaxShared));
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -80,6 +80,8 @@ GEMV_CASES = [
     (6144, 2048, 8), (2560, 9728, 8), (1, 256, 1),
     (40000, 512, 2), (40000, 512, 6),   # more 16-row units per CTA than one pass holds
     (300, 21504, 3),                    # long K: several activation phases
+    (1000, 21504, 1), (2560, 9728, 1),  # one row: 12 phases; a ragged last phase (38 groups)
+    (8, 8192, 1), (40000, 512, 1),      # one row: half a row-block pair; several passes
 ]
 
 

@@ -41,6 +41,7 @@ constexpr int kMaxConsumerWarps = 18;
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kRecBytes = 512;   // activation record of one half group: 8 columns x 8 tiles x 8 B
 constexpr int kZeroBytes = 96;   // the operand of lanes off the block diagonal (bytes 32..95)
+constexpr int kPro = 4;          // float4s of the activation row kept per consumer thread
 
 struct Params {
     int64_t N;
@@ -63,11 +64,15 @@ struct Params {
 };
 
 // qs byte held in byte j of code word i of a lane's block.  Odd blocks: word i = bytes 4i..4i+3.
-// Even blocks: word 0 = bytes {0, 1, 14, 15} (the two 2-byte tails), word i >= 1 = 4i-2 .. 4i+1.
+// Even blocks: word i = bytes 4i-2 .. 4i+1 mod 16 (word 0 = {14, 15, 0, 1}: the two 2-byte tails).
 __device__ __forceinline__ int code_byte(bool odd, int i, int j) {
-    if (odd) return 4 * i + j;
-    if (i == 0) return j < 2 ? j : 12 + j;
-    return 4 * i - 2 + j;
+    return odd ? 4 * i + j : (4 * i + j + 14) & 15;
+}
+// The inverse: code word and byte of qs byte m.
+__device__ __forceinline__ void code_slot(bool odd, int m, int& i, int& j) {
+    const int mm = odd ? m : (m + 2) & 15;
+    i = mm >> 2;
+    j = mm & 3;
 }
 
 // One task: rows g and g + 8 of one block per lane in each of NR row blocks (the same K range,
@@ -102,8 +107,8 @@ __device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t r
             da[r] = __high2float(*reinterpret_cast<const __half2*>(&ra[0]));
             db[r] = __high2float(*reinterpret_cast<const __half2*>(&rb[0]));
         } else {
-            ca[r][0] = __byte_perm(ra[0], ra[4], 0x5432);
-            cb[r][0] = __byte_perm(rb[0], rb[4], 0x5432);
+            ca[r][0] = __byte_perm(ra[0], ra[4], 0x3254);   // qs 14, 15 (word 4), qs 0, 1 (word 0)
+            cb[r][0] = __byte_perm(rb[0], rb[4], 0x3254);
 #pragma unroll
             for (int i = 1; i < 4; ++i) {
                 ca[r][i] = ra[i];
@@ -219,21 +224,35 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     pdl_trigger();
     pdl_wait();   // the activations (and residual) come from the previous kernel
 
-    const int K = G * 256;
+    const int K = G * 256, K4 = K / 4;
+    // Rows of up to kPro float4 per consumer thread are read once and kept in registers; longer
+    // ones are read twice (statistics, then the records).
+    const bool onepass = K4 <= kPro * nct;
+    float4 xv[kPro];
     // 1. largest |gamma * x| and sum of x^2 over the row
     {
         float mx = 0.f, ss = 0.f;
         const float4* x4 = reinterpret_cast<const float4*>(p.x);
         const float4* g4 = reinterpret_cast<const float4*>(p.gamma);
-#pragma unroll 4
-        for (int i = tid; i < K / 4; i += nct) {
-            float4 v = __ldg(x4 + i);
+        auto take = [&](float4 v, int i) {
             ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             if (p.gamma) {
                 const float4 gm = __ldg(g4 + i);
                 v.x *= gm.x; v.y *= gm.y; v.z *= gm.z; v.w *= gm.w;
             }
             mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            return v;
+        };
+        if (onepass) {
+#pragma unroll
+            for (int u = 0; u < kPro; ++u) {
+                const int i = tid + u * nct;
+                xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < K4) xv[u] = take(__ldg(x4 + i), i);
+            }
+        } else {
+#pragma unroll 4
+            for (int i = tid; i < K4; i += nct) (void)take(__ldg(x4 + i), i);
         }
         mx = warp_max(mx);
         ss = warp_sum(ss);
@@ -262,42 +281,68 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     // 2. activation records: record (hg, column 2t + h), tile tau, register r holds the h part of
     // the two elements of block 2t + (hg & 1) of group hg / 2 that lane t's k-slots of that register
     // meet in the A operand (bytes j = r and r + 2 of code word tau / 2, nibble tau & 1).
-    // Four registers per thread and round, their loads issued before any conversion.
+    uint8_t* xf = smem + p.xf_off;
     {
         const float sc = misc[64];
-        uint8_t* xf = smem + p.xf_off;
-        const int nreg = 2 * G * 64;   // (hg, t, tau, r)
-        for (int i0 = tid; i0 < nreg; i0 += 4 * nct) {
-            float v0[4], v1[4];
-            uint32_t off[4];
+        if (onepass) {
+            // scatter my float4s: element m of a block's nibble half goes to the slot of qs byte m
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * nct;
-                v0[u] = v1[u] = 0.f;
-                off[u] = 0;
-                if (i < nreg) {
-                    const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
-                    const bool odd = hg & 1;
-                    const int base = (hg >> 1) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
-                    const int k0 = base + code_byte(odd, tau >> 1, r);
-                    const int k1 = base + code_byte(odd, tau >> 1, r + 2);
-                    v0[u] = __ldg(p.x + k0);
-                    v1[u] = __ldg(p.x + k1);
-                    if (p.gamma) {
-                        v0[u] *= __ldg(p.gamma + k0);
-                        v1[u] *= __ldg(p.gamma + k1);
+            for (int u = 0; u < kPro; ++u) {
+                const int i = tid + u * nct;
+                if (i < K4) {
+                    const int k0 = 4 * i;
+                    const int blk = (k0 >> 5) & 7, e0 = k0 & 31;
+                    const bool odd = blk & 1;
+                    const uint32_t rec = static_cast<uint32_t>((2 * (k0 >> 8) + (odd ? 1 : 0)) * kRecBytes +
+                                                               (blk >> 1) * 128 + (e0 >> 4) * 8);
+                    const float v4[4] = {xv[u].x * sc, xv[u].y * sc, xv[u].z * sc, xv[u].w * sc};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        int ci, cj;
+                        code_slot(odd, (e0 & 15) + e, ci, cj);
+                        const uint32_t off = rec + ci * 16 + (cj & 1) * 4 + (cj >> 1) * 2;
+                        __half h, l;
+                        split_hi_lo(v4[e], h, l);
+                        *reinterpret_cast<__half*>(xf + off) = h;
+                        *reinterpret_cast<__half*>(xf + off + 64) = l;
                     }
-                    off[u] = static_cast<uint32_t>(hg * kRecBytes + (2 * t) * 64 + tau * 8 + r * 4);
                 }
             }
+        } else {
+            // gather: four registers per thread and round, their loads issued before converting
+            const int nreg = 2 * G * 64;   // (hg, t, tau, r)
+            for (int i0 = tid; i0 < nreg; i0 += 4 * nct) {
+                float v0[4], v1[4];
+                uint32_t off[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (i0 + u * nct < nreg) {
-                    __half h0, l0, h1, l1;
-                    split_hi_lo(v0[u] * sc, h0, l0);
-                    split_hi_lo(v1[u] * sc, h1, l1);
-                    *reinterpret_cast<__half2*>(xf + off[u]) = __halves2half2(h0, h1);
-                    *reinterpret_cast<__half2*>(xf + off[u] + 64) = __halves2half2(l0, l1);
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * nct;
+                    v0[u] = v1[u] = 0.f;
+                    off[u] = 0;
+                    if (i < nreg) {
+                        const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
+                        const bool odd = hg & 1;
+                        const int base = (hg >> 1) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
+                        const int k0 = base + code_byte(odd, tau >> 1, r);
+                        const int k1 = base + code_byte(odd, tau >> 1, r + 2);
+                        v0[u] = __ldg(p.x + k0);
+                        v1[u] = __ldg(p.x + k1);
+                        if (p.gamma) {
+                            v0[u] *= __ldg(p.gamma + k0);
+                            v1[u] *= __ldg(p.gamma + k1);
+                        }
+                        off[u] = static_cast<uint32_t>(hg * kRecBytes + (2 * t) * 64 + tau * 8 + r * 4);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (i0 + u * nct < nreg) {
+                        __half h0, l0, h1, l1;
+                        split_hi_lo(v0[u] * sc, h0, l0);
+                        split_hi_lo(v1[u] * sc, h1, l1);
+                        *reinterpret_cast<__half2*>(xf + off[u]) = __halves2half2(h0, h1);
+                        *reinterpret_cast<__half2*>(xf + off[u] + 64) = __halves2half2(l0, l1);
+                    }
                 }
             }
         }

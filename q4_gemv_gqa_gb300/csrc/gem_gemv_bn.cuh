@@ -1,0 +1,389 @@
+// gem_gemv_bn.cuh — Q4_0 GEMV for 2..8 activation rows on mma.sync, with the activations
+// converted once per call into mma operand records (not once per CTA).
+//
+// act_prep_kernel turns x (optionally RMSNorm-weighted: gamma * x, the 1/rms factor being applied
+// to the output) into binary16 hi + lo operand records in global memory, with one power of two per
+// row that takes its largest magnitude to [2^13, 2^14).  The GEMV kernel then walks K phase by
+// phase: at the start of a phase each consumer warp takes its half group's operands (32 registers)
+// from a record buffer in shared memory and keeps them for every row block of the phase; the
+// producer bulk-copies the next phase's records into the buffer as soon as every warp has taken
+// its operands (long before they are needed), and streams weights through the usual TMA ring.
+//
+// MMA mapping (m16n8k16, f16 x f16 -> f32): A = 16 weight rows x 16 codes of one block (low
+// nibbles: k-tile 0, high nibbles: k-tile 1), B = the same 16 codes' activations x 8 columns (the
+// activation rows, hi and lo parts in two separate mma), so D[row][b] of one block is scaled by
+// the row's block scale d before it is summed.  A half group is the 4 even or the 4 odd blocks of
+// a 256-weight group (as in the one-row kernel): odd blocks give each lane an aligned code word,
+// even ones one byte permute of two words.
+//
+// Reference: "Q4_0 dequant-matvec" (GGML block: fp16 d, 16 bytes of codes, value (q - 8) * d).
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "gem_gemv_b1.cuh"
+
+namespace gem {
+namespace gemv_bn {
+
+using gemv_mma::kBoxBytes;
+using gemv_mma::kGroupBytes;
+using gemv_mma::kMaxSlots;
+using gemv_mma::kUnitRows;
+
+constexpr int kMaxConsumerWarps = 18;
+constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+constexpr int kEntryBytes = 32;                    // one lane's hi (16 B) and lo (16 B) operands of one block
+constexpr int kHgBytes = 4 * 32 * kEntryBytes;     // one half group: 4 blocks x 32 lanes
+constexpr int kPrepThreads = 256;
+
+// Records: [hg][j][lane][hi uint4, lo uint4]; lane (g, t) = activation row g, k-slot t.  For block
+// 2j + (hg & 1) of group hg / 2, register r of k-tile tau holds the two elements whose codes sit in
+// bytes r and r + 2 of code word t (nibble tau): the operand layout the weights' A fragments meet.
+// rowinfo[b] = {2^e_b, 2^-e_b (* 1/rms of row b when gamma is given)}.
+struct PrepParams {
+    const float* x;
+    int64_t ldx;
+    const float* gamma;
+    float eps;
+    int G;
+    int B;
+    int nchunk;          // CTAs per activation row
+    uint8_t* rec;
+    float2* rowinfo;
+};
+
+__global__ void __launch_bounds__(kPrepThreads) act_prep_kernel(const PrepParams p) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red_m[kPrepThreads / 32], red_s[kPrepThreads / 32];
+    __shared__ float sc_sh;
+    const int b = blockIdx.y, chunk = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.G * 256;
+    const float* xr = p.x + b * p.ldx;
+    float mx = 0.f, ss = 0.f;
+    for (int i = tid; i < K / 4; i += kPrepThreads) {
+        float4 v = __ldg(reinterpret_cast<const float4*>(xr) + i);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        if (p.gamma) {
+            const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma) + i);
+            v.x *= gm.x; v.y *= gm.y; v.z *= gm.z; v.w *= gm.w;
+        }
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    mx = warp_max(mx);
+    ss = warp_sum(ss);
+    if (lane == 0) {
+        red_m[warp] = mx;
+        red_s[warp] = ss;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float m = 0.f, q = 0.f;
+        for (int w = 0; w < kPrepThreads / 32; ++w) {
+            m = fmaxf(m, red_m[w]);
+            q += red_s[w];
+        }
+        int e = 0;
+        if (m > 0.f) e = 13 - (((__float_as_int(m) >> 23) & 0xff) - 127);
+        e = max(-126, min(126, e));
+        sc_sh = __int_as_float((127 + e) << 23);
+        if (chunk == 0) {
+            float out = __int_as_float((127 - e) << 23);
+            if (p.gamma) out *= rsqrtf(q / static_cast<float>(K) + p.eps);
+            p.rowinfo[b] = make_float2(__int_as_float((127 + e) << 23), out);
+        }
+    }
+    __syncthreads();
+    const float sc = sc_sh;
+    // entries (hg, j, t) of row b, this CTA's contiguous share
+    const int nent = 2 * p.G * 16;
+    const int e0 = static_cast<int>((static_cast<int64_t>(chunk) * nent) / p.nchunk);
+    const int e1 = static_cast<int>((static_cast<int64_t>(chunk + 1) * nent) / p.nchunk);
+    for (int e = e0 + tid; e < e1; e += kPrepThreads) {
+        const int hg = e >> 4, j = (e >> 2) & 3, t = e & 3;
+        const bool odd = hg & 1;
+        const int base = (hg >> 1) * 256 + (2 * j + (odd ? 1 : 0)) * 32;
+        float v[8];   // tile 0: bytes 0, 2, 1, 3 of code word t; tile 1: the same + 16
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int jj = (u & 3) == 1 ? 2 : ((u & 3) == 2 ? 1 : (u & 3));
+            const int k = base + gemv_b1::code_byte(odd, t, jj) + (u >> 2) * 16;
+            v[u] = __ldg(xr + k) * (p.gamma ? __ldg(p.gamma + k) : 1.f) * sc;
+        }
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            __half h0, l0, h1, l1;
+            split_hi_lo(v[2 * r], h0, l0);
+            split_hi_lo(v[2 * r + 1], h1, l1);
+            const __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
+            hw[r] = *reinterpret_cast<const uint32_t*>(&hh);
+            lw[r] = *reinterpret_cast<const uint32_t*>(&ll);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.rec + (static_cast<size_t>(hg * 4 + j) * 32 + (b * 4 + t)) * kEntryBytes);
+        dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        dst[1] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+}
+
+struct Params {
+    int64_t N;
+    int G;
+    int B;
+    float* y;
+    int64_t ldy;
+    const float* residual;
+    int64_t ldr;
+    const uint8_t* rec;
+    const float2* rowinfo;
+    int act;
+    int U, up, gps, nphase, ns, ncw, rps;
+    uint32_t stage_bytes, full_off, empty_off, rfull_off, rempty_off, xf_off, red_off;
+    int* status;
+};
+
+// One task: the 4 blocks of my half group in rows g and g + 8 of one row block, all B columns.
+// a = shared offset of row g, group jg, plus 16 for odd blocks; acc += d * D per block.
+template <bool ODD>
+__device__ __forceinline__ void task_bn(const uint8_t* smem, uint32_t a, int t, uint32_t sel, const uint4 (&xh)[4],
+                                        const uint4 (&xl)[4], float (&acc)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[2];
+        float dsc[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t* rg = smem + a + h * 8 * kGroupBytes + 36 * j;
+            const uint32_t d0 = *reinterpret_cast<const uint32_t*>(rg);
+            if constexpr (ODD) {
+                w[h] = *reinterpret_cast<const uint32_t*>(rg + 4 + 4 * t);
+                dsc[h] = __high2float(*reinterpret_cast<const __half2*>(&d0));
+            } else {
+                const uint32_t wa = *reinterpret_cast<const uint32_t*>(rg + 4 * t);
+                const uint32_t wb = *reinterpret_cast<const uint32_t*>(rg + 16);
+                w[h] = __byte_perm(wa, wb, sel);
+                dsc[h] = __low2float(*reinterpret_cast<const __half2*>(&d0));
+            }
+        }
+        uint32_t l02, l13, h02, h13, m02, m13, n02, n13;
+        gemv_mma::dequant_word(w[0], l02, l13, h02, h13);
+        gemv_mma::dequant_word(w[1], m02, m13, n02, n13);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(c, l02, m02, l13, m13, xh[j].x, xh[j].y);
+        mma_16816(c, h02, n02, h13, n13, xh[j].z, xh[j].w);
+        mma_16816(c, l02, m02, l13, m13, xl[j].x, xl[j].y);
+        mma_16816(c, h02, n02, h13, n13, xl[j].z, xl[j].w);
+        acc[0] = fmaf(dsc[0], c[0], acc[0]);
+        acc[1] = fmaf(dsc[0], c[1], acc[1]);
+        acc[2] = fmaf(dsc[1], c[2], acc[2]);
+        acc[3] = fmaf(dsc[1], c[3], acc[3]);
+    }
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+template <int NMAT>
+__global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __grid_constant__ CUtensorMap tm0,
+                                                                      const __grid_constant__ CUtensorMap tm1,
+                                                                      const Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.full_off);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + p.empty_off);
+    uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + p.rfull_off);
+    uint64_t* rempty = reinterpret_cast<uint64_t*>(smem + p.rempty_off);
+    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [rb][warp][lane][4]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ncw = p.ncw, nct = ncw * 32;
+    const int G = p.G, gps = p.gps, nphase = p.nphase, ns = p.ns, rps = p.rps;
+    const uint32_t stage_bytes = p.stage_bytes;
+    const uint32_t rstride = static_cast<uint32_t>(gps * kBoxBytes);
+    const uint32_t rec_phase = static_cast<uint32_t>(2 * gps * kHgBytes);   // one record buffer
+    const int C = gridDim.x, c = blockIdx.x;
+    const int u0 = static_cast<int>((static_cast<int64_t>(c) * p.U) / C);
+    const int u1 = static_cast<int>((static_cast<int64_t>(c + 1) * p.U) / C);
+    const int npass = (u1 - u0 + p.up - 1) / p.up;
+
+    __shared__ int any_failed;
+    if (tid == 0) {
+        any_failed = 0;
+        for (int i = 0; i < ns; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], ncw);
+        }
+        mbar_init(rfull, 1);
+        mbar_init(rempty, ncw);
+        fence_mbar_init();
+        prefetch_tensormap(&tm0);
+        if (NMAT == 2) prefetch_tensormap(&tm1);
+    }
+    __syncthreads();
+
+    // ---------------- producer warp ----------------
+    // Order: (pass, phase, row-block tuple).  Each phase's records go out before its weight
+    // stages; the first stages of the first phase go out before griddepcontrol.wait (the weights
+    // are not written by earlier kernels, the records are).
+    if (warp == ncw) {
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            bool ok = true;
+            int s = 0, slot = 0;
+            uint32_t par = 1;
+            int pre = 0;   // stages issued before the wait
+            auto issue = [&](int pass, int ph, int v) -> bool {
+                const int ub = u0 + pass * p.up;
+                const int nrb = min(p.up, u1 - ub) * NMAT;
+                const int nr = min(rps, nrb - v * rps);
+                const int g0 = ph * gps;
+                const int ng = min(gps, G - g0);
+                if (s == ns) pdl_trigger();
+                if (s >= ns && !mbar_wait(&empty[slot], par, p.status)) return false;
+                uint8_t* dst = smem + static_cast<size_t>(slot) * stage_bytes;
+                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nr * ng * kBoxBytes));
+                for (int r = 0; r < nr; ++r) {
+                    const int rb = v * rps + r;
+                    const int row0 = (ub + rb / NMAT) * kUnitRows;
+                    const CUtensorMap* tm = (NMAT == 2 && (rb & 1)) ? &tm1 : &tm0;
+                    for (int j = 0; j < ng; ++j)
+                        tma_load_2d(dst + r * rstride + j * kBoxBytes, tm, (g0 + j) * kGroupBytes, row0, &full[slot],
+                                    policy);
+                }
+                ++s;
+                if (++slot == ns) {
+                    slot = 0;
+                    par ^= 1u;
+                }
+                return true;
+            };
+            {
+                const int nrb0 = min(p.up, u1 - u0) * NMAT;
+                const int nv0 = (nrb0 + rps - 1) / rps;
+                for (int v = 0; v < nv0 && pre < ns; ++v, ++pre) (void)issue(0, 0, v);
+            }
+            pdl_wait();
+            int q = 0;
+            for (int pass = 0; pass < npass && ok; ++pass) {
+                const int ub = u0 + pass * p.up;
+                const int nrb = min(p.up, u1 - ub) * NMAT;
+                const int nv = (nrb + rps - 1) / rps;
+                for (int ph = 0; ph < nphase && ok; ++ph, ++q) {
+                    // the buffer is free once every warp holds phase q - 1's operands
+                    if (q >= 1 && !(ok = mbar_wait(rempty, (q - 1) & 1, p.status))) break;
+                    const int ng = min(gps, G - ph * gps);
+                    const uint32_t bytes = static_cast<uint32_t>(2 * ng * kHgBytes);
+                    mbar_arrive_expect_tx(rfull, bytes);
+                    bulk_load(smem + p.xf_off, p.rec + static_cast<size_t>(ph) * rec_phase, bytes, rfull);
+                    for (int v = (q == 0 ? pre : 0); v < nv && ok; ++v) ok = issue(pass, ph, v);
+                }
+            }
+            if (s <= ns) pdl_trigger();
+            if (!ok) drain_stages(full, ns, max(0, s - ns), s - 1);
+        } else {
+            pdl_trigger();
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    pdl_trigger();
+    pdl_wait();   // row scales (and the residual) come from earlier kernels
+
+    const int g = lane >> 2, t = lane & 3;
+    const int jg = warp >> 1;
+    const bool odd = warp & 1;
+    const bool col = g < p.B;   // activation row g exists
+    const uint32_t aoff = static_cast<uint32_t>(jg * kBoxBytes + g * kGroupBytes + (odd ? 16 : 0));
+    const uint32_t sel = t == 0 ? 0x3254u : 0x3210u;   // even blocks: word 0 joins the two tails
+
+    bool ok = true;
+    int s = 0, slot = 0;
+    uint32_t par = 0;
+    auto run = [&](auto odd_tag) {
+        constexpr bool ODD = decltype(odd_tag)::value;
+        int q = 0;
+        for (int pass = 0; pass < npass; ++pass) {
+            const int ub = u0 + pass * p.up;
+            const int nrb = min(p.up, u1 - ub) * NMAT;
+            const int nv = (nrb + rps - 1) / rps;
+            gemv_mma::consumer_sync(nct);   // the previous pass has read `red`
+            for (int ph = 0; ph < nphase; ++ph, ++q) {
+                const bool mine = jg < min(gps, G - ph * gps);
+                if (ok) ok = mbar_wait(rfull, q & 1, p.status);
+                uint4 xh[4], xl[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xh[j] = xl[j] = make_uint4(0u, 0u, 0u, 0u);
+                if (mine && col && ok) {
+                    const uint4* e = reinterpret_cast<const uint4*>(smem + p.xf_off + (warp * 4 * 32 + lane) * kEntryBytes);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        xh[j] = e[j * 32 * 2];
+                        xl[j] = e[j * 32 * 2 + 1];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) gemv_mma::mbar_arrive(rempty);   // operands now in registers
+                for (int v = 0; v < nv; ++v) {
+                    if (ok) ok = mbar_wait(&full[slot], par, p.status);
+                    if (mine && ok) {
+                        const int nr = min(rps, nrb - v * rps);
+                        for (int r = 0; r < nr; ++r) {
+                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                            task_bn<ODD>(smem, static_cast<uint32_t>(slot) * stage_bytes + r * rstride + aoff, t, sel,
+                                         xh, xl, acc);
+                            float4* rr = reinterpret_cast<float4*>(red) + ((v * rps + r) * ncw + warp) * 32 + lane;
+                            if (ph) {
+                                const float4 o = *rr;
+                                acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+                            }
+                            *rr = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) gemv_mma::mbar_arrive(&empty[slot]);
+                    ++s;
+                    if (++slot == ns) {
+                        slot = 0;
+                        par ^= 1u;
+                    }
+                }
+            }
+            gemv_mma::consumer_sync(nct);   // every partial sum of the pass written
+            const int B = p.B;
+            const int items = nrb * kUnitRows * B;
+            for (int idx = tid; idx < items; idx += nct) {
+                const int rb = idx / (kUnitRows * B), rem = idx - rb * (kUnitRows * B);
+                const int r16 = rem / B, b = rem - r16 * B;
+                if (NMAT == 2 && (rb & 1)) continue;
+                const int64_t n = static_cast<int64_t>(ub + rb / NMAT) * kUnitRows + r16;
+                if (n >= p.N) continue;
+                const int ln = (r16 & 7) * 4 + (b >> 1), comp = (r16 >> 3) * 2 + (b & 1);
+                float v = 0.f;
+                for (int w = 0; w < ncw; ++w) v += red[((rb * ncw + w) * 32 + ln) * 4 + comp];
+                const float out = p.rowinfo[b].y;
+                v *= out;
+                if (NMAT == 1) {
+                    if (p.residual) v += p.residual[b * p.ldr + n];
+                } else {
+                    float uv = 0.f;
+                    for (int w = 0; w < ncw; ++w) uv += red[(((rb + 1) * ncw + w) * 32 + ln) * 4 + comp];
+                    v = gemv_mma::act_fn(v, p.act) * (uv * out);
+                }
+                p.y[b * p.ldy + n] = v;
+            }
+        }
+    };
+    if (odd) run(std::true_type{});
+    else run(std::false_type{});
+    if (!ok) atomicOr(&any_failed, 1);
+    gemv_mma::consumer_sync(nct);
+    if (any_failed && tid == 0) drain_stages(full, ns, max(0, s - ns), s - 1);
+}
+
+}  // namespace gemv_bn
+}  // namespace gem

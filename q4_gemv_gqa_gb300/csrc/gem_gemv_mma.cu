@@ -33,9 +33,10 @@ gem_status ensure_smem_mma(const void* fn, int device, size_t bytes) {
 // Plan and launch; the caller has checked the op and that the fast-path conditions hold
 // (K % 256 == 0, 16-byte aligned matrices and activation rows).
 gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di) {
-    if (op.B == 1) {
+    {
         bool planned = false;
-        const gem_status st1 = gemv_enqueue_b1(op, stream, di, &planned);
+        const gem_status st1 = op.B == 1 ? gemv_enqueue_b1(op, stream, di, &planned)
+                                         : gemv_enqueue_bn(op, stream, di, &planned);
         if (planned || st1 != GEM_OK) return st1;
     }
     const int nmat = op.W1 ? 2 : 1;

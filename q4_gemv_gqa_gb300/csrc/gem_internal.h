@@ -52,6 +52,8 @@ struct GemvOp {
     const float* norm_gamma;              // nullable: RMSNorm x first (gamma over K)
     float eps;
     int act;                              // pair mode: 0 SiLU, 1 GELU-tanh
+    void* act_ws;                         // nullable: operand records of a 2..8-row call
+    size_t act_ws_bytes;                  //   (gemv_rec_bytes); else the library's own array
 };
 gem_status gemv_check(const GemvOp& op);
 gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream);
@@ -60,6 +62,13 @@ gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceI
 // One-row (B = 1) tensor-core kernel; *planned = false when K is too long for its shared-memory
 // layout (nothing launched).
 gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, bool* planned);
+// 2..8 rows: activation prep kernel + tensor-core kernel over operand records; *planned = false
+// when no layout fits (nothing launched).  Records live in op.act_ws when it holds
+// gemv_rec_bytes(B, K), else in a library-owned per-device array of kGemvRecScratchBytes (shared
+// by every call on the device: calls on concurrently running streams must not both use it).
+constexpr size_t kGemvRecScratchBytes = size_t(4) << 20;
+size_t gemv_rec_bytes(int B, int64_t K);
+gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, bool* planned);
 
 // ---- norms / RoPE / activation -------------------------------------------------------------
 struct RopeOp {

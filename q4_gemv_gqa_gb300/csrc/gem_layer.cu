@@ -14,6 +14,8 @@
 //   6  down GEMV with the residual add fused (post_norms: down GEMV, then norm + residual)
 // Every kernel requests its weights (or cached K/V rows) before griddepcontrol.wait, so
 // each launch's HBM stream starts while its predecessor is still running.
+#include <algorithm>
+
 #include "gem_internal.h"
 
 namespace gem {
@@ -23,6 +25,8 @@ struct LayerWs {
     float *qkv, *attn, *act, *tmp;
     void* attn_ws;
     size_t attn_ws_bytes;
+    void* rec;            // GEMV operand records (2..8 rows), shared by the layer's GEMVs in turn
+    size_t rec_bytes;
     size_t total;
 };
 
@@ -42,6 +46,9 @@ LayerWs layout(const gem_layer_desc* L, int B, int64_t cap, void* base) {
     w.attn_ws_bytes = attn_workspace_bytes(B, static_cast<int>(L->n_q), static_cast<int>(L->n_kv),
                                            static_cast<int>(L->d), cap, L->window);
     w.attn_ws = take(w.attn_ws_bytes);
+    const int64_t kmax = std::max<int64_t>(std::max<int64_t>(L->H, L->n_q * L->d), L->F);
+    w.rec_bytes = gemv_rec_bytes(B, kmax);
+    w.rec = w.rec_bytes ? take(w.rec_bytes) : nullptr;
     w.total = off;
     return w;
 }
@@ -91,6 +98,10 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
     GemvOp gateup{L->w_gate, L->w_up, F, H, B, x, H, w.act, F, nullptr, 0, L->g_ffn, L->eps, L->act};
     GemvOp down{L->w_down, nullptr, H, F, B, w.act, F, L->post_norms ? w.tmp : x, H,
                 L->post_norms ? nullptr : x, H, nullptr, 0.f, 0};
+    for (GemvOp* op : {&qkv, &oproj, &gateup, &down}) {
+        op->act_ws = w.rec;
+        op->act_ws_bytes = w.rec_bytes;
+    }
     RopeOp rope{};
     rope.qkv = w.qkv;
     rope.ldqkv = nqkv;

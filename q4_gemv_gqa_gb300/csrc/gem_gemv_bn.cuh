@@ -326,6 +326,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                         xl[j] = e[j * 32 * 2 + 1];
                     }
                 }
+                // The next bulk copy into the buffer (async proxy) may follow the arrive at once:
+                // order my reads of it (generic proxy) before that write.
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) gemv_mma::mbar_arrive(rempty);   // operands now in registers
                 for (int v = 0; v < nv; ++v) {

@@ -84,6 +84,10 @@ GEM_API gem_status gem_device_status(int32_t *flags, int reset);
  *   x        [B][ldx] fp32, ldx >= K.       y  [B][ldy] fp32, ldy >= N.
  *   residual nullable, [B][ldy] fp32; may alias y (read before write, element-wise).
  *   Accumulation is fp32.  y must not overlap W or x.
+ *   For B >= 2 the call converts x into tensor-core operand records first (a second launch on the
+ *   same stream), kept in a library-owned array of 4 MiB per device (K <= 130816): calls on two
+ *   streams of one device that may run at the same time must not both have B >= 2.
+ *   gem_decode_layer keeps its records in its own workspace instead.
  */
 GEM_API gem_status gem_q4_0_gemv(const void *W, int64_t N, int64_t K, const float *x, int64_t ldx,
                          int B, float *y, int64_t ldy, const float *residual, void *stream);

@@ -61,7 +61,53 @@ struct AttnParams {
     float eps;
     int rope_dim, v_mode;
     uint16_t *k_out, *v_out;
+    // flash kernel: the grid's splits of one (sequence, KV head) form a thread-block cluster and
+    // merge their states through distributed shared memory (no partials, no merge launch)
+    int cluster;
 };
+
+constexpr int kMaxClusterSplits = 16;   // largest cluster the flash splits of one KV head form
+
+// Every thread of every CTA of the cluster arrives, then waits (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Cluster merge of the splits of one (sequence, KV head): CTA `rank` combines output elements
+// [rank * chunk, ...) of the G heads, over splits 0 .. nsplit - 1 in ascending order:
+// M = max_s m_s,  out = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.  exp = this CTA's export
+// area [G][D + 2] (o[0..D), m, l), filled before the call by CTAs with split < nsplit.
+// Every CTA of the cluster calls it exactly once (it holds two cluster barriers).
+__device__ void cluster_merge(const float* exp, int G, int D, int nsplit, uint32_t rank, uint32_t csize,
+                              float* out) {
+    cluster_sync_all();   // every split's export written
+    const int n = nsplit > 1 ? G * D : 0;   // one split: its CTA wrote the output itself
+    const int chunk = (n + static_cast<int>(csize) - 1) / static_cast<int>(csize);
+    const int lo = static_cast<int>(rank) * chunk, hi = min(n, lo + chunk);
+    for (int e = lo + static_cast<int>(threadIdx.x); e < hi; e += static_cast<int>(blockDim.x)) {
+        const int h = e / D, i = e - h * D;
+        const float* eh = exp + h * (D + 2);
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, ld_cluster_f32(eh + D, static_cast<uint32_t>(sp)));
+        float L = 0.f, O = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const float f = expf(ld_cluster_f32(eh + D, static_cast<uint32_t>(sp)) - M);
+            L = fmaf(f, ld_cluster_f32(eh + D + 1, static_cast<uint32_t>(sp)), L);
+            O = fmaf(f, ld_cluster_f32(eh + i, static_cast<uint32_t>(sp)), O);
+        }
+        out[static_cast<int64_t>(h) * D + i] = O / L;
+    }
+    cluster_sync_all();   // peers are done reading this CTA's export
+}
 
 __host__ __device__ __forceinline__ int tile_slots(int d) { return d <= 64 ? 128 : (d <= 128 ? 64 : 32); }
 
@@ -392,9 +438,14 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     const int T = P.window ? min(P.window, p + 1) : p + 1;
     int nsplit, t0, t1;
     split_range(T, kFlashTile, P.nsplit_max, split, nsplit, t0, t1);
-    if (split >= nsplit) {
+    // cluster merge: export area after the combine buffers (inside the idle rings)
+    float* cexp = reinterpret_cast<float*>(smem) + 2 * kFlashWarps * 4 + kFlashWarps * 4 * D;
+    if (split >= nsplit) {   // no tiles in this split (short prefix)
         pdl_trigger();
         if (P.early) pdl_wait();
+        if (P.cluster)
+            cluster_merge(cexp, G, D, nsplit, static_cast<uint32_t>(split), gridDim.x,
+                          P.out + b * P.ldo + static_cast<int64_t>(g * G) * D);
         return;
     }
     const int ntile = t1 - t0;
@@ -656,6 +707,12 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
         const int hg = g * G + h;
         if (nsplit == 1) {
             P.out[b * P.ldo + static_cast<int64_t>(hg) * D + i] = O / L;
+        } else if (P.cluster) {
+            cexp[h * (D + 2) + i] = O;
+            if (i == 0) {
+                cexp[h * (D + 2) + D] = M;
+                cexp[h * (D + 2) + D + 1] = L;
+            }
         } else {
             float* dst = P.part + ((static_cast<int64_t>(b) * P.n_q + hg) * P.nsplit_max + split) * (D + 2);
             dst[i] = O;
@@ -665,6 +722,9 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
             }
         }
     }
+    if (P.cluster)
+        cluster_merge(cexp, G, D, nsplit, static_cast<uint32_t>(split), gridDim.x,
+                      P.out + b * P.ldo + static_cast<int64_t>(g * G) * D);
 }
 
 // Ordered merge of split states:  M = max_s m_s,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s
@@ -738,6 +798,7 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const AttnPara
 
 struct Plan {
     bool flash;
+    bool cluster;   // flash splits merged inside a thread-block cluster (no workspace)
     int tp, nsplit_max, ltile, ns;
     uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off;
     size_t smem, ws;
@@ -745,7 +806,61 @@ struct Plan {
 
 bool use_flash(int n_q, int n_kv, int d) { return d <= 256 && n_q / n_kv <= 4; }
 
-Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num_sms) {
+size_t flash_smem(int d) {
+    const size_t ring = static_cast<size_t>(kFlashWarps) * kFlashStages * 2 * kFlashTile * d * 2;
+    // + the fused path's rotated query heads, K row, rotation table and new K/V rows (28 d bytes)
+    return align_up(ring + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2 + 28ull * d, 1024) + 1024;
+}
+
+const void* pick(int d, bool flash);
+gem_status ensure_smem_attn(const void* fn, int device, size_t bytes);
+
+// Largest cluster of flash CTAs (16, non-portable, or 8) the device can schedule for head
+// dimension d; 1 when none.  Queried once per (device, d).  Used for d <= 128 only: at d = 256
+// (two CTAs per SM) the clustered splits measured slower than the merge launch (Gemma
+// sliding-window layer, 16 KV heads x 1024 slots: 19.3 us against 12.3 us).
+int flash_cluster_max(int d, int device) {
+    if (d > 128) return 1;
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> done;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find({device, d});
+    if (it != done.end()) return it->second;
+    int best = 1;
+    const void* fn = pick(d, true);
+    const size_t smem = flash_smem(d);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess) {
+        for (int cs : {kMaxClusterSplits, 8}) {
+            if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+                (void)cudaGetLastError();
+                continue;
+            }
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(cs, 1, 1);
+            cfg.blockDim = dim3(kFlashWarps * 32);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute a[1];
+            a[0].id = cudaLaunchAttributeClusterDimension;
+            a[0].val.clusterDim.x = cs;
+            a[0].val.clusterDim.y = 1;
+            a[0].val.clusterDim.z = 1;
+            cfg.attrs = a;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) {
+                best = cs;
+                break;
+            }
+            (void)cudaGetLastError();
+        }
+    } else {
+        (void)cudaGetLastError();
+    }
+    done[{device, d}] = best;
+    return best;
+}
+
+Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num_sms, int cluster_max) {
     Plan pl{};
     pl.flash = use_flash(n_q, n_kv, d);
     pl.tp = pl.flash ? kFlashTile : tile_slots(d);
@@ -759,13 +874,15 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
         if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
     }
     ns = std::min<int64_t>(ns, kMaxSplits);
+    // flash: the splits of one (sequence, KV head) merge in a cluster when the device allows one
+    // of that many CTAs (the split count is capped at the cluster size)
+    pl.cluster = pl.flash && ns > 1 && cluster_max >= 2;
+    if (pl.cluster) ns = std::min<int64_t>(ns, cluster_max);
     pl.nsplit_max = static_cast<int>(ns);
     pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
-    pl.ws = static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
+    pl.ws = pl.cluster ? 0 : static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
     if (pl.flash) {
-        const size_t ring = static_cast<size_t>(kFlashWarps) * kFlashStages * 2 * kFlashTile * d * 2;
-        // + the fused path's rotated query heads, K row, rotation table and new K/V rows (28 d bytes)
-        pl.smem = align_up(ring + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2 + 28ull * d, 1024) + 1024;
+        pl.smem = flash_smem(d);
         return pl;
     }
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
@@ -820,8 +937,9 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     if (st != GEM_OK || op.B == 0 || op.n_q == 0) return st;
     DeviceInfo di;
     if ((st = device_info(&di)) != GEM_OK) return st;
-    const Plan pl = make_plan(op.B, op.n_q, op.n_kv, op.d, op.cache_cap, op.window, di.num_sms);
-    if (pl.nsplit_max > 1 && (!op.workspace || op.ws_bytes < pl.ws)) return GEM_ERR_WORKSPACE;
+    const int cmax = use_flash(op.n_q, op.n_kv, op.d) ? flash_cluster_max(op.d, di.device) : 1;
+    const Plan pl = make_plan(op.B, op.n_q, op.n_kv, op.d, op.cache_cap, op.window, di.num_sms, cmax);
+    if (pl.nsplit_max > 1 && !pl.cluster && (!op.workspace || op.ws_bytes < pl.ws)) return GEM_ERR_WORKSPACE;
     if (pl.smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
     AttnParams P{};
     P.q = op.q;
@@ -851,6 +969,7 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     P.pa_off = pl.pa_off;
     P.st_off = pl.st_off;
     P.status = op.status ? op.status : di.status_word;
+    P.cluster = pl.cluster ? 1 : 0;
     RopeFreq fr{};
     if (fuse) {
         if (!pl.flash) return GEM_ERR_UNSUPPORTED_SHAPE;
@@ -883,6 +1002,11 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
     dim3 grid(pl.nsplit_max, op.n_kv, op.B);
     void* args[] = {&tmK, &tmV, &P, &fr};   // the split kernel takes the first three
+    if (pl.cluster) {
+        if (pl.nsplit_max > 8)
+            GEM_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+        return launch_pdl_cluster(fn, grid, dim3(kFlashWarps * 32), pl.smem, stream, args, pl.nsplit_max);
+    }
     if ((st = launch_pdl(fn, grid, dim3(pl.flash ? kFlashWarps * 32 : kAttnThreads), pl.smem, stream, args)) != GEM_OK)
         return st;
     if (pl.nsplit_max > 1) {
@@ -900,8 +1024,9 @@ size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, 
     if (B <= 0 || n_q <= 0 || n_kv <= 0 || cache_cap <= 0) return 0;
     DeviceInfo di;
     if (device_info(&di) != GEM_OK) return 0;
-    const Plan pl = make_plan(B, n_q, n_kv, d, cache_cap, window, di.num_sms);
-    return pl.nsplit_max > 1 ? align_up(pl.ws, 256) : 0;
+    const int cmax = use_flash(n_q, n_kv, d) ? flash_cluster_max(d, di.device) : 1;
+    const Plan pl = make_plan(B, n_q, n_kv, d, cache_cap, window, di.num_sms, cmax);
+    return pl.nsplit_max > 1 && !pl.cluster ? align_up(pl.ws, 256) : 0;
 }
 
 gem_status attn_check(const AttnOp& op) {

@@ -39,6 +39,9 @@ gem_status make_tensor_map_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const 
 // Launch with programmatic stream serialization enabled.
 gem_status launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                       void** args);
+// Same, with thread-block clusters of cluster_x CTAs along x (gridDim.x a multiple of it).
+gem_status launch_pdl_cluster(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              void** args, int cluster_x);
 
 // ---- Q4_0 GEMV ----------------------------------------------------------------------------
 struct GemvOp {

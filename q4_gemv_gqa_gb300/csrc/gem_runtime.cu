@@ -82,6 +82,11 @@ gem_status make_tensor_map_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const 
 
 gem_status launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                       void** args) {
+    return launch_pdl_cluster(kernel, grid, block, smem, stream, args, 1);
+}
+
+gem_status launch_pdl_cluster(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              void** args, int cluster_x) {
     // Every kernel of the library asks for the largest shared-memory carveout, so consecutive
     // launches never need the SM's L1/shared split changed (which would keep a dependent launch
     // from starting on an SM until the previous kernel has drained from it).
@@ -100,11 +105,19 @@ gem_status launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cu
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster_x > 1) {
+        if (grid.x % static_cast<unsigned>(cluster_x)) return GEM_ERR_INVALID_ARG;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     GEM_CUDA_TRY(cudaLaunchKernelExC(&cfg, kernel, args));
     return GEM_OK;
 }

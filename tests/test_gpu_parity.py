@@ -283,6 +283,8 @@ ATTN_CASES = [
     (32, 16, 256, 1024, [700], 1024, 1.0),              # ring not yet full
     (32, 4, 512, 0, [32768], 32769, 1.0),               # Gemma full-attention shape
     (6, 2, 256, 0, [5000], 5001, 0.0625),
+    (16, 8, 128, 0, [0], 4097, 128 ** -0.5),            # a long cache with one position: one split
+    (16, 8, 128, 0, [20], 4097, 128 ** -0.5),           #   and two of the planned splits busy
 ]
 
 
@@ -324,9 +326,27 @@ def test_attention_deterministic_repeat(gem, torch_mod):
     assert t.equal(o1, o2)
 
 
-def test_attention_needs_workspace(gem, torch_mod):
+def test_attention_deterministic_repeat_flash(gem, torch_mod):
     t = torch_mod
     n_q, n_kv, d, cap = 16, 8, 128, 4097
+    q = _cu(t, gem_synth.normal_f32(11, 1, (1, n_q * d)))
+    kc = _half_cache(t, gem_synth.normal_f16_bits(11, 2, (1, n_kv, cap, d)))
+    vc = _half_cache(t, gem_synth.normal_f16_bits(11, 3, (1, n_kv, cap, d)))
+    pos = _cu(t, np.array([cap - 1], np.int32))
+    need = gem.gqa_decode_attn_workspace(1, n_q, n_kv, d, cap, 0)
+    ws = t.empty(max(need, 1), dtype=t.uint8, device="cuda")
+    o1 = t.empty((1, n_q * d), device="cuda")
+    o2 = t.empty((1, n_q * d), device="cuda")
+    gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o1, ws if need else None)
+    gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o2, ws if need else None)
+    t.cuda.synchronize()
+    assert t.equal(o1, o2)
+
+
+def test_attention_needs_workspace(gem, torch_mod):
+    """The d = 512 kernel merges its splits through a caller workspace."""
+    t = torch_mod
+    n_q, n_kv, d, cap = 8, 4, 512, 4097
     need = gem.gqa_decode_attn_workspace(1, n_q, n_kv, d, cap, 0)
     assert need > 0
     q = t.zeros((1, n_q * d), device="cuda")

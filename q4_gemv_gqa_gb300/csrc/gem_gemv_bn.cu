@@ -68,9 +68,6 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     p.act = op.act;
     p.status = di.status_word;
     p.U = static_cast<int>((op.N + kUnitRows - 1) / kUnitRows);
-    const int C = std::min(di.num_sms, p.U);
-    const int umax = (p.U + C - 1) / C;
-
     // operand records: the caller's workspace, else the library's array
     const size_t rec_bytes = gemv_rec_bytes(B, op.K);
     uint8_t* rec = static_cast<uint8_t*>(op.act_ws);
@@ -83,10 +80,11 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     }
     p.rec = rec;
     p.rowinfo = reinterpret_cast<const float2*>(rec + rec_bytes - 8 * sizeof(float2));
+    const void* fn = nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<2>)
+                               : reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<1>);
 
-    const int rps = umax * nmat >= 2 ? 2 : 1;
-    p.rps = rps;
     const size_t budget = std::min<size_t>(gemv_mma::kSmemBudget, di.smem_optin);
+    int rps = 1, umax = 1;
     auto layout = [&](int gp, int u, int n, bool commit) -> size_t {
         const size_t stage = static_cast<size_t>(rps * gp) * kBoxBytes;
         const size_t recbuf = static_cast<size_t>(2 * gp) * kHgBytes;
@@ -115,40 +113,86 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
         }
         return align_up(off, 128);
     };
-    // Phase width 1..7 groups (2 consumer warps per group, one record buffer of 2 gps half groups x
-    // 4 KB): for each width the most units per pass with a ring of at least 4 stages; then the
+    // For ks-way K splits (each CTA sees ceil(G / ks) groups) and ncl CTA groups over the units:
+    // phase width 1..7 groups (2 consumer warps per group, one record buffer of 2 gps half groups
+    // x 4 KB); for each width the most units per pass with a ring of at least 4 stages; then the
     // width with the most busy warps per stage (2 gps x its share of full phases), fewer passes on
-    // ties.
+    // ties.  A split needs every CTA's units in one pass and its sums to fit the record buffer.
     int gps = 0, up = 0, ns = 0;
-    double best = -1.0;
-    for (int c = std::min(7, p.G); c >= 1; --c) {
-        const int nph = (p.G + c - 1) / c;
-        for (int u = umax; u >= 1; u = u > 1 ? (u + 1) / 2 : 0) {
-            const int stages = (nmat * u + rps - 1) / rps * nph;
-            const int want = std::min(4, stages);
-            int n = 0;
-            for (int m = std::min(kMaxSlots, stages); m >= want && !n; --m)
-                if (layout(c, u, m, false) <= budget) n = m;
-            if (!n) {
-                if (u == 1) break;
-                continue;
+    auto plan = [&](int ks, int ncl) -> bool {
+        umax = (p.U + ncl - 1) / ncl;
+        rps = umax * nmat >= 2 ? 2 : 1;
+        const int Gk = (p.G + ks - 1) / ks;
+        double best = -1.0;
+        gps = 0;
+        for (int c = std::min(7, Gk); c >= 1; --c) {
+            const int nph = (Gk + c - 1) / c;
+            for (int u = umax; u >= 1; u = u > 1 ? (u + 1) / 2 : 0) {
+                if (ks > 1 && u < umax) break;
+                const int stages = (nmat * u + rps - 1) / rps * nph;
+                const int want = std::min(4, stages);
+                int n = 0;
+                for (int m = std::min(kMaxSlots, stages); m >= want && !n; --m)
+                    if (layout(c, u, m, false) <= budget) n = m;
+                if (!n) {
+                    if (u == 1) break;
+                    continue;
+                }
+                if (ks > 1 && static_cast<size_t>(nmat) * u * kUnitRows * B * 4 > static_cast<size_t>(2 * c) * kHgBytes)
+                    break;
+                const int passes = (umax + u - 1) / u;
+                const double score = 2.0 * Gk / static_cast<double>(nph) - 0.01 * passes;
+                if (score > best) {
+                    best = score;
+                    gps = c;
+                    up = u;
+                    ns = n;
+                }
+                break;
             }
-            const int passes = (umax + u - 1) / u;
-            const double score = 2.0 * c * p.G / (static_cast<double>(nph) * c) - 0.01 * passes;
-            if (score > best) {
-                best = score;
-                gps = c;
-                up = u;
-                ns = n;
-            }
-            break;
         }
+        return gps > 0;
+    };
+    // A K split (clusters of ks CTAs) where each CTA would otherwise hold at most two units: there
+    // every CTA would copy all of K's records (4 B x K x B) for a few rows of weights.
+    int ks = 1, ncl = std::min(di.num_sms, p.U);
+    const int um1 = (p.U + di.num_sms - 1) / di.num_sms;
+    for (int k : {4, 2}) {
+        if (um1 > 2 || p.G < 32) continue;   // K >= 8192 (shorter K measured no faster split)
+        int n = std::min(di.num_sms / k, p.U);
+        if (!plan(k, n)) continue;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(n * k);
+        cfg.blockDim = dim3((2 * gps + 1) * 32);
+        cfg.dynamicSmemBytes = layout(gps, up, ns, false);
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = k;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if ((st = ensure_smem_bn(fn, di.device, cfg.dynamicSmemBytes)) != GEM_OK) return st;
+        int nmax = 0;
+        if (cudaOccupancyMaxActiveClusters(&nmax, fn, &cfg) != cudaSuccess || nmax <= 0) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        if (nmax < n) {
+            n = nmax;
+            if (!plan(k, n)) continue;
+        }
+        ks = k;
+        ncl = n;
+        break;
     }
-    if (!gps) return GEM_OK;   // not planned
-    const int nphase = (p.G + gps - 1) / gps;
+    if (ks == 1 && !plan(1, ncl)) return GEM_OK;   // not planned
+    const int C = ncl * ks;
+    p.ks = ks;
+    p.rps = rps;
     p.up = up;
     p.gps = gps;
-    p.nphase = nphase;
+    p.nphase = ((p.G + ks - 1) / ks + gps - 1) / gps;
     p.ns = ns;
     p.ncw = 2 * gps;
     const size_t smem = layout(gps, up, ns, true);
@@ -167,8 +211,6 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     } else {
         tm1 = tm0;
     }
-    const void* fn = nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<2>)
-                               : reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<1>);
     if ((st = ensure_smem_bn(fn, di.device, smem)) != GEM_OK) return st;
     *planned = true;
 
@@ -187,7 +229,7 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
                          stream, pargs)) != GEM_OK)
         return st;
     void* args[] = {&tm0, &tm1, &p};
-    return launch_pdl(fn, dim3(C), dim3((p.ncw + 1) * 32), smem, stream, args);
+    return launch_pdl_cluster(fn, dim3(C), dim3((p.ncw + 1) * 32), smem, stream, args, ks);
 }
 
 }  // namespace gem

@@ -140,6 +140,7 @@ struct Params {
     const float2* rowinfo;
     int act;
     int U, up, gps, nphase, ns, ncw, rps;
+    int ks;              // K split: CTAs of a ks-CTA cluster take K ranges of the same units (1: none)
     uint32_t stage_bytes, full_off, empty_off, rfull_off, rempty_off, xf_off, red_off;
     int* status;
 };
@@ -182,6 +183,20 @@ __device__ __forceinline__ void task_bn(const uint8_t* smem, uint32_t a, int t, 
     }
 }
 
+// Every thread of every CTA of the cluster arrives, then waits (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
@@ -201,14 +216,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ncw = p.ncw, nct = ncw * 32;
-    const int G = p.G, gps = p.gps, nphase = p.nphase, ns = p.ns, rps = p.rps;
+    const int gps = p.gps, ns = p.ns, rps = p.rps;
     const uint32_t stage_bytes = p.stage_bytes;
     const uint32_t rstride = static_cast<uint32_t>(gps * kBoxBytes);
     const uint32_t rec_phase = static_cast<uint32_t>(2 * gps * kHgBytes);   // one record buffer
-    const int C = gridDim.x, c = blockIdx.x;
-    const int u0 = static_cast<int>((static_cast<int64_t>(c) * p.U) / C);
-    const int u1 = static_cast<int>((static_cast<int64_t>(c + 1) * p.U) / C);
-    const int npass = (u1 - u0 + p.up - 1) / p.up;
+    // K split: cluster cid (of ncl) owns a unit range; its CTA `rank` owns groups [gk0, gk0 + Gr)
+    const int ks = p.ks, rank = static_cast<int>(blockIdx.x) % ks, cid = static_cast<int>(blockIdx.x) / ks;
+    const int ncl = static_cast<int>(gridDim.x) / ks;
+    const int gk0 = rank * p.G / ks, Gr = (rank + 1) * p.G / ks - gk0;
+    const int nphr = (Gr + gps - 1) / gps;   // this CTA's phases
+    const int u0 = static_cast<int>((static_cast<int64_t>(cid) * p.U) / ncl);
+    const int u1 = static_cast<int>((static_cast<int64_t>(cid + 1) * p.U) / ncl);
+    const int npass = (u1 - u0 + p.up - 1) / p.up;   // 1 whenever ks > 1
 
     __shared__ int any_failed;
     if (tid == 0) {
@@ -241,7 +260,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                 const int nrb = min(p.up, u1 - ub) * NMAT;
                 const int nr = min(rps, nrb - v * rps);
                 const int g0 = ph * gps;
-                const int ng = min(gps, G - g0);
+                const int ng = min(gps, Gr - g0);
                 if (s == ns) pdl_trigger();
                 if (s >= ns && !mbar_wait(&empty[slot], par, p.status)) return false;
                 uint8_t* dst = smem + static_cast<size_t>(slot) * stage_bytes;
@@ -251,8 +270,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                     const int row0 = (ub + rb / NMAT) * kUnitRows;
                     const CUtensorMap* tm = (NMAT == 2 && (rb & 1)) ? &tm1 : &tm0;
                     for (int j = 0; j < ng; ++j)
-                        tma_load_2d(dst + r * rstride + j * kBoxBytes, tm, (g0 + j) * kGroupBytes, row0, &full[slot],
-                                    policy);
+                        tma_load_2d(dst + r * rstride + j * kBoxBytes, tm, (gk0 + g0 + j) * kGroupBytes, row0,
+                                    &full[slot], policy);
                 }
                 ++s;
                 if (++slot == ns) {
@@ -272,13 +291,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                 const int ub = u0 + pass * p.up;
                 const int nrb = min(p.up, u1 - ub) * NMAT;
                 const int nv = (nrb + rps - 1) / rps;
-                for (int ph = 0; ph < nphase && ok; ++ph, ++q) {
+                for (int ph = 0; ph < nphr && ok; ++ph, ++q) {
                     // the buffer is free once every warp holds phase q - 1's operands
                     if (q >= 1 && !(ok = mbar_wait(rempty, (q - 1) & 1, p.status))) break;
-                    const int ng = min(gps, G - ph * gps);
+                    const int ng = min(gps, Gr - ph * gps);
                     const uint32_t bytes = static_cast<uint32_t>(2 * ng * kHgBytes);
                     mbar_arrive_expect_tx(rfull, bytes);
-                    bulk_load(smem + p.xf_off, p.rec + static_cast<size_t>(ph) * rec_phase, bytes, rfull);
+                    bulk_load(smem + p.xf_off,
+                              p.rec + static_cast<size_t>(2 * gk0) * kHgBytes + static_cast<size_t>(ph) * rec_phase,
+                              bytes, rfull);
                     for (int v = (q == 0 ? pre : 0); v < nv && ok; ++v) ok = issue(pass, ph, v);
                 }
             }
@@ -286,6 +307,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
             if (!ok) drain_stages(full, ns, max(0, s - ns), s - 1);
         } else {
             pdl_trigger();
+        }
+        __syncwarp();
+        if (ks > 1) {   // the two cluster barriers of the consumers' combine
+            cluster_sync_all();
+            cluster_sync_all();
         }
         return;
     }
@@ -312,8 +338,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
             const int nrb = min(p.up, u1 - ub) * NMAT;
             const int nv = (nrb + rps - 1) / rps;
             gemv_mma::consumer_sync(nct);   // the previous pass has read `red`
-            for (int ph = 0; ph < nphase; ++ph, ++q) {
-                const bool mine = jg < min(gps, G - ph * gps);
+            for (int ph = 0; ph < nphr; ++ph, ++q) {
+                const bool mine = jg < min(gps, Gr - ph * gps);
                 if (ok) ok = mbar_wait(rfull, q & 1, p.status);
                 uint4 xh[4], xl[4];
 #pragma unroll
@@ -359,6 +385,44 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
             gemv_mma::consumer_sync(nct);   // every partial sum of the pass written
             const int B = p.B;
             const int items = nrb * kUnitRows * B;
+            if (ks > 1) {
+                // this CTA's sums over its K range, per (row block, row, activation row), into the
+                // (now idle) record buffer; the cluster then adds its ks ranges in rank order
+                float* part = reinterpret_cast<float*>(smem + p.xf_off);
+                for (int idx = tid; idx < items; idx += nct) {
+                    const int rb = idx / (kUnitRows * B), rem = idx - rb * (kUnitRows * B);
+                    const int r16 = rem / B, b = rem - r16 * B;
+                    const int ln = (r16 & 7) * 4 + (b >> 1), comp = (r16 >> 3) * 2 + (b & 1);
+                    float v = 0.f;
+                    for (int w = 0; w < ncw; ++w) v += red[((rb * ncw + w) * 32 + ln) * 4 + comp];
+                    part[idx] = v;
+                }
+                cluster_sync_all();
+                const int nout = nrb / NMAT * kUnitRows * B;   // outputs (unit row, activation row)
+                const int chunk = (nout + ks - 1) / ks;
+                for (int oi = rank * chunk + tid; oi < min(nout, (rank + 1) * chunk); oi += nct) {
+                    const int u = oi / (kUnitRows * B), rem = oi - u * (kUnitRows * B);
+                    const int r16 = rem / B, b = rem - r16 * B;
+                    const int64_t n = static_cast<int64_t>(ub + u) * kUnitRows + r16;
+                    if (n >= p.N) continue;
+                    const int ig = ((u * NMAT) * kUnitRows + r16) * B + b;
+                    float v = 0.f, uv = 0.f;
+                    for (int r = 0; r < ks; ++r) v += ld_cluster_f32(part + ig, static_cast<uint32_t>(r));
+                    if (NMAT == 2)
+                        for (int r = 0; r < ks; ++r)
+                            uv += ld_cluster_f32(part + ig + kUnitRows * B, static_cast<uint32_t>(r));
+                    const float out = p.rowinfo[b].y;
+                    v *= out;
+                    if (NMAT == 1) {
+                        if (p.residual) v += p.residual[b * p.ldr + n];
+                    } else {
+                        v = gemv_mma::act_fn(v, p.act) * (uv * out);
+                    }
+                    p.y[b * p.ldy + n] = v;
+                }
+                cluster_sync_all();   // the peers have read this CTA's sums
+                continue;
+            }
             for (int idx = tid; idx < items; idx += nct) {
                 const int rb = idx / (kUnitRows * B), rem = idx - rb * (kUnitRows * B);
                 const int r16 = rem / B, b = rem - r16 * B;

@@ -470,32 +470,38 @@ def run_gem(args):
         dist.destroy_process_group()
 
 
-def _oracle_sample(wl, budget_s):
-    """Oracle layer steps on the workload's shapes until ~budget_s of CPU work."""
+_ORACLE_TENSORS = {}
+
+
+def _oracle_sample(wl, budget_s, max_cached=4):
+    """Oracle layer steps on the workload's layers, in order and cycling over the first
+    `max_cached` of them (tensors built once), until ~budget_s of CPU work (at least one step)."""
     import oracle
-    shape, cap = wl.layers[0], wl.cache_cap[0]
     T = wl.pos + 1
     pos = np.full(wl.B, wl.pos, np.int32)
     done, bytes_done, t_spent = 0, 0, 0.0
-    x = configs.layer_input(shape.H, wl.B, 0).astype(np.float64)
-    li = 0
-    while t_spent < budget_s and li < len(wl.layers):
-        tens = configs.layer_tensors(wl.layers[li], wl.B, wl.cache_cap[li], 0, li)
-        t0 = time.perf_counter()
+    x = configs.layer_input(wl.layers[0].H, wl.B, 0).astype(np.float64)
+    ncyc = min(max_cached, len(wl.layers))
+    while done == 0 or t_spent < budget_s:
+        li = done % ncyc
+        key = (wl.name, li, wl.B)
+        if key not in _ORACLE_TENSORS:
+            _ORACLE_TENSORS[key] = configs.layer_tensors(wl.layers[li], wl.B, wl.cache_cap[li], 0, li)
+        tens = _ORACLE_TENSORS[key]
+        t0 = time.perf_counter()   # (a repeated step rewrites the same appended slot: same work)
         x = oracle.decode_layer(wl.layers[li], tens, x, pos, tens.k_cache, tens.v_cache)
         t_spent += time.perf_counter() - t0
         s = wl.layers[li]
         bytes_done += layer_bytes(s, wl.B, min(T, s.window) if s.window else T)["total"]
         done += 1
-        li += 1
     return done, bytes_done, t_spent, oracle.num_threads()
 
 
 def cpu_baseline(wl, args):
     done, b, t, cores = _oracle_sample(wl, args.cpu_budget)
     return {"value": round(b / t / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%d of %d layer steps of %s (fp64 scalar C, OpenMP over rows/heads), %.1f s"
-                      % (done, len(wl.layers), wl.name, t),
+            "sample": "%d layer steps of %s (its first %d layers in turn; fp64 scalar C, OpenMP over "
+                      "rows/heads), %.1f s" % (done, wl.name, min(4, len(wl.layers)), t),
             "ms_per_layer": round(t * 1e3 / done, 1)}
 
 
@@ -506,7 +512,7 @@ def run_reference(args):
     wl = configs.workload(args.workload)
     if args.layers:
         wl = configs.with_layers(wl, args.layers)
-    per_step = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    per_step = args.cpu_budget / max(1, args.steps + args.warmup)   # at least one layer step each
     for _ in range(args.warmup):
         _oracle_sample(configs.with_layers(wl, 1), 0.0)
     tot_b, tot_t, cores, done = 0, 0.0, 1, 0

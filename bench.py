@@ -69,6 +69,20 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def device_record(torch, index: int) -> dict:
+    """GPU name, SM count, L2 size and driver version of the measuring device."""
+    pr = torch.cuda.get_device_properties(index)
+    rec = {"name": pr.name, "sms": pr.multi_processor_count,
+           "l2_bytes": getattr(pr, "L2_cache_size", None), "driver": None}
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=driver_version",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+        rec["driver"] = out.stdout.strip() or None
+    except Exception:
+        pass
+    return rec
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -461,6 +475,7 @@ def run_gem(args):
                     "d2h_bytes_per_step": int(hout.numel() * 4)},
             "gpu_launches": model.launches_per_step() * args.steps,
             "clocks": clk.summary(),
+            "device": device_record(torch, local),
             "device_flags": flags,
             "cpu_baseline": cpu,
         }

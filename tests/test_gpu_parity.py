@@ -456,3 +456,34 @@ def test_decode_layer_stack_each_layer_from_oracle_input(gem, torch_mod, name, n
         assert status == 0
         _, ref = _layer_parity(shape, tens, x, pos, got, gk, gv, "%s layer %d" % (name, layer))
         x = ref
+
+
+# ---- logit projection + argmax (test only) ---------------------------------------------------
+#
+# A Q4_0 GEMV from the final hidden state to a Qwen3-size vocabulary, then the token choice:
+# the GPU logits must match the oracle's within the parity tolerance and pick the same argmax
+# (lowest index on ties).  Rows whose oracle top-2 gap is within twice the max-abs tolerance are
+# ambiguous by construction and are counted, not judged.
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_logit_projection_argmax(gem, torch_mod, B):
+    from parity import MAX_ABS
+    t = torch_mod
+    V, H = 151936, 2048
+    W = gem_synth.q4_0_matrix(7, 77, V, H)
+    x = gem_synth.normal_f32(7, 78, (B, H))
+    ref = oracle.q4_0_gemv(W, V, H, x)
+    y = t.full((B, V), float("nan"), device="cuda")
+    gem.q4_0_gemv(_cu(t, W), V, H, _cu(t, x), y)
+    got_idx = t.argmax(y, dim=1).cpu().numpy()   # first maximal index
+    t.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, "logits B=%d" % B)
+    decided = 0
+    for b in range(B):
+        top2 = np.sort(ref[b])[-2:]
+        if top2[1] - top2[0] < 2 * MAX_ABS:
+            continue
+        assert int(got_idx[b]) == oracle.argmax(ref[b]), "row %d: GPU argmax %d, oracle %d" % (
+            b, int(got_idx[b]), oracle.argmax(ref[b]))
+        decided += 1
+    assert decided >= 1

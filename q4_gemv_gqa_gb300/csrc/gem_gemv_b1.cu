@@ -56,9 +56,10 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
             gps = c;
         }
     }
-    // Stages hold two row blocks (sharing the activation operand) unless no CTA has two.
-    const int rps = umax * nmat >= 2 ? 2 : 1;
-    p.rps = rps;
+    // Stages hold up to three row blocks sharing the activation operand (as many as the CTAs'
+    // units allow; three when they come in threes, e.g. nine units per CTA).
+    const int rbmax = umax * nmat;
+    int rps = rbmax >= kMaxRps && rbmax % kMaxRps == 0 ? kMaxRps : std::min(2, rbmax);
     const size_t budget = std::min<size_t>(gemv_mma::kSmemBudget, di.smem_optin);
     const size_t xf = static_cast<size_t>(2 * p.G) * kRecBytes + kZeroBytes;
     auto layout = [&](int up, int ns, bool commit) -> size_t {
@@ -89,14 +90,21 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
     int up = umax, ns = 0;
     for (;;) {
         const int stages = (nmat * up + rps - 1) / rps * nphase;
-        const int want = std::min(4, stages);
+        // at least 4 stages in flight (3 when a stage is >= 40 KB)
+        const int want = std::min(static_cast<size_t>(rps * gps) * kBoxBytes >= 40 * 1024 ? 3 : 4, stages);
         ns = 0;
         for (int n = std::min(kMaxSlots, stages); n >= want && !ns; --n)
             if (layout(up, n, false) <= budget) ns = n;
-        if (ns) break;
+        if (ns && (up == umax || rps <= 2)) break;
+        if (ns || rps > 2) {   // three row blocks only with every unit in one pass
+            rps = std::min(2, rbmax);
+            up = umax;
+            continue;
+        }
         if (up > 1) up = (up + 1) / 2;
         else return GEM_OK;   // not planned: records too large for this K
     }
+    p.rps = rps;
     p.up = up;
     p.gps = gps;
     p.nphase = nphase;

@@ -42,6 +42,7 @@ constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kRecBytes = 512;   // activation record of one half group: 8 columns x 8 tiles x 8 B
 constexpr int kZeroBytes = 96;   // the operand of lanes off the block diagonal (bytes 32..95)
 constexpr int kPro = 4;          // float4s of the activation row kept per consumer thread
+constexpr int kMaxRps = 3;       // row blocks per stage at most
 
 struct Params {
     int64_t N;
@@ -55,7 +56,7 @@ struct Params {
     int U;               // 16-row units
     int up;              // units per pass
     int gps;             // groups per phase (stage = rps row blocks x gps groups)
-    int rps;             // row blocks per stage: 2, or 1 when no CTA has two
+    int rps;             // row blocks per stage (1..kMaxRps): as many as the CTAs' units allow
     int nphase;
     int ns;
     int ncw;             // consumer warps = 2 * gps
@@ -81,7 +82,7 @@ __device__ __forceinline__ void code_slot(bool odd, int m, int& i, int& j) {
 // further); xr = shared offset of the lane's 64-byte activation operand.
 template <bool ODD, int NR>
 __device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t rstride, uint32_t xr,
-                                     float (&t0)[2], float (&t1)[2]) {
+                                     float (&t0)[kMaxRps], float (&t1)[kMaxRps]) {
     const uint4* xp = reinterpret_cast<const uint4*>(smem + xr);
     uint4 xb[4];
 #pragma unroll
@@ -371,15 +372,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
             const int nrb = min(p.up, u1 - ub) * NMAT;
             gemv_mma::consumer_sync(nct);   // the previous pass has read `red`
             for (int v = 0; v * rps < nrb; ++v) {
-                const bool two = rps == 2 && 2 * v + 1 < nrb;
-                float t0[2] = {0.f, 0.f}, t1[2] = {0.f, 0.f};
+                const int nr = min(rps, nrb - v * rps);
+                float t0[kMaxRps], t1[kMaxRps];
+#pragma unroll
+                for (int r = 0; r < kMaxRps; ++r) t0[r] = t1[r] = 0.f;
                 uint32_t xr = xbase;
                 for (int ph = 0; ph < nphase; ++ph, xr += xstep) {
                     const bool mine = jg < min(gps, G - ph * gps);
                     if (ok) ok = mbar_wait(&full[slot], par, p.status);
                     if (mine && ok) {
                         const uint32_t a = static_cast<uint32_t>(slot) * stage_bytes + aoff;
-                        if (two) task<ODD, 2>(smem, a, rstride, xr, t0, t1);
+                        if (nr == 3) task<ODD, 3>(smem, a, rstride, xr, t0, t1);
+                        else if (nr == 2) task<ODD, 2>(smem, a, rstride, xr, t0, t1);
                         else task<ODD, 1>(smem, a, rstride, xr, t0, t1);
                     }
                     __syncwarp();
@@ -393,19 +397,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                 // rows g and g + 8 of the stage's row blocks: sum the quad's four blocks, one
                 // value per (row, warp)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < kMaxRps; ++r) {
                     t0[r] += __shfl_xor_sync(0xffffffffu, t0[r], 1);
                     t1[r] += __shfl_xor_sync(0xffffffffu, t1[r], 1);
                     t0[r] += __shfl_xor_sync(0xffffffffu, t0[r], 2);
                     t1[r] += __shfl_xor_sync(0xffffffffu, t1[r], 2);
                 }
                 if (t == 0) {
-                    const int rb = v * rps;
-                    red[(rb * kUnitRows + g) * ncw + warp] = t0[0];
-                    red[(rb * kUnitRows + g + 8) * ncw + warp] = t1[0];
-                    if (two) {
-                        red[((rb + 1) * kUnitRows + g) * ncw + warp] = t0[1];
-                        red[((rb + 1) * kUnitRows + g + 8) * ncw + warp] = t1[1];
+#pragma unroll
+                    for (int r = 0; r < kMaxRps; ++r) {
+                        if (r < nr) {
+                            const int rb = v * rps + r;
+                            red[(rb * kUnitRows + g) * ncw + warp] = t0[r];
+                            red[(rb * kUnitRows + g + 8) * ncw + warp] = t1[r];
+                        }
                     }
                 }
             }

@@ -141,7 +141,10 @@ GEM_API gem_status gem_rmsnorm_qknorm_rope(float *qkv, int64_t ldqkv, int B, int
  *   out     [B][ldo] fp32.
  *   d       64, 128, 256 or 512.  n_q % n_kv == 0 and n_q / n_kv <= 8.
  *   workspace  device scratch of gem_gqa_decode_attn_workspace() bytes (same B, n_q, n_kv,
- *           d, cache_cap, window), 256-byte aligned; contents need no initialisation.
+ *           d, cache_cap, window), 256-byte aligned; contents need no initialisation.  The
+ *           query returns 0 (workspace may be NULL) where the splits of a KV head merge inside
+ *           a thread-block cluster (d <= 128, n_q / n_kv <= 4, on devices that schedule the
+ *           cluster) or where one split covers the range.
  *   Results are deterministic: the split count depends only on (p, shape, device), and
  *   partial states are merged in ascending split order.
  */

@@ -82,6 +82,8 @@ GEMV_CASES = [
     (300, 21504, 3),                    # long K: several activation phases
     (1000, 21504, 1), (2560, 9728, 1),  # one row: 12 phases; a ragged last phase (38 groups)
     (8, 8192, 1), (40000, 512, 1),      # one row: half a row-block pair; several passes
+    (40, 65536, 1),                     # one row, operand records beyond shared memory: fallback kernel
+    (24, 131328, 2),                    # two rows, records beyond the library array: fallback kernel
 ]
 
 

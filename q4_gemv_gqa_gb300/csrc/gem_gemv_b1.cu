@@ -40,32 +40,20 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
     p.act = op.act;
     p.status = di.status_word;
     p.U = static_cast<int>((op.N + kUnitRows - 1) / kUnitRows);
-    const int C = std::min(di.num_sms, p.U);
-    const int umax = (p.U + C - 1) / C;
-
-    // Phase width: 4..9 groups (2 consumer warps per group); the widest (longest runs per row,
-    // most warps) unless a narrower one wastes at least 5 % fewer warp slots over its
-    // ceil(G / gps) phases.
-    int gps = 1;
-    double best = -1.0;
-    for (int c = std::min(kMaxConsumerWarps / 2, p.G); c >= std::min(4, p.G); --c) {
-        const int nph = (p.G + c - 1) / c;
-        const double eff = static_cast<double>(p.G) / (static_cast<double>(nph) * c);
-        if (eff > best + 0.05) {
-            best = eff;
-            gps = c;
-        }
-    }
-    // Stages hold up to three row blocks sharing the activation operand (as many as the CTAs'
-    // units allow; three when they come in threes, e.g. nine units per CTA).
-    const int rbmax = umax * nmat;
-    int rps = rbmax >= kMaxRps && rbmax % kMaxRps == 0 ? kMaxRps : std::min(2, rbmax);
+    auto kernel_of = [&](int ks) {
+        if (ks == 2)
+            return nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_b1_kernel<2, 2>)
+                             : reinterpret_cast<const void*>(q4_0_gemv_b1_kernel<1, 2>);
+        return nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_b1_kernel<2, 1>)
+                         : reinterpret_cast<const void*>(q4_0_gemv_b1_kernel<1, 1>);
+    };
     const size_t budget = std::min<size_t>(gemv_mma::kSmemBudget, di.smem_optin);
-    const size_t xf = static_cast<size_t>(2 * p.G) * kRecBytes + kZeroBytes;
-    auto layout = [&](int up, int ns, bool commit) -> size_t {
+    int gps = 1, rps = 1, rbmax = 1, umax = 1, up = 1, ns = 0, Gk = p.G;
+    auto layout = [&](int u, int n, bool commit) -> size_t {
+        const size_t xf = static_cast<size_t>(2 * Gk) * kRecBytes + kZeroBytes;
         const size_t stage = static_cast<size_t>(rps * gps) * kBoxBytes;
-        const size_t red = static_cast<size_t>(nmat) * up * kUnitRows * (2 * gps) * 4;
-        size_t off = align_up(static_cast<size_t>(ns) * stage, 128);
+        const size_t red = static_cast<size_t>(nmat) * u * kUnitRows * (2 * gps) * 4;
+        size_t off = align_up(static_cast<size_t>(n) * stage, 128);
         const size_t full_off = off;
         off += kMaxSlots * 8;
         const size_t empty_off = off;
@@ -86,28 +74,86 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
         }
         return align_up(off, 128);
     };
-    const int nphase = (p.G + gps - 1) / gps;
-    int up = umax, ns = 0;
-    for (;;) {
-        const int stages = (nmat * up + rps - 1) / rps * nphase;
-        // at least 4 stages in flight (3 when a stage is >= 40 KB)
-        const int want = std::min(static_cast<size_t>(rps * gps) * kBoxBytes >= 40 * 1024 ? 3 : 4, stages);
-        ns = 0;
-        for (int n = std::min(kMaxSlots, stages); n >= want && !ns; --n)
-            if (layout(up, n, false) <= budget) ns = n;
-        if (ns && (up == umax || rps <= 2)) break;
-        if (ns || rps > 2) {   // three row blocks only with every unit in one pass
-            rps = std::min(2, rbmax);
-            up = umax;
-            continue;
+    // Plan for ks-way K splits (each CTA owns ceil(G / ks) groups) and ncl CTA groups over the
+    // units.  Phase width: 4..9 groups (2 consumer warps per group); the widest (longest runs per
+    // row, most warps) unless a narrower one wastes at least 5 % fewer warp slots over its
+    // phases.  Stages hold up to three row blocks sharing the activation operand (three when a
+    // CTA's units come in threes and still fit one pass).  A split needs one pass.
+    auto plan = [&](int ks, int ncl) -> bool {
+        Gk = (p.G + ks - 1) / ks;
+        umax = (p.U + ncl - 1) / ncl;
+        gps = 1;
+        double best = -1.0;
+        for (int c = std::min(kMaxConsumerWarps / 2, Gk); c >= std::min(4, Gk); --c) {
+            const int nph = (Gk + c - 1) / c;
+            const double eff = static_cast<double>(Gk) / (static_cast<double>(nph) * c);
+            if (eff > best + 0.05) {
+                best = eff;
+                gps = c;
+            }
         }
-        if (up > 1) up = (up + 1) / 2;
-        else return GEM_OK;   // not planned: records too large for this K
+        rbmax = umax * nmat;
+        rps = rbmax >= kMaxRps && rbmax % kMaxRps == 0 ? kMaxRps : std::min(2, rbmax);
+        const int nphase = (Gk + gps - 1) / gps;
+        up = umax;
+        for (;;) {
+            const int stages = (nmat * up + rps - 1) / rps * nphase;
+            // at least 4 stages in flight (3 when a stage is >= 40 KB)
+            const int want = std::min(static_cast<size_t>(rps * gps) * kBoxBytes >= 40 * 1024 ? 3 : 4, stages);
+            ns = 0;
+            for (int n = std::min(kMaxSlots, stages); n >= want && !ns; --n)
+                if (layout(up, n, false) <= budget) ns = n;
+            if (ns && (up == umax || rps <= 2)) break;
+            if (ns || rps > 2) {   // three row blocks only with every unit in one pass
+                rps = std::min(2, rbmax);
+                up = umax;
+                continue;
+            }
+            if (up > 1) up = (up + 1) / 2;
+            else return false;
+        }
+        return ks == 1 || up == umax;
+    };
+    // K split over 2-CTA clusters where the units do not divide evenly over the SMs and the
+    // slowest CTA's share shrinks by at least 10 % (e.g. 336 units: 3 per CTA, or 5 per CTA pair
+    // at half the groups each).
+    int ks = 1, ncl = std::min(di.num_sms, p.U);
+    const int um1 = (p.U + ncl - 1) / ncl;
+    if (p.U % ncl != 0 && um1 <= 3 && p.G >= 64) {   // long K (K >= 16384: measured faster split)
+        int n = std::min(di.num_sms / 2, p.U);
+        if (plan(2, n)) {
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(2 * n);
+            cfg.blockDim = dim3((2 * gps + 1) * 32);
+            cfg.dynamicSmemBytes = layout(up, ns, false);
+            cudaLaunchAttribute a[1];
+            a[0].id = cudaLaunchAttributeClusterDimension;
+            a[0].val.clusterDim.x = 2;
+            a[0].val.clusterDim.y = 1;
+            a[0].val.clusterDim.z = 1;
+            cfg.attrs = a;
+            cfg.numAttrs = 1;
+            gem_status st0;
+            if ((st0 = ensure_smem_b1(kernel_of(2), di.device, cfg.dynamicSmemBytes)) != GEM_OK) return st0;
+            int nmax = 0;
+            if (cudaOccupancyMaxActiveClusters(&nmax, kernel_of(2), &cfg) != cudaSuccess || nmax <= 0) {
+                (void)cudaGetLastError();
+            } else {
+                if (nmax < n) n = nmax;
+                if (plan(2, n) && 10 * ((p.U + n - 1) / n) < 2 * 9 * um1) {
+                    ks = 2;
+                    ncl = n;
+                }
+            }
+        }
     }
+    if (ks == 1 && !plan(1, ncl)) return GEM_OK;   // not planned: records too large for this K
+    const int C = ncl * ks;
+    p.ks = ks;
     p.rps = rps;
     p.up = up;
     p.gps = gps;
-    p.nphase = nphase;
+    p.nphase = (Gk + gps - 1) / gps;
     p.ns = ns;
     p.ncw = 2 * gps;
     const size_t smem = layout(up, ns, true);
@@ -127,12 +173,11 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
     } else {
         tm1 = tm0;
     }
-    const void* fn = nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_b1_kernel<2>)
-                               : reinterpret_cast<const void*>(q4_0_gemv_b1_kernel<1>);
+    const void* fn = kernel_of(ks);
     if ((st = ensure_smem_b1(fn, di.device, smem)) != GEM_OK) return st;
     *planned = true;
     void* args[] = {&tm0, &tm1, &p};
-    return launch_pdl(fn, dim3(C), dim3((p.ncw + 1) * 32), smem, stream, args);
+    return launch_pdl_cluster(fn, dim3(C), dim3((p.ncw + 1) * 32), smem, stream, args, ks);
 }
 
 }  // namespace gem

@@ -57,6 +57,7 @@ struct Params {
     int up;              // units per pass
     int gps;             // groups per phase (stage = rps row blocks x gps groups)
     int rps;             // row blocks per stage (1..kMaxRps): as many as the CTAs' units allow
+    int ks;              // K split (the kernel's KS): the CTAs of a ks-CTA cluster take K ranges of the same units
     int nphase;
     int ns;
     int ncw;             // consumer warps = 2 * gps
@@ -74,6 +75,20 @@ __device__ __forceinline__ void code_slot(bool odd, int m, int& i, int& j) {
     const int mm = odd ? m : (m + 2) & 15;
     i = mm >> 2;
     j = mm & 3;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
 // One task: rows g and g + 8 of one block per lane in each of NR row blocks (the same K range,
@@ -140,7 +155,9 @@ __device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t r
     }
 }
 
-template <int NMAT>
+// KS = 1, or 2 for the form whose CTA pairs (thread-block clusters) split K (a separate
+// instantiation, so the plain form carries none of the split's code).
+template <int NMAT, int KS>
 __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __grid_constant__ CUtensorMap tm0,
                                                                       const __grid_constant__ CUtensorMap tm1,
                                                                       const Params p) {
@@ -155,10 +172,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     const int G = p.G, gps = p.gps, nphase = p.nphase, ns = p.ns, rps = p.rps;
     const uint32_t stage_bytes = p.stage_bytes;
     const uint32_t rstride = static_cast<uint32_t>(gps * kBoxBytes);   // second row block of a stage
-    const int C = gridDim.x, c = blockIdx.x;
-    const int u0 = static_cast<int>((static_cast<int64_t>(c) * p.U) / C);
-    const int u1 = static_cast<int>((static_cast<int64_t>(c + 1) * p.U) / C);
-    const int npass = (u1 - u0 + p.up - 1) / p.up;
+    // K split: cluster cid (of ncl) owns a unit range; its CTA `rank` owns groups [gk0, gk0 + Gr)
+    constexpr int ks = KS;
+    const int rank = static_cast<int>(blockIdx.x) % ks, cid = static_cast<int>(blockIdx.x) / ks;
+    const int ncl = static_cast<int>(gridDim.x) / ks;
+    const int gk0 = KS == 1 ? 0 : rank * G / ks;
+    const int Gr = KS == 1 ? G : (rank + 1) * G / ks - gk0;
+    const int nphr = KS == 1 ? nphase : (Gr + gps - 1) / gps;   // this CTA's phases
+    const int u0 = static_cast<int>((static_cast<int64_t>(cid) * p.U) / ncl);
+    const int u1 = static_cast<int>((static_cast<int64_t>(cid + 1) * p.U) / ncl);
+    const int npass = (u1 - u0 + p.up - 1) / p.up;   // 1 whenever ks > 1
 
     __shared__ int any_failed;
     if (tid == 0) {
@@ -187,9 +210,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                 const int nrb = min(p.up, u1 - ub) * NMAT;
                 for (int v = 0; v * rps < nrb && ok; ++v) {
                     const int nr = min(rps, nrb - v * rps);
-                    for (int ph = 0; ph < nphase; ++ph) {
+                    for (int ph = 0; ph < nphr; ++ph) {
                         const int g0 = ph * gps;
-                        const int ng = min(gps, G - g0);
+                        const int ng = min(gps, Gr - g0);
                         if (s == ns) pdl_trigger();   // ring filled once
                         if (s >= ns) {
                             ok = mbar_wait(&empty[slot], par, p.status);
@@ -202,8 +225,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                             const int row0 = (ub + rb / NMAT) * kUnitRows;
                             const CUtensorMap* tm = (NMAT == 2 && (rb & 1)) ? &tm1 : &tm0;
                             for (int j = 0; j < ng; ++j)
-                                tma_load_2d(dst + r * rstride + j * kBoxBytes, tm, (g0 + j) * kGroupBytes, row0,
-                                            &full[slot], policy);
+                                tma_load_2d(dst + r * rstride + j * kBoxBytes, tm, (gk0 + g0 + j) * kGroupBytes,
+                                            row0, &full[slot], policy);
                         }
                         ++s;
                         if (++slot == ns) {
@@ -218,6 +241,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
         } else {
             pdl_trigger();
         }
+        if constexpr (KS > 1) {   // the two cluster barriers of the consumers' combine
+            __syncwarp();
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
 
@@ -226,6 +254,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     pdl_wait();   // the activations (and residual) come from the previous kernel
 
     const int K = G * 256, K4 = K / 4;
+    // this CTA's records cover groups [gk0, gk0 + Gr): float4s [kr0, kr1) of the row
+    const int kr0 = gk0 * 64, kr1 = (gk0 + Gr) * 64;
     // Rows of up to kPro float4 per consumer thread are read once and kept in registers; longer
     // ones are read twice (statistics, then the records).
     const bool onepass = K4 <= kPro * nct;
@@ -290,11 +320,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
 #pragma unroll
             for (int u = 0; u < kPro; ++u) {
                 const int i = tid + u * nct;
-                if (i < K4) {
+                if (i >= kr0 && i < kr1) {
                     const int k0 = 4 * i;
                     const int blk = (k0 >> 5) & 7, e0 = k0 & 31;
                     const bool odd = blk & 1;
-                    const uint32_t rec = static_cast<uint32_t>((2 * (k0 >> 8) + (odd ? 1 : 0)) * kRecBytes +
+                    const uint32_t rec = static_cast<uint32_t>((2 * ((k0 >> 8) - gk0) + (odd ? 1 : 0)) * kRecBytes +
                                                                (blk >> 1) * 128 + (e0 >> 4) * 8);
                     const float v4[4] = {xv[u].x * sc, xv[u].y * sc, xv[u].z * sc, xv[u].w * sc};
 #pragma unroll
@@ -311,7 +341,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
             }
         } else {
             // gather: four registers per thread and round, their loads issued before converting
-            const int nreg = 2 * G * 64;   // (hg, t, tau, r)
+            const int nreg = 2 * Gr * 64;   // (local hg, t, tau, r)
             for (int i0 = tid; i0 < nreg; i0 += 4 * nct) {
                 float v0[4], v1[4];
                 uint32_t off[4];
@@ -323,7 +353,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                     if (i < nreg) {
                         const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
                         const bool odd = hg & 1;
-                        const int base = (hg >> 1) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
+                        const int base = ((hg >> 1) + gk0) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
                         const int k0 = base + code_byte(odd, tau >> 1, r);
                         const int k1 = base + code_byte(odd, tau >> 1, r + 2);
                         v0[u] = __ldg(p.x + k0);
@@ -347,7 +377,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                 }
             }
         }
-        if (tid < kZeroBytes / 4) reinterpret_cast<uint32_t*>(xf + 2 * G * kRecBytes)[tid] = 0u;
+        if (tid < kZeroBytes / 4) reinterpret_cast<uint32_t*>(xf + 2 * Gr * kRecBytes)[tid] = 0u;
         gemv_mma::consumer_sync(nct);
     }
 
@@ -359,7 +389,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     const uint32_t aoff = static_cast<uint32_t>(jg * kBoxBytes + g * kGroupBytes + 36 * t + (odd ? 16 : 0));
     const bool diag = (g >> 1) == t;
     const uint32_t xbase = diag ? p.xf_off + static_cast<uint32_t>(warp * kRecBytes + g * 64)
-                                : p.xf_off + static_cast<uint32_t>(2 * G * kRecBytes + 32);
+                                : p.xf_off + static_cast<uint32_t>(2 * Gr * kRecBytes + 32);
     const uint32_t xstep = diag ? static_cast<uint32_t>(2 * gps * kRecBytes) : 0u;   // per phase
 
     bool ok = true;
@@ -377,8 +407,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
 #pragma unroll
                 for (int r = 0; r < kMaxRps; ++r) t0[r] = t1[r] = 0.f;
                 uint32_t xr = xbase;
-                for (int ph = 0; ph < nphase; ++ph, xr += xstep) {
-                    const bool mine = jg < min(gps, G - ph * gps);
+                for (int ph = 0; ph < nphr; ++ph, xr += xstep) {
+                    const bool mine = jg < min(gps, Gr - ph * gps);
                     if (ok) ok = mbar_wait(&full[slot], par, p.status);
                     if (mine && ok) {
                         const uint32_t a = static_cast<uint32_t>(slot) * stage_bytes + aoff;
@@ -417,22 +447,54 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
             gemv_mma::consumer_sync(nct);   // every partial sum of the pass written
             const float out = misc[65];
             const int rows_in_pass = nrb * kUnitRows;
-            for (int row = tid; row < rows_in_pass; row += nct) {
-                const int rb = row / kUnitRows, r16 = row - rb * kUnitRows;
-                if (NMAT == 2 && (rb & 1)) continue;
-                const int64_t n = static_cast<int64_t>(ub + rb / NMAT) * kUnitRows + r16;
-                if (n >= p.N) continue;
-                float v = 0.f;
-                for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
-                v *= out;
-                if (NMAT == 1) {
-                    if (p.residual) v += p.residual[n];
-                } else {
-                    float uv = 0.f;
-                    for (int w = 0; w < ncw; ++w) uv += red[(row + kUnitRows) * ncw + w];
-                    v = gemv_mma::act_fn(v, p.act) * (uv * out);
+            if constexpr (KS > 1) {
+                // this CTA's sums over its K range per row, into the (now idle) records; the
+                // cluster then adds its ks ranges in rank order
+                float* part = reinterpret_cast<float*>(smem + p.xf_off);
+                for (int row = tid; row < rows_in_pass; row += nct) {
+                    float v = 0.f;
+                    for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
+                    part[row] = v;
                 }
-                p.y[n] = v;
+                cluster_sync_all();
+                const int nout = nrb / NMAT * kUnitRows;   // output rows of the pass
+                const int chunk = (nout + ks - 1) / ks;
+                for (int oi = rank * chunk + tid; oi < min(nout, (rank + 1) * chunk); oi += nct) {
+                    const int u = oi / kUnitRows, r16 = oi - u * kUnitRows;
+                    const int64_t n = static_cast<int64_t>(ub + u) * kUnitRows + r16;
+                    if (n >= p.N) continue;
+                    const int row = (u * NMAT) * kUnitRows + r16;
+                    float v = 0.f, uv = 0.f;
+                    for (int r = 0; r < ks; ++r) v += ld_cluster_f32(part + row, static_cast<uint32_t>(r));
+                    if (NMAT == 2)
+                        for (int r = 0; r < ks; ++r) uv += ld_cluster_f32(part + row + kUnitRows, static_cast<uint32_t>(r));
+                    v *= out;
+                    if (NMAT == 1) {
+                        if (p.residual) v += p.residual[n];
+                    } else {
+                        v = gemv_mma::act_fn(v, p.act) * (uv * out);
+                    }
+                    p.y[n] = v;
+                }
+                cluster_sync_all();   // the peers have read this CTA's sums
+            } else {
+                for (int row = tid; row < rows_in_pass; row += nct) {
+                    const int rb = row / kUnitRows, r16 = row - rb * kUnitRows;
+                    if (NMAT == 2 && (rb & 1)) continue;
+                    const int64_t n = static_cast<int64_t>(ub + rb / NMAT) * kUnitRows + r16;
+                    if (n >= p.N) continue;
+                    float v = 0.f;
+                    for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
+                    v *= out;
+                    if (NMAT == 1) {
+                        if (p.residual) v += p.residual[n];
+                    } else {
+                        float uv = 0.f;
+                        for (int w = 0; w < ncw; ++w) uv += red[(row + kUnitRows) * ncw + w];
+                        v = gemv_mma::act_fn(v, p.act) * (uv * out);
+                    }
+                    p.y[n] = v;
+                }
             }
         }
     };

@@ -183,19 +183,8 @@ __device__ __forceinline__ void task_bn(const uint8_t* smem, uint32_t a, int t, 
     }
 }
 
-// Every thread of every CTA of the cluster arrives, then waits (release / acquire).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// The same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
+using gemv_b1::cluster_sync_all;
+using gemv_b1::ld_cluster_f32;
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

@@ -83,6 +83,7 @@ GEMV_CASES = [
     (1000, 21504, 1), (2560, 9728, 1),  # one row: 12 phases; a ragged last phase (38 groups)
     (8, 8192, 1), (40000, 512, 1),      # one row: half a row-block pair; several passes
     (40, 65536, 1),                     # one row, operand records beyond shared memory: fallback kernel
+    (5376, 21504, 1), (2600, 16384, 1), # one row, K split over CTA pairs (uneven units per CTA)
     (24, 131328, 2),                    # two rows, records beyond the library array: fallback kernel
 ]
 
@@ -125,6 +126,21 @@ def test_gemv_residual_in_place(gem, torch_mod):
     gem.q4_0_gemv(_cu(t, W), N, K, _cu(t, x), y, residual=y)
     t.cuda.synchronize()
     assert_close(y.cpu().numpy(), ref, "gemv residual in place")
+
+
+@pytest.mark.parametrize("N,K,B", [(2600, 16384, 1), (2600, 16384, 2)])
+def test_gemv_residual_in_place_k_split(gem, torch_mod, N, K, B):
+    """Long K and more units than CTAs: the partial sums of a CTA pair (or cluster) are combined
+    before the residual is added, in place."""
+    t = torch_mod
+    W = gem_synth.q4_0_matrix(2, 8, N, K)
+    x = gem_synth.normal_f32(2, 9, (B, K))
+    r = gem_synth.normal_f32(2, 10, (B, N))
+    ref = oracle.q4_0_gemv(W, N, K, x, residual=r)
+    y = _cu(t, r)
+    gem.q4_0_gemv(_cu(t, W), N, K, _cu(t, x), y, residual=y)
+    t.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, "gemv residual in place, K split B=%d" % B)
 
 
 @pytest.mark.parametrize("N,K,B,offset", [(45, 96, 2, 0), (40, 512, 1, 2), (130, 3200, 3, 0)])
@@ -427,6 +443,8 @@ LAYER_CASES = [
     ("gemma-small-full", _small_gemma(True), 1, [300]),
     ("gemma4-31b-swa", configs.GEMMA31_SWA, 1, [32768]),
     ("gemma4-31b-full", configs.GEMMA31_FULL, 1, [32768]),
+    # hidden 16384: the QKV and fused gate/up projections split K over CTA pairs
+    ("wide-hidden", replace(configs.QWEN3_1_7B, H=16384, F=2816), 1, [700]),
 ]
 
 

@@ -238,24 +238,26 @@ def time_graph(torch, g, reps, warmup=3):
 # ---- arms -------------------------------------------------------------------------------------
 
 def run_kernel_only(args):
-    """A single op on its own (for ncu captures): `gemv` = the 31B FFN projection
-    (K=5376, N=21504) over 8 rotated matrices at --batch; `attn` = GQA decode attention over
-    the workload's first --layers caches."""
+    """A single op on its own (for ncu captures): `gemv` = a 31B FFN projection over --mats
+    rotated matrices at --batch (--gemv-shape up: K=5376 -> N=21504; down: K=21504 -> N=5376);
+    `attn` = GQA decode attention over the workload's first --layers caches."""
     import torch
     import q4_gemv_gqa_gb300 as gem
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     res = {"kernel": args.kernel}
     if args.kernel == "gemv":
         B = args.batch
-        mats = [torch.from_numpy(gem_synth.q4_0_matrix(0, 5000 + i, 21504, 5376)).cuda()
+        N, K = (21504, 5376) if args.gemv_shape == "up" else (5376, 21504)
+        res["shape"] = {"N": N, "K": K, "B": B}
+        mats = [torch.from_numpy(gem_synth.q4_0_matrix(0, 5000 + i, N, K)).cuda()
                 for i in range(args.mats)]
-        x = torch.from_numpy(gem_synth.normal_f32(0, 6000, (B, 5376))).cuda()
-        y = torch.empty((B, 21504), device="cuda")
+        x = torch.from_numpy(gem_synth.normal_f32(0, 6000, (B, K))).cuda()
+        y = torch.empty((B, N), device="cuda")
 
         def run():
             for W in mats:
-                gem.q4_0_gemv(W, 21504, 5376, x, y)
-        b = gemv_bytes(21504, 5376, B)
+                gem.q4_0_gemv(W, N, K, x, y)
+        b = gemv_bytes(N, K, B)
         n = len(mats)
     else:
         wl = configs.workload(args.workload)
@@ -563,6 +565,8 @@ def main():
                     help="time one op alone (for profiler captures) instead of the step")
     ap.add_argument("--batch", type=int, default=1, help="--kernel gemv: activation rows")
     ap.add_argument("--mats", type=int, default=8, help="--kernel gemv: rotated matrices")
+    ap.add_argument("--gemv-shape", choices=["up", "down"], default="up",
+                    help="--kernel gemv: 31B FFN up (5376 -> 21504) or down (21504 -> 5376) projection")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -42,6 +42,7 @@ constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kRecBytes = 512;   // activation record of one half group: 8 columns x 8 tiles x 8 B
 constexpr int kZeroBytes = 96;   // the operand of lanes off the block diagonal (bytes 32..95)
 constexpr int kPro = 4;          // float4s of the activation row kept per consumer thread
+constexpr int kProSplit = 6;     // the same for a CTA of a K split (its range only)
 constexpr int kMaxRps = 3;       // row blocks per stage at most
 
 struct Params {
@@ -256,11 +257,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     const int K = G * 256, K4 = K / 4;
     // this CTA's records cover groups [gk0, gk0 + Gr): float4s [kr0, kr1) of the row
     const int kr0 = gk0 * 64, kr1 = (gk0 + Gr) * 64;
-    // Rows of up to kPro float4 per consumer thread are read once and kept in registers; longer
-    // ones are read twice (statistics, then the records).
-    const bool onepass = K4 <= kPro * nct;
-    float4 xv[kPro];
-    // 1. largest |gamma * x| and sum of x^2 over the row
+    // Without a fused RMSNorm the CTAs of a K split scale their own range by their own power of
+    // two (exact) and unscale their partial sums before the cluster adds them, so each reads only
+    // its range; the norm's sum of squares needs the whole row.
+    const bool own_range = KS > 1 && !p.gamma;
+    const int sr0 = own_range ? kr0 : 0, sr1 = own_range ? kr1 : K4;   // float4s the statistics read
+    // Up to kProN float4 per consumer thread are read once and kept in registers; longer ranges
+    // are read twice (statistics, then the records).
+    constexpr int kProN = KS > 1 ? kProSplit : kPro;
+    const bool onepass = sr1 - sr0 <= kProN * nct;
+    float4 xv[kProN];
+    // 1. largest |gamma * x| and sum of x^2 over the statistics' range
     {
         float mx = 0.f, ss = 0.f;
         const float4* x4 = reinterpret_cast<const float4*>(p.x);
@@ -276,14 +283,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
         };
         if (onepass) {
 #pragma unroll
-            for (int u = 0; u < kPro; ++u) {
-                const int i = tid + u * nct;
+            for (int u = 0; u < kProN; ++u) {
+                const int i = sr0 + tid + u * nct;
                 xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < K4) xv[u] = take(__ldg(x4 + i), i);
+                if (i < sr1) xv[u] = take(__ldg(x4 + i), i);
             }
         } else {
 #pragma unroll 4
-            for (int i = tid; i < K4; i += nct) (void)take(__ldg(x4 + i), i);
+            for (int i = sr0 + tid; i < sr1; i += nct) (void)take(__ldg(x4 + i), i);
         }
         mx = warp_max(mx);
         ss = warp_sum(ss);
@@ -318,8 +325,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
         if (onepass) {
             // scatter my float4s: element m of a block's nibble half goes to the slot of qs byte m
 #pragma unroll
-            for (int u = 0; u < kPro; ++u) {
-                const int i = tid + u * nct;
+            for (int u = 0; u < kProN; ++u) {
+                const int i = sr0 + tid + u * nct;
                 if (i >= kr0 && i < kr1) {
                     const int k0 = 4 * i;
                     const int blk = (k0 >> 5) & 7, e0 = k0 & 31;
@@ -448,13 +455,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
             const float out = misc[65];
             const int rows_in_pass = nrb * kUnitRows;
             if constexpr (KS > 1) {
-                // this CTA's sums over its K range per row, into the (now idle) records; the
-                // cluster then adds its ks ranges in rank order
+                // this CTA's sums over its K range per row (unscaled when the CTA scaled its own
+                // range), into the (now idle) records; the cluster then adds its ks ranges in rank
+                // order
                 float* part = reinterpret_cast<float*>(smem + p.xf_off);
+                const float pscale = own_range ? out : 1.f;
                 for (int row = tid; row < rows_in_pass; row += nct) {
                     float v = 0.f;
                     for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
-                    part[row] = v;
+                    part[row] = v * pscale;
                 }
                 cluster_sync_all();
                 const int nout = nrb / NMAT * kUnitRows;   // output rows of the pass
@@ -468,11 +477,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                     for (int r = 0; r < ks; ++r) v += ld_cluster_f32(part + row, static_cast<uint32_t>(r));
                     if (NMAT == 2)
                         for (int r = 0; r < ks; ++r) uv += ld_cluster_f32(part + row + kUnitRows, static_cast<uint32_t>(r));
-                    v *= out;
+                    const float cs = own_range ? 1.f : out;
+                    v *= cs;
                     if (NMAT == 1) {
                         if (p.residual) v += p.residual[n];
                     } else {
-                        v = gemv_mma::act_fn(v, p.act) * (uv * out);
+                        v = gemv_mma::act_fn(v, p.act) * (uv * cs);
                     }
                     p.y[n] = v;
                 }

@@ -84,6 +84,7 @@ GEMV_CASES = [
     (8, 8192, 1), (40000, 512, 1),      # one row: half a row-block pair; several passes
     (40, 65536, 1),                     # one row, operand records beyond shared memory: fallback kernel
     (5376, 21504, 1), (2600, 16384, 1), # one row, K split over CTA pairs (uneven units per CTA)
+    (2600, 32768, 1),                   # the same, each CTA's half of the row read twice
     (24, 131328, 2),                    # two rows, records beyond the library array: fallback kernel
 ]
 

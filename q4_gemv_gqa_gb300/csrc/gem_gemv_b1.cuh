@@ -242,10 +242,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
         } else {
             pdl_trigger();
         }
-        if constexpr (KS > 1) {   // the two cluster barriers of the consumers' combine
+        if constexpr (KS > 1) {   // the consumers' combine: two cluster barriers per pass (one pass)
             __syncwarp();
-            cluster_sync_all();
-            cluster_sync_all();
+            for (int i = 0; i < 2 * npass; ++i) cluster_sync_all();
         }
         return;
     }

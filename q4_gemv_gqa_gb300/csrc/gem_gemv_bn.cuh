@@ -298,9 +298,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
             pdl_trigger();
         }
         __syncwarp();
-        if (ks > 1) {   // the two cluster barriers of the consumers' combine
-            cluster_sync_all();
-            cluster_sync_all();
+        if (ks > 1) {   // the consumers' combine: two cluster barriers per pass (one pass)
+            for (int i = 0; i < 2 * npass; ++i) cluster_sync_all();
         }
         return;
     }

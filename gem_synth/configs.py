@@ -132,5 +132,32 @@ def layer_tensors(shape: LayerShape, B: int, cap: int, seed: int, layer: int) ->
     )
 
 
+def layer_weights(shape: LayerShape, seed: int, layer: int) -> LayerTensors:
+    """The weights and norm weights of layer_tensors() (same draws), without the caches."""
+    s, L = shape, layer
+    return LayerTensors(
+        w_qkv=q4_0_matrix(seed, tid(L, ROLE_W_QKV), s.n_qkv, s.H),
+        w_o=q4_0_matrix(seed, tid(L, ROLE_W_O), s.H, s.n_q * s.d),
+        w_gate=q4_0_matrix(seed, tid(L, ROLE_W_GATE), s.F, s.H),
+        w_up=q4_0_matrix(seed, tid(L, ROLE_W_UP), s.F, s.H),
+        w_down=q4_0_matrix(seed, tid(L, ROLE_W_DOWN), s.H, s.F),
+        g_attn=norm_weight(seed, tid(L, ROLE_G_ATTN), s.H),
+        g_ffn=norm_weight(seed, tid(L, ROLE_G_FFN), s.H),
+        g_q=norm_weight(seed, tid(L, ROLE_G_Q), s.d) if s.qk_norm else None,
+        g_k=norm_weight(seed, tid(L, ROLE_G_K), s.d) if s.qk_norm else None,
+        g_post_attn=norm_weight(seed, tid(L, ROLE_G_POST_ATTN), s.H) if s.post_norms else None,
+        g_post_ffn=norm_weight(seed, tid(L, ROLE_G_POST_FFN), s.H) if s.post_norms else None,
+        k_cache=None,
+        v_cache=None,
+    )
+
+
+def kv_cache(shape: LayerShape, B: int, cap: int, seed: int, layer: int) -> tuple:
+    """The (K, V) caches of layer_tensors() (same draws): uint16 [B, n_kv, cap, d] each."""
+    s, L = shape, layer
+    return (normal_f16_bits(seed, tid(L, ROLE_K_CACHE), (B, s.n_kv, cap, s.d)),
+            normal_f16_bits(seed, tid(L, ROLE_V_CACHE), (B, s.n_kv, cap, s.d)))
+
+
 def layer_input(H: int, B: int, seed: int) -> np.ndarray:
     return normal_f32(seed, tid(0, ROLE_X), (B, H))

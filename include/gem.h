@@ -13,8 +13,14 @@
  *
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller.  The library never
- *     allocates device memory; calls that need scratch take a caller-provided workspace
- *     whose size is returned by the matching *_workspace() query.
+ *     allocates device memory in a call (gem_step_plan_create, a set-up call, is the one
+ *     exception); calls that need scratch take a caller-provided workspace whose size is
+ *     returned by the matching *_workspace() query.  Two calls keep their scratch in arrays
+ *     of the library instead, one per device: gem_q4_0_gemv with B >= 2 (its operand records,
+ *     4 MiB) and gem_gqa_decode_attn_noalloc (its split partials, 8 MiB).  Calls of the same
+ *     one of these two that can run at the same time on one device (different streams) race
+ *     on its array; calls issued in order on one stream are safe.  gem_q4_0_gemv_ws and
+ *     gem_gqa_decode_attn take a caller workspace and share nothing.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Every
  *     call only enqueues work and returns; results are ready when the stream reaches them.
  *   - Activations are fp32, row-major [B][...] with the given row stride (in elements).
@@ -74,6 +80,38 @@ GEM_API int gem_version(void);
  * GEM_ERR_CUDA.  Not for use inside stream capture. */
 GEM_API gem_status gem_device_status(int32_t *flags, int reset);
 
+/* The status that a set of GEM_DEVFLAG_* bits (from gem_device_status() or a caller's own
+ * status word) stands for: GEM_ERR_TIMEOUT when GEM_DEVFLAG_TIMEOUT is set, else
+ * GEM_ERR_DEVICE_FLAG when any other bit is set, else GEM_OK.  Host only; no device call. */
+GEM_API gem_status gem_status_from_flags(int32_t flags);
+
+/*
+ * Failure detection controls.  The pages have no counterpart of these calls: they let a
+ * caller bound how long a kernel may wait for a copy or a grid barrier, and let tests make
+ * one such wait run out without faulting or hanging the GPU.
+ *
+ * gem_set_wait_limit  sets the wall-time limit of every device-side wait (mbarrier waits on
+ *         asynchronous copies, grid barriers of gem_decode_step) on the current device, in
+ *         nanoseconds; 0 restores the default of 1 s.  Accepted range 1000 .. 60e9 ns, else
+ *         GEM_ERR_INVALID_ARG.  A wait that runs out sets GEM_DEVFLAG_TIMEOUT, lets the
+ *         copies it issued land (again bounded) and leaves the kernel; the outputs of that
+ *         call are then unspecified.  Synchronous: call it while no library kernel runs on
+ *         the device, outside stream capture.
+ * gem_set_test_injection  sets GEM_INJECT_* bits on the current device (0 clears them),
+ *         same synchronisation rules.  While set:
+ *           GEM_INJECT_RING_SHORTFALL  the one-row Q4_0 GEMV (B = 1, K % 256 == 0) makes
+ *             CTA 0 expect 16 bytes more than its last ring stage receives, so that stage's
+ *             wait runs out after the wait limit (every copy still lands);
+ *           GEM_INJECT_GRID_ARRIVAL  gem_decode_step makes CTA 0 leave out its arrival at
+ *             the step's first grid barrier, so every CTA's barrier wait runs out and the
+ *             step is aborted (the plan must then be destroyed and created again).
+ *         Meant for tests of the timeout path only.
+ */
+#define GEM_INJECT_RING_SHORTFALL 1
+#define GEM_INJECT_GRID_ARRIVAL 2
+GEM_API gem_status gem_set_wait_limit(uint64_t ns);
+GEM_API gem_status gem_set_test_injection(int mask);
+
 /*
  * Q4_0 dequantise-and-matvec  [GEM] "Native Metal diagnostic: buffer ownership": the
  * SIMD-group Q4_0 matvec at the 31B FFN shape (5376 -> 21504) and the scalar C check.
@@ -86,11 +124,47 @@ GEM_API gem_status gem_device_status(int32_t *flags, int reset);
  *   Accumulation is fp32.  y must not overlap W or x.
  *   For B >= 2 the call converts x into tensor-core operand records first (a second launch on the
  *   same stream), kept in a library-owned array of 4 MiB per device (K <= 130816): calls on two
- *   streams of one device that may run at the same time must not both have B >= 2.
- *   gem_decode_layer keeps its records in its own workspace instead.
+ *   streams of one device that may run at the same time must not both have B >= 2.  Use
+ *   gem_q4_0_gemv_ws to give each call its own records instead.
  */
 GEM_API gem_status gem_q4_0_gemv(const void *W, int64_t N, int64_t K, const float *x, int64_t ldx,
                          int B, float *y, int64_t ldy, const float *residual, void *stream);
+
+/*
+ * gem_q4_0_gemv with a caller-provided workspace for the operand records of a 2..8-row call,
+ * so calls on concurrently running streams share no state.  Same arithmetic, layout and
+ * errors as gem_q4_0_gemv, plus:
+ *   workspace  device scratch of gem_q4_0_gemv_workspace(B, K) bytes, 256-byte aligned
+ *              (else GEM_ERR_MISALIGNED); contents need no initialisation.  When the query
+ *              returns 0 (B = 1) workspace may be NULL; otherwise a missing or smaller
+ *              workspace is GEM_ERR_WORKSPACE and nothing is launched.
+ */
+GEM_API size_t gem_q4_0_gemv_workspace(int B, int64_t K);
+GEM_API gem_status gem_q4_0_gemv_ws(const void *W, int64_t N, int64_t K, const float *x,
+                                    int64_t ldx, int B, float *y, int64_t ldy,
+                                    const float *residual, void *workspace, size_t ws_bytes,
+                                    void *stream);
+
+/*
+ * The Q4_0 GEMV with the pre-norm and the gated activation fused in: the form the layer step
+ * runs for its QKV projection (norm), its gate/up pair (norm, two matrices, activation) and
+ * its O / down projections (residual).  [GELO] 06 block topology (pre-norm before the merged
+ * QKV and before the merged gate/up projections, gated activation); [GEM] "Native Metal
+ * diagnostic: buffer ownership" (the gate+up two-matrix single launch).
+ *
+ *   xh[b]  = gamma ? x[b] / sqrt(mean_k x[b][k]^2 + eps) * gamma : x[b]
+ *   W1 NULL:  y[b][n] = sum_k deq(W0)[n][k] xh[b][k]  (+ residual[b][n])
+ *   W1 set:   y[b][n] = act(sum_k deq(W0)[n][k] xh[b][k]) * sum_k deq(W1)[n][k] xh[b][k]
+ *             act 0: silu, 1: gelu_tanh (as gem_swiglu); residual must be NULL.
+ *   W0, W1  N x K Q4_0 (same layout as gem_q4_0_gemv); gamma [K] fp32 or NULL; eps >= 0.
+ *   Other arguments, the workspace (gem_q4_0_gemv_workspace(B, K) bytes for B >= 2) and the
+ *   errors are those of gem_q4_0_gemv_ws.
+ */
+GEM_API gem_status gem_q4_0_gemv_fused(const void *W0, const void *W1, int64_t N, int64_t K,
+                                       const float *x, int64_t ldx, int B, const float *gamma,
+                                       float eps, int act, float *y, int64_t ldy,
+                                       const float *residual, void *workspace, size_t ws_bytes,
+                                       void *stream);
 
 /*
  * Weighted RMSNorm  [GEM] "weighted RMSNorm over one or many heads"; [GELO] 06 pre-norm.
@@ -157,6 +231,25 @@ GEM_API gem_status gem_gqa_decode_attn(const float *q, int64_t ldq, const uint16
                                int32_t *status, void *stream);
 
 /*
+ * QK-norm, RoPE, KV append and decode attention in one call: the form the layer step runs.
+ * [GELO] 02/05/06 and [GEM] as for gem_rmsnorm_qknorm_rope and gem_gqa_decode_attn.
+ *   Same result as gem_rmsnorm_qknorm_rope(qkv, ...) followed by gem_gqa_decode_attn(q = qkv,
+ *   ...): the caches receive the new rows and out the attention output.  For head_dim <= 256
+ *   and n_q / n_kv <= 4 it is one launch (the attention kernel normalises and rotates its
+ *   query heads and appends the new rows itself, leaving qkv unchanged); other shapes take
+ *   the two launches (qkv's Q and K columns are then left normalised and rotated).  Treat
+ *   qkv as unspecified after the call.  The workspace is gem_gqa_decode_attn_workspace()'s.
+ */
+GEM_API gem_status gem_gqa_decode_attn_fused(const float *qkv, int64_t ldqkv, int B, int n_q,
+                                             int n_kv, int d, const float *gamma_q,
+                                             const float *gamma_k, int v_mode, float eps,
+                                             const int32_t *pos, float theta, int rope_dim,
+                                             uint16_t *k_cache, uint16_t *v_cache,
+                                             int64_t cache_cap, int window, float scale,
+                                             float *out, int64_t ldo, void *workspace,
+                                             size_t ws_bytes, int32_t *status, void *stream);
+
+/*
  * gem_gqa_decode_attn without a caller-supplied workspace: the split partials live in a
  * fixed array inside the library, so the call allocates no device memory at all (no
  * cudaMalloc/cudaFree, no allocating library routine).  The decode-attention pages have no
@@ -168,10 +261,15 @@ GEM_API gem_status gem_gqa_decode_attn(const float *q, int64_t ldq, const uint16
  *   - plain C callers that have no device allocator of their own for a scratch buffer.
  * Arguments, results and errors are those of gem_gqa_decode_attn (same kernels, same split
  * plan, so the output is bit-identical to that call's), except:
- *   - the split partials need gem_gqa_decode_attn_workspace() bytes for the same shape; when
- *     that exceeds GEM_ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) the call launches nothing and
- *     returns GEM_ERR_WORKSPACE.  (On a 152-SM GPU every supported shape with
- *     B * n_kv <= 152 fits; the largest such need is about 7.5 MB.)
+ *   - the split partials need gem_gqa_decode_attn_workspace() bytes for the same shape,
+ *     B * n_q * ns * (d + 2) * 4 bytes where ns is the split count of the plan.  ns grows
+ *     with the number of SMs (about 2 * SMs / (B * n_kv) splits) and, for d = 512 or
+ *     n_q / n_kv = 8, with the attended range: each split covers at most 1024 positions, so
+ *     ns >= ceil(min(window or cache_cap, cache_cap) / 1024).  When the need exceeds
+ *     GEM_ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) the call launches nothing and returns
+ *     GEM_ERR_WORKSPACE.  Example on a 152-SM GPU: the 4-KV-head, d = 512, n_q = 32 layer with
+ *     cache_cap = 32769 fits at B = 1 (76 splits, 5.0 MB) but not at B = 8 (33 splits, 17.4 MB); query
+ *     gem_gqa_decode_attn_workspace() to know before calling.
  *   - the array exists once per device and every call on that device shares it.  Calls issued
  *     in order on one stream are safe; two calls that can run at the same time on one device
  *     (different streams, or different host threads with different streams) race on the

@@ -22,9 +22,10 @@ ACT_GELU_TANH = 1
 DEVFLAG_POS_RANGE = 1
 DEVFLAG_TIMEOUT = 2
 
-__all__ = ["GemError", "q4_0_gemv", "rmsnorm", "rmsnorm_qknorm_rope", "gqa_decode_attn",
-           "gqa_decode_attn_workspace", "swiglu", "decode_layer", "decode_layer_workspace",
-           "DeviceLayer", "device_status", "LayerDesc"]
+__all__ = ["GemError", "q4_0_gemv", "q4_0_gemv_workspace", "q4_0_gemv_fused", "rmsnorm", "rmsnorm_qknorm_rope", "gqa_decode_attn",
+           "gqa_decode_attn_workspace", "gqa_decode_attn_fused", "swiglu", "decode_layer", "decode_layer_workspace",
+           "DeviceLayer", "device_status", "status_from_flags", "set_wait_limit",
+           "set_test_injection", "LayerDesc"]
 
 
 class GemError(RuntimeError):
@@ -89,17 +90,83 @@ def device_status(reset: bool = False) -> int:
     return v.value
 
 
+def status_from_flags(flags: int) -> int:
+    """gem_status that a set of GEM_DEVFLAG_* bits stands for (host only)."""
+    return int(lib.gem_status_from_flags(flags))
+
+
+INJECT_RING_SHORTFALL = 1
+INJECT_GRID_ARRIVAL = 2
+
+
+def set_wait_limit(ns: int) -> None:
+    """Wall-time limit of every device-side wait on the current device (0: default 1 s)."""
+    _check(lib.gem_set_wait_limit(int(ns)), "gem_set_wait_limit")
+
+
+def set_test_injection(mask: int) -> None:
+    """GEM_INJECT_* bits: make one bounded wait run out (tests of the timeout path)."""
+    _check(lib.gem_set_test_injection(int(mask)), "gem_set_test_injection")
+
+
+def q4_0_gemv_workspace(B: int, K: int) -> int:
+    return int(lib.gem_q4_0_gemv_workspace(B, K))
+
+
 def q4_0_gemv(W: torch.Tensor, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
-              residual: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y[b] = deq(W) @ x[b] (+ residual[b]).  x: [B, >=K] fp32, y: [B, >=N] fp32."""
+              residual: torch.Tensor | None = None, stream=None,
+              workspace: torch.Tensor | None = None, shared_records: bool = False) -> torch.Tensor:
+    """y[b] = deq(W) @ x[b] (+ residual[b]).  x: [B, >=K] fp32, y: [B, >=N] fp32.
+
+    With B >= 2 the call goes through gem_q4_0_gemv_ws with `workspace` (a uint8 device tensor
+    of q4_0_gemv_workspace(B, K) bytes; allocated here when not given), so concurrent calls
+    share no state.  shared_records=True calls gem_q4_0_gemv instead, whose records live in
+    the library's own per-device array."""
     B = x.shape[0] if x.dim() == 2 else 1
     _q4_bytes(W, N, K)
     if x.shape[-1] < K or y.shape[-1] < N:
         raise ValueError("x must have >= K columns and y >= N")
-    st = lib.gem_q4_0_gemv(_dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"),
-                           x.shape[-1], B, _dev(y, torch.float32, "y"), y.shape[-1],
-                           _dev(residual, torch.float32, "residual"), _stream(stream))
-    _check(st, "gem_q4_0_gemv")
+    need = q4_0_gemv_workspace(B, K) if K % 32 == 0 else 0
+    if shared_records or need == 0:
+        st = lib.gem_q4_0_gemv(_dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"),
+                               x.shape[-1], B, _dev(y, torch.float32, "y"), y.shape[-1],
+                               _dev(residual, torch.float32, "residual"), _stream(stream))
+        _check(st, "gem_q4_0_gemv")
+        return y
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    st = lib.gem_q4_0_gemv_ws(_dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"),
+                              x.shape[-1], B, _dev(y, torch.float32, "y"), y.shape[-1],
+                              _dev(residual, torch.float32, "residual"),
+                              _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                              _stream(stream))
+    _check(st, "gem_q4_0_gemv_ws")
+    return y
+
+
+def q4_0_gemv_fused(W0: torch.Tensor, W1: torch.Tensor | None, N: int, K: int, x: torch.Tensor,
+                    y: torch.Tensor, gamma: torch.Tensor | None = None, eps: float = 1e-6,
+                    act: int = ACT_SILU, residual: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Pre-norm (gamma) + Q4_0 GEMV, or the gate/up pair (W1) with the gated activation.
+    x: [B, >=K] fp32, y: [B, >=N] fp32; workspace as for q4_0_gemv (allocated when needed)."""
+    B = x.shape[0] if x.dim() == 2 else 1
+    _q4_bytes(W0, N, K)
+    if W1 is not None:
+        _q4_bytes(W1, N, K)
+    if x.shape[-1] < K or y.shape[-1] < N:
+        raise ValueError("x must have >= K columns and y >= N")
+    need = q4_0_gemv_workspace(B, K) if K % 32 == 0 else 0
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    st = lib.gem_q4_0_gemv_fused(_dev(W0, torch.uint8, "W0"), _dev(W1, torch.uint8, "W1"), N, K,
+                                 _dev(x, torch.float32, "x"), x.shape[-1], B,
+                                 _dev(gamma, torch.float32, "gamma"), eps, act,
+                                 _dev(y, torch.float32, "y"), y.shape[-1],
+                                 _dev(residual, torch.float32, "residual"),
+                                 _dev(workspace, torch.uint8, "workspace") if need else None,
+                                 workspace.numel() if need else 0, _stream(stream))
+    _check(st, "gem_q4_0_gemv_fused")
     return y
 
 
@@ -150,6 +217,27 @@ def gqa_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
         _dev(pos, torch.int32, "pos"), window, scale, _dev(out, torch.float32, "out"),
         out.shape[-1], ws_ptr, ws_bytes, _dev(status, torch.int32, "status"), _stream(stream))
     _check(st, "gem_gqa_decode_attn")
+    return out
+
+
+def gqa_decode_attn_fused(qkv: torch.Tensor, n_q: int, n_kv: int, d: int,
+                          gamma_q: torch.Tensor | None, gamma_k: torch.Tensor | None, v_mode: int,
+                          eps: float, pos: torch.Tensor, theta: float, rope_dim: int,
+                          k_cache: torch.Tensor, v_cache: torch.Tensor, window: int, scale: float,
+                          out: torch.Tensor, workspace: torch.Tensor | None = None,
+                          status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """QK-norm + RoPE + KV append + attention from the raw QKV projection row (qkv [B, ldqkv])."""
+    B = qkv.shape[0]
+    cap = _cache_shape(k_cache, v_cache, B, n_kv, d)
+    st = lib.gem_gqa_decode_attn_fused(
+        _dev(qkv, torch.float32, "qkv"), qkv.shape[-1], B, n_q, n_kv, d,
+        _dev(gamma_q, torch.float32, "gamma_q"), _dev(gamma_k, torch.float32, "gamma_k"), v_mode, eps,
+        _dev(pos, torch.int32, "pos"), theta, rope_dim, _dev(k_cache, _HALF_BITS, "k_cache"),
+        _dev(v_cache, _HALF_BITS, "v_cache"), cap, window, scale, _dev(out, torch.float32, "out"),
+        out.shape[-1], _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel() if workspace is not None else 0, _dev(status, torch.int32, "status"),
+        _stream(stream))
+    _check(st, "gem_gqa_decode_attn_fused")
     return out
 
 

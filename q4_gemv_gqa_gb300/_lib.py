@@ -32,13 +32,22 @@ PROTOTYPES = {
     "gem_last_cuda_error": (i32, []),
     "gem_version": (i32, []),
     "gem_device_status": (i32, [p, i32]),
+    "gem_status_from_flags": (i32, [i32]),
+    "gem_set_wait_limit": (i32, [C.c_uint64]),
+    "gem_set_test_injection": (i32, [i32]),
     "gem_q4_0_gemv": (i32, [p, i64, i64, p, i64, i32, p, i64, p, p]),
+    "gem_q4_0_gemv_workspace": (C.c_size_t, [i32, i64]),
+    "gem_q4_0_gemv_ws": (i32, [p, i64, i64, p, i64, i32, p, i64, p, p, C.c_size_t, p]),
+    "gem_q4_0_gemv_fused": (i32, [p, p, i64, i64, p, i64, i32, p, C.c_float, i32, p, i64, p, p,
+                                  C.c_size_t, p]),
     "gem_rmsnorm": (i32, [p, i32, i64, p, C.c_float, p, p]),
     "gem_rmsnorm_qknorm_rope": (i32, [p, i64, i32, i32, i32, i32, p, p, i32, C.c_float, p,
                                       C.c_float, i32, p, p, i64, i32, p, p]),
     "gem_gqa_decode_attn_workspace": (C.c_size_t, [i32, i32, i32, i32, i64, i32]),
     "gem_gqa_decode_attn": (i32, [p, i64, p, p, i32, i32, i32, i32, i64, p, i32, C.c_float,
                                   p, i64, p, C.c_size_t, p, p]),
+    "gem_gqa_decode_attn_fused": (i32, [p, i64, i32, i32, i32, i32, p, p, i32, C.c_float, p, C.c_float,
+                                        i32, p, p, i64, i32, C.c_float, p, i64, p, C.c_size_t, p, p]),
     "gem_gqa_decode_attn_noalloc": (i32, [p, i64, p, p, i32, i32, i32, i32, i64, p, i32,
                                           C.c_float, p, i64, p, p]),
     "gem_swiglu": (i32, [p, p, i32, i64, i32, p, p]),

@@ -12,8 +12,10 @@
 // through one ring of shared-memory stages with TMA (2-D map over [B*n_kv*cap][d]
 // binary16, boxes of TP rows x 64 elements, 128-byte swizzle so ldmatrix is conflict-free).
 // When launched inside the layer chain, the tiles are requested before
-// griddepcontrol.wait: only the new token's slot is written by the preceding kernel, and
-// that one row is re-read after the wait.
+// griddepcontrol.wait.  That is safe under the library's launch rule (gem_device.cuh): the
+// kernel two or more launches back (e.g. the previous step's append of this layer) has
+// completed by then, and of the cache only the new token's slot can be written by the
+// immediately preceding kernel; that one row is re-read (or, fused, produced) after the wait.
 //
 // Arithmetic.  Scores S = (scale q) K^T and the value sum P V run on mma.sync m16n8k16
 // (binary16 inputs, fp32 accumulate).  K and V are binary16 already (exact operands); q
@@ -138,12 +140,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid
     const int L = P.ltile * TP;       // score row length
     const int QA = D + 8, PA = L + 8;  // padded row pitches (elements)
 
-    if (!P.early) pdl_wait();
+    if (!P.early) pdl_wait_trigger();
     const int p = P.pos[b];
     const bool bad = p < 0 || (P.window == 0 && static_cast<int64_t>(p) >= P.cap);
     if (bad) {  // every CTA waits before leaving, so completion of this grid implies its predecessor's
-        pdl_trigger();
-        if (P.early) pdl_wait();
+        if (P.early) pdl_wait_trigger();
         if (t == 0 && split == 0 && g == 0) atomicOr(P.status, GEM_DEVFLAG_POS_RANGE);
         return;
     }
@@ -151,8 +152,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid
     int nsplit, t0, t1;
     split_range(T, TP, P.nsplit_max, split, nsplit, t0, t1);
     if (split >= nsplit) {
-        pdl_trigger();
-        if (P.early) pdl_wait();
+        if (P.early) pdl_wait_trigger();
         return;
     }
     const int ntile = t1 - t0;
@@ -188,8 +188,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid
     }
     __shared__ int s_npre;
     if (t == 0) s_npre = npre;
-    pdl_trigger();
-    if (P.early) pdl_wait();
+    if (P.early) pdl_wait_trigger();
 
     // q of this KV head's G query heads -> A operand rows (hi in rows 0..7, lo in 8..15).
     // All loads of a thread are issued before any is used: one L2 round trip in total.
@@ -426,12 +425,11 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     const int gq = lane >> 2, tq = lane & 3;
     const int G = P.G;
 
-    if (!P.early) pdl_wait();
+    if (!P.early) pdl_wait_trigger();
     const int p = P.pos[b];
     const bool bad = p < 0 || (P.window == 0 && static_cast<int64_t>(p) >= P.cap);
     if (bad) {
-        pdl_trigger();
-        if (P.early) pdl_wait();
+        if (P.early) pdl_wait_trigger();
         if (t_id == 0 && split == 0 && g == 0) atomicOr(P.status, GEM_DEVFLAG_POS_RANGE);
         return;
     }
@@ -441,8 +439,7 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     // cluster merge: export area after the combine buffers (inside the idle rings)
     float* cexp = reinterpret_cast<float*>(smem) + 2 * kFlashWarps * 4 + kFlashWarps * 4 * D;
     if (split >= nsplit) {   // no tiles in this split (short prefix)
-        pdl_trigger();
-        if (P.early) pdl_wait();
+        if (P.early) pdl_wait_trigger();
         if (P.cluster)
             cluster_merge(cexp, G, D, nsplit, static_cast<uint32_t>(split), gridDim.x,
                           P.out + b * P.ldo + static_cast<int64_t>(g * G) * D);
@@ -486,8 +483,7 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
             cs[i] = c;
             sn[i] = s;
         }
-    pdl_trigger();
-    if (P.early) pdl_wait();
+    if (P.early) pdl_wait_trigger();
 
     const bool owner = slot_p >= t0 * kFlashTile && slot_p < t1 * kFlashTile;
     if (P.fuse) {
@@ -739,8 +735,7 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const AttnPara
     __shared__ float wsh[kMaxSplits], lsh[kMaxSplits];
     __shared__ float psum[kMergeThreads];
     __shared__ float red[kMergeThreads / 32];
-    pdl_trigger();
-    pdl_wait();
+    pdl_wait_trigger();
     const int bh = blockIdx.x;
     const int b = bh / P.n_q, h = bh - b * P.n_q;
     const int p = P.pos[b];
@@ -1050,6 +1045,10 @@ gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_lau
 gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, false); }
 bool attn_fusable(int n_q, int n_kv, int d) { return n_kv > 0 && n_q % n_kv == 0 && use_flash(n_q, n_kv, d); }
 gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, true); }
+// The fused form as a stand-alone call: nothing is read before griddepcontrol.wait.
+gem_status attn_enqueue_fused_standalone(const AttnOp& op, cudaStream_t stream) {
+    return attn_launch(op, stream, false, true);
+}
 
 // ---- split-partial scratch owned by the library (gem_gqa_decode_attn_noalloc) --------------
 // One fixed array per device (a module-scope __device__ variable exists once in every device
@@ -1112,6 +1111,72 @@ gem_status gem_gqa_decode_attn(const float* q, int64_t ldq, const uint16_t* k_ca
     op.ws_bytes = ws_bytes;
     op.status = status;
     return gem::attn_enqueue(op, static_cast<cudaStream_t>(stream));
+}
+
+gem_status gem_gqa_decode_attn_fused(const float* qkv, int64_t ldqkv, int B, int n_q, int n_kv, int d,
+                                     const float* gamma_q, const float* gamma_k, int v_mode, float eps,
+                                     const int32_t* pos, float theta, int rope_dim, uint16_t* k_cache,
+                                     uint16_t* v_cache, int64_t cache_cap, int window, float scale, float* out,
+                                     int64_t ldo, void* workspace, size_t ws_bytes, int32_t* status,
+                                     void* stream_v) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    gem::RopeOp rope{};
+    rope.qkv = const_cast<float*>(qkv);
+    rope.ldqkv = ldqkv;
+    rope.B = B;
+    rope.n_q = n_q;
+    rope.n_kv = n_kv;
+    rope.d = d;
+    rope.gamma_q = gamma_q;
+    rope.gamma_k = gamma_k;
+    rope.v_mode = v_mode;
+    rope.eps = eps;
+    rope.pos = pos;
+    rope.theta = theta;
+    rope.rope_dim = rope_dim;
+    rope.k_cache = k_cache;
+    rope.v_cache = v_cache;
+    rope.cache_cap = cache_cap;
+    rope.window = window;
+    rope.status = status;
+    gem::AttnOp op{};
+    op.q = qkv;
+    op.ldq = ldqkv;
+    op.k_cache = k_cache;
+    op.v_cache = v_cache;
+    op.B = B;
+    op.n_q = n_q;
+    op.n_kv = n_kv;
+    op.d = d;
+    op.cache_cap = cache_cap;
+    op.pos = pos;
+    op.window = window;
+    op.scale = scale;
+    op.out = out;
+    op.ldo = ldo;
+    op.workspace = workspace;
+    op.ws_bytes = ws_bytes;
+    op.status = status;
+    gem_status st;
+    if ((st = gem::rope_check(rope)) != GEM_OK || (st = gem::attn_check(op)) != GEM_OK) return st;
+    if (B == 0 || n_q == 0) return GEM_OK;
+    if (gem::attn_fusable(n_q, n_kv, d)) {
+        op.gamma_q = gamma_q;
+        op.gamma_k = gamma_k;
+        op.eps = eps;
+        op.theta = theta;
+        op.rope_dim = rope_dim;
+        op.v_mode = v_mode;
+        op.k_out = k_cache;
+        op.v_out = v_cache;
+        return gem::attn_enqueue_fused_standalone(op, stream);
+    }
+    // other shapes: the QK-norm / RoPE / append launch, then attention (as the layer chain does)
+    if (gem::attn_workspace_bytes(B, n_q, n_kv, d, cache_cap, window) > ws_bytes ||
+        (gem::attn_workspace_bytes(B, n_q, n_kv, d, cache_cap, window) && !workspace))
+        return GEM_ERR_WORKSPACE;
+    if ((st = gem::rope_enqueue(rope, stream)) != GEM_OK) return st;
+    return gem::attn_enqueue_in_chain(op, stream);
 }
 
 gem_status gem_gqa_decode_attn_noalloc(const float* q, int64_t ldq, const uint16_t* k_cache,

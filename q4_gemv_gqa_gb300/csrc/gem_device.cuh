@@ -15,11 +15,24 @@
 namespace gem {
 
 // ---- programmatic dependent launch --------------------------------------------------
-// Everything issued before pdl_wait() may only read data that no earlier kernel in the
-// stream writes (weights, old KV rows).  pdl_trigger() lets the next kernel in the stream
-// start its own prologue while this one runs.
+// The rule every kernel of the library keeps:
+//   (1) a thread executes pdl_trigger() only after it has itself returned from pdl_wait()
+//       (pdl_wait_trigger() does both), and no other thread of the CTA triggers earlier;
+//   (2) every CTA executes pdl_wait() (in at least one thread) before it exits.
+// griddepcontrol.wait returns once the preceding kernel of the stream has completed and its
+// writes are visible.  So by (1) the next kernel is launched only when every CTA of this one
+// has passed its wait, i.e. when the kernel BEFORE this one has completed; and by (2) the
+// completion of a kernel implies the completion of every earlier one.  Consequently a kernel
+// may read before its own pdl_wait() any data that the immediately preceding kernel does not
+// write: weights, positions, and K/V rows written by any kernel two or more launches back
+// (the previous decode step's appended rows included).  Data written by the immediately
+// preceding kernel is read only after the wait.  Nothing is written before the wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_trigger() {
+    pdl_wait();
+    pdl_trigger();
+}
 
 // ---- shared-memory addresses and mbarriers --------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -61,16 +74,38 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar`.  Gives up after GEM_WAIT_LIMIT_NS of wall time,
-// records GEM_DEVFLAG_TIMEOUT in *status and returns false.  A healthy wait takes
-// microseconds; the limit only guards against a copy that never lands.
+// ---- run-time controls of the bounded waits ----------------------------------------------
+// Each translation unit with kernels holds its own copy of these two words (module-scope
+// device variables exist per module); gem_set_wait_limit() and gem_set_test_injection()
+// write every registered copy on the current device.
+//   g_wait_limit_ns  wall-time limit of every device-side wait (default GEM_WAIT_LIMIT_NS);
+//   g_test_inject    GEM_INJECT_* bits: make one bounded wait run out on purpose (tests of
+//                    the timeout path; 0 in normal use).
+static __device__ unsigned long long g_wait_limit_ns = GEM_WAIT_LIMIT_NS;
+static __device__ int g_test_inject = 0;
+namespace {
+struct DeviceControlsRegistration {
+    DeviceControlsRegistration() { register_device_controls(&g_wait_limit_ns, &g_test_inject); }
+};
+const DeviceControlsRegistration g_device_controls_registration;
+}  // namespace
+
+__device__ __forceinline__ uint64_t wait_limit_ns() {
+    return *reinterpret_cast<const volatile unsigned long long*>(&g_wait_limit_ns);
+}
+__device__ __forceinline__ int test_inject() { return *reinterpret_cast<const volatile int*>(&g_test_inject); }
+
+// Wait for phase `parity` of `bar`.  Gives up after wait_limit_ns() of wall time, records
+// GEM_DEVFLAG_TIMEOUT in *status and returns false.  A healthy wait takes microseconds;
+// the limit only guards against a copy that never lands.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = wait_limit_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > GEM_WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit) {
             if (status) atomicOr(status, GEM_DEVFLAG_TIMEOUT);
             return false;
         }

@@ -32,8 +32,7 @@ __global__ void __launch_bounds__(512) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ gamma, float eps,
                                                       float* __restrict__ out) {
     __shared__ float red[32];
-    pdl_trigger();
-    pdl_wait();
+    pdl_wait_trigger();
     const float* xr = x + blockIdx.x * H;
     float* orow = out + blockIdx.x * H;
     float ss = 0.f;
@@ -47,8 +46,7 @@ __global__ void __launch_bounds__(512) postnorm_residual_kernel(float* __restric
                                                                 int64_t H, const float* __restrict__ gamma,
                                                                 float eps) {
     __shared__ float red[32];
-    pdl_trigger();
-    pdl_wait();
+    pdl_wait_trigger();
     const float* tr = t + blockIdx.x * H;
     float* xr = x + blockIdx.x * H;
     float ss = 0.f;
@@ -59,8 +57,7 @@ __global__ void __launch_bounds__(512) postnorm_residual_kernel(float* __restric
 
 __global__ void swiglu_kernel(const float* __restrict__ gate, const float* __restrict__ up, int64_t n, int act,
                               float* __restrict__ out) {
-    pdl_trigger();
-    pdl_wait();
+    pdl_wait_trigger();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
         out[i] = act_apply(gate[i], act) * up[i];
@@ -74,15 +71,14 @@ constexpr int kRopeWarps = 4;
 __global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const RopeOp op, const RopeFreq fr, int early) {
     __shared__ float buf[kRopeWarps][kMaxHeadDim];
     __shared__ float cs_tab[kMaxHeadDim / 2], sn_tab[kMaxHeadDim / 2];
-    pdl_trigger();
-    if (!early) pdl_wait();
+    if (!early) pdl_wait_trigger();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int b = blockIdx.y;
     const int d = op.d;
     const int p = op.pos[b];
     const bool bad = p < 0 || (op.window == 0 && static_cast<int64_t>(p) >= op.cache_cap);
     if (bad) {
-        if (early) pdl_wait();
+        if (early) pdl_wait_trigger();
         if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(op.status, GEM_DEVFLAG_POS_RANGE);
         return;
     }
@@ -93,7 +89,7 @@ __global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const Rope
         cs_tab[i] = c;
         sn_tab[i] = s;
     }
-    if (early) pdl_wait();  // q/k/v rows come from the preceding projection
+    if (early) pdl_wait_trigger();  // q/k/v rows come from the preceding projection
     __syncthreads();
     const int head = blockIdx.x * kRopeWarps + w;
     const int nheads = op.n_q + op.n_kv;

@@ -96,6 +96,74 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
 
 }  // namespace gem
 
+extern "C" size_t gem_q4_0_gemv_workspace(int B, int64_t K) {
+    if (B < 2 || B > 8 || K <= 0) return 0;
+    return gem::align_up(gem::gemv_rec_bytes(B, K), 256);
+}
+
+extern "C" gem_status gem_q4_0_gemv_ws(const void* W, int64_t N, int64_t K, const float* x, int64_t ldx, int B,
+                                       float* y, int64_t ldy, const float* residual, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+    gem::GemvOp op{};
+    op.W0 = W;
+    op.W1 = nullptr;
+    op.N = N;
+    op.K = K;
+    op.B = B;
+    op.x = x;
+    op.ldx = ldx;
+    op.y = y;
+    op.ldy = ldy;
+    op.residual = residual;
+    op.ldr = ldy;
+    op.norm_gamma = nullptr;
+    op.eps = 0.f;
+    op.act = 0;
+    gem_status st = gem::gemv_check(op);
+    if (st != GEM_OK || B == 0 || N == 0) return st;
+    const size_t need = gem_q4_0_gemv_workspace(B, K);
+    if (need) {
+        if (!workspace || ws_bytes < need) return GEM_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255) return GEM_ERR_MISALIGNED;
+        op.act_ws = workspace;
+        op.act_ws_bytes = ws_bytes;
+    }
+    return gem::gemv_enqueue(op, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" gem_status gem_q4_0_gemv_fused(const void* W0, const void* W1, int64_t N, int64_t K, const float* x,
+                                          int64_t ldx, int B, const float* gamma, float eps, int act, float* y,
+                                          int64_t ldy, const float* residual, void* workspace, size_t ws_bytes,
+                                          void* stream) {
+    gem::GemvOp op{};
+    op.W0 = W0;
+    op.W1 = W1;
+    op.N = N;
+    op.K = K;
+    op.B = B;
+    op.x = x;
+    op.ldx = ldx;
+    op.y = y;
+    op.ldy = ldy;
+    op.residual = residual;
+    op.ldr = ldy;
+    op.norm_gamma = gamma;
+    op.eps = eps;
+    op.act = act;
+    if (W1 && residual) return GEM_ERR_INVALID_ARG;
+    if (gamma && !(eps >= 0.f)) return GEM_ERR_INVALID_ARG;
+    gem_status st = gem::gemv_check(op);
+    if (st != GEM_OK || B == 0 || N == 0) return st;
+    const size_t need = gem_q4_0_gemv_workspace(B, K);
+    if (need) {
+        if (!workspace || ws_bytes < need) return GEM_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255) return GEM_ERR_MISALIGNED;
+        op.act_ws = workspace;
+        op.act_ws_bytes = ws_bytes;
+    }
+    return gem::gemv_enqueue(op, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" gem_status gem_q4_0_gemv(const void* W, int64_t N, int64_t K, const float* x, int64_t ldx, int B,
                                     float* y, int64_t ldy, const float* residual, void* stream) {
     gem::GemvOp op{};

@@ -214,13 +214,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                     for (int ph = 0; ph < nphr; ++ph) {
                         const int g0 = ph * gps;
                         const int ng = min(gps, Gr - g0);
-                        if (s == ns) pdl_trigger();   // ring filled once
                         if (s >= ns) {
                             ok = mbar_wait(&empty[slot], par, p.status);
                             if (!ok) break;
                         }
                         uint8_t* dst = smem + static_cast<size_t>(slot) * stage_bytes;
-                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nr * ng * kBoxBytes));
+                        // Test hook (GEM_INJECT_RING_SHORTFALL): CTA 0 expects 16 bytes more than
+                        // its last stage copies, so the consumers' wait on it runs out.  The last
+                        // stage's slot is never refilled, and every copy still lands.
+                        uint32_t extra = 0;
+                        if (KS == 1 && blockIdx.x == 0 && pass == npass - 1 && (v + 1) * rps >= nrb &&
+                            ph == nphr - 1 && (test_inject() & GEM_INJECT_RING_SHORTFALL))
+                            extra = 16;
+                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nr * ng * kBoxBytes) + extra);
                         for (int r = 0; r < nr; ++r) {
                             const int rb = v * rps + r;
                             const int row0 = (ub + rb / NMAT) * kUnitRows;
@@ -237,11 +243,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                     }
                 }
             }
-            if (s <= ns) pdl_trigger();
             if (!ok) drain_stages(full, ns, max(0, s - ns), s - 1);
-        } else {
-            pdl_trigger();
         }
+        // the producer warp never triggers dependents: the consumers do, after their wait
         if constexpr (KS > 1) {   // the consumers' combine: two cluster barriers per pass (one pass)
             __syncwarp();
             for (int i = 0; i < 2 * npass; ++i) cluster_sync_all();
@@ -250,8 +254,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     }
 
     // ---------------- consumer warps ----------------
-    pdl_trigger();
-    pdl_wait();   // the activations (and residual) come from the previous kernel
+    pdl_wait_trigger();   // the activations (and residual) come from the previous kernel
 
     const int K = G * 256, K4 = K / 4;
     // this CTA's records cover groups [gk0, gk0 + Gr): float4s [kr0, kr1) of the row

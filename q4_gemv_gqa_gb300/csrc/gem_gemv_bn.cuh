@@ -54,8 +54,7 @@ struct PrepParams {
 };
 
 __global__ void __launch_bounds__(kPrepThreads) act_prep_kernel(const PrepParams p) {
-    pdl_trigger();
-    pdl_wait();
+    pdl_wait_trigger();
     __shared__ float red_m[kPrepThreads / 32], red_s[kPrepThreads / 32];
     __shared__ float sc_sh;
     const int b = blockIdx.y, chunk = blockIdx.x;
@@ -250,7 +249,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                 const int nr = min(rps, nrb - v * rps);
                 const int g0 = ph * gps;
                 const int ng = min(gps, Gr - g0);
-                if (s == ns) pdl_trigger();
                 if (s >= ns && !mbar_wait(&empty[slot], par, p.status)) return false;
                 uint8_t* dst = smem + static_cast<size_t>(slot) * stage_bytes;
                 mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nr * ng * kBoxBytes));
@@ -292,11 +290,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                     for (int v = (q == 0 ? pre : 0); v < nv && ok; ++v) ok = issue(pass, ph, v);
                 }
             }
-            if (s <= ns) pdl_trigger();
             if (!ok) drain_stages(full, ns, max(0, s - ns), s - 1);
-        } else {
-            pdl_trigger();
         }
+        // the producer warp never triggers dependents: the consumers do, after their wait
         __syncwarp();
         if (ks > 1) {   // the consumers' combine: two cluster barriers per pass (one pass)
             for (int i = 0; i < 2 * npass; ++i) cluster_sync_all();
@@ -305,8 +301,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
     }
 
     // ---------------- consumer warps ----------------
-    pdl_trigger();
-    pdl_wait();   // row scales (and the residual) come from earlier kernels
+    pdl_wait_trigger();   // row scales (and the residual) come from earlier kernels
 
     const int g = lane >> 2, t = lane & 3;
     const int jg = warp >> 1;

@@ -36,8 +36,7 @@ __global__ void __launch_bounds__(256) q4_0_gemv_generic_kernel(const uint8_t* _
     __shared__ float rstd[8];
     __shared__ float red[8][8];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    pdl_trigger();
-    pdl_wait();
+    pdl_wait_trigger();
     if (p.gamma) {
         for (int b = 0; b < BATCH; ++b) {
             float part = 0.f;

@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
                     const int ul = rb / NMAT, m = rb % NMAT;
                     const int g0 = ph * p.gps;
                     const int ng = min(p.gps, p.G - g0);
-                    if (s == p.ns) pdl_trigger();   // ring filled once: weights only so far
                     if (s >= p.ns) {
                         ok = mbar_wait(&empty[slot], par, p.status);
                         if (!ok) break;
@@ -212,17 +211,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
                     }
                 }
             }
-            if (s <= p.ns) pdl_trigger();
             if (!ok) drain_stages(full, p.ns, max(0, s - p.ns), s - 1);
-        } else {
-            pdl_trigger();
         }
-        return;
+        return;   // the producer warp never triggers: the consumers do, after their wait
     }
 
     // ---------------- consumer warps ----------------
-    pdl_trigger();
-    pdl_wait();  // activations and residual come from the previous kernel
+    pdl_wait_trigger();  // activations and residual come from the previous kernel
 
     const int g = lane >> 2, t = lane & 3;
     const int jg = warp >> 1, eta = warp & 1;   // my half group inside every stage

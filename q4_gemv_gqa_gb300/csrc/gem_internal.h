@@ -9,10 +9,15 @@
 
 #include "../../include/gem.h"
 
-// Wall-time limit of every device-side wait on an asynchronous copy (1 s).
+// Default wall-time limit of every device-side wait on an asynchronous copy or a grid
+// barrier (1 s); gem_set_wait_limit() changes it at run time.
 #define GEM_WAIT_LIMIT_NS 1000000000ull
 
 namespace gem {
+
+// Called once per translation unit with kernels (static initialisation): the host handles of
+// that unit's wait-limit (unsigned long long) and test-injection (int) device words.
+void register_device_controls(const void* wait_limit_symbol, const void* inject_symbol);
 
 // Record a CUDA error for gem_last_cuda_error() and map it to a status.
 gem_status cuda_fail(cudaError_t e);
@@ -139,6 +144,7 @@ gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream);
 // Only for shapes that attn_fusable() accepts.
 bool attn_fusable(int n_q, int n_kv, int d);
 gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream);
+gem_status attn_enqueue_fused_standalone(const AttnOp& op, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -5,6 +5,7 @@
 #include <mutex>
 #include <set>
 #include <utility>
+#include <vector>
 
 #include "gem_internal.h"
 
@@ -21,6 +22,16 @@ std::mutex g_dev_mutex;
 bool g_dev_ready[kMaxDevices];
 gem::DeviceInfo g_dev[kMaxDevices];
 
+// Host handles of every translation unit's wait-limit and test-injection device words.
+struct ControlSymbols {
+    std::mutex mu;
+    std::vector<std::pair<const void*, const void*>> syms;
+};
+ControlSymbols& control_symbols() {
+    static ControlSymbols c;   // constructed on first use (static initialisation order)
+    return c;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 cudaError_t g_encode_err = cudaSuccess;
@@ -28,6 +39,12 @@ cudaError_t g_encode_err = cudaSuccess;
 }  // namespace
 
 namespace gem {
+
+void register_device_controls(const void* wait_limit_symbol, const void* inject_symbol) {
+    ControlSymbols& c = control_symbols();
+    std::lock_guard<std::mutex> lk(c.mu);
+    c.syms.emplace_back(wait_limit_symbol, inject_symbol);
+}
 
 gem_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -141,6 +158,30 @@ const char* gem_status_string(int status) {
 }
 
 int gem_last_cuda_error(void) { return g_last_cuda_error; }
+
+gem_status gem_status_from_flags(int32_t flags) {
+    if (flags & GEM_DEVFLAG_TIMEOUT) return GEM_ERR_TIMEOUT;
+    if (flags) return GEM_ERR_DEVICE_FLAG;
+    return GEM_OK;
+}
+
+gem_status gem_set_wait_limit(uint64_t ns) {
+    if (ns == 0) ns = GEM_WAIT_LIMIT_NS;
+    if (ns < 1000ull || ns > 60000000000ull) return GEM_ERR_INVALID_ARG;
+    const unsigned long long v = ns;
+    ControlSymbols& c = control_symbols();
+    std::lock_guard<std::mutex> lk(c.mu);
+    for (const auto& sym : c.syms) GEM_CUDA_TRY(cudaMemcpyToSymbol(sym.first, &v, sizeof(v)));
+    return GEM_OK;
+}
+
+gem_status gem_set_test_injection(int mask) {
+    if (mask & ~(GEM_INJECT_RING_SHORTFALL | GEM_INJECT_GRID_ARRIVAL)) return GEM_ERR_INVALID_ARG;
+    ControlSymbols& c = control_symbols();
+    std::lock_guard<std::mutex> lk(c.mu);
+    for (const auto& sym : c.syms) GEM_CUDA_TRY(cudaMemcpyToSymbol(sym.second, &mask, sizeof(mask)));
+    return GEM_OK;
+}
 
 int gem_version(void) { return 100; }
 

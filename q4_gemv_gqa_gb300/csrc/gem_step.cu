@@ -132,11 +132,12 @@ __device__ __forceinline__ void tma_load_box(void* dst, const CUtensorMap* tm, i
 __device__ bool ring_wait(uint64_t* bar, uint32_t par, Sync* sync, const volatile int* stop, int* status) {
     if (mbar_try_wait(bar, par)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = wait_limit_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, par)) return true;
         if (*stop || ld_volatile(&sync->abort)) return false;
-        if (globaltimer_ns() - t0 > GEM_WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit) {
             atomicOr(status, GEM_DEVFLAG_TIMEOUT);
             atomicExch(&sync->abort, 1);
             return false;
@@ -272,23 +273,27 @@ struct Ctx {
 // release-add on a monotonic arrival counter per CTA; a CTA leaves when the counter
 // reaches the end of its barrier's round (acquire loads), so no reset or second flag is
 // needed and the last arrival releases everyone with its own add.
-__device__ __forceinline__ bool grid_sync(Ctx& cx) {
+// Test hook (GEM_INJECT_GRID_ARRIVAL): CTA 0 leaves out its arrival at the first barrier of
+// the step, so every CTA's wait runs out; the step is aborted (the plan must be recreated).
+__device__ __forceinline__ bool grid_sync(Ctx& cx, bool first) {
     __shared__ int ok_sh;
     consumer_sync();
     if (threadIdx.x == 0) {
         Sync* sy = cx.P->sync;
         bool ok = cx.ok;
         const unsigned long long C = gridDim.x;
-        const unsigned long long old = atom_add_release64(&sy->arrived, 1ull);
+        const bool skip = first && blockIdx.x == 0 && (test_inject() & GEM_INJECT_GRID_ARRIVAL);
+        const unsigned long long old = skip ? ld_acquire64(&sy->arrived) : atom_add_release64(&sy->arrived, 1ull);
         const unsigned long long target = (old / C + 1) * C;
         if (ld_acquire64(&sy->arrived) < target) {
             const uint64_t t0 = globaltimer_ns();
+            const uint64_t limit = wait_limit_ns();
             while (ld_acquire64(&sy->arrived) < target) {
                 if (ld_volatile(&sy->abort)) {
                     ok = false;
                     break;
                 }
-                if (globaltimer_ns() - t0 > GEM_WAIT_LIMIT_NS) {
+                if (globaltimer_ns() - t0 > limit) {
                     atomicOr(cx.P->status, GEM_DEVFLAG_TIMEOUT);
                     atomicExch(&sy->abort, 1);
                     ok = false;
@@ -856,15 +861,15 @@ __device__ __forceinline__ void consumer(const Params& P, uint8_t* smem, uint64_
         if (l == 0 || L.rope_w != P.layers[l - 1].rope_w || L.rope_dim != P.layers[l - 1].rope_dim)
             rope_table(cx, L);   // read by attention after the barrier, which also orders it
         gemv_phase<1>(cx, L.qkv, P.x, H, L.g_attn, L.eps, P.qkv, L.n_qkv, nullptr, 0);
-        if (!grid_sync(cx)) break;
+        if (!grid_sync(cx, l == 0)) break;
         attn_phase<D>(cx, L);
-        if (!grid_sync(cx)) break;
+        if (!grid_sync(cx, false)) break;
         gemv_phase<1>(cx, L.o, P.attn, nqd, nullptr, 0.f, P.x, H, P.x, 0);
-        if (!grid_sync(cx)) break;
+        if (!grid_sync(cx, false)) break;
         gemv_phase<2>(cx, L.gu, P.x, H, L.g_ffn, L.eps, P.act, L.F, nullptr, L.act);
-        if (!grid_sync(cx)) break;
+        if (!grid_sync(cx, false)) break;
         gemv_phase<1>(cx, L.down, P.act, L.F, nullptr, 0.f, P.x, H, P.x, 0);
-        if (l + 1 < P.nlayers && !grid_sync(cx)) break;
+        if (l + 1 < P.nlayers && !grid_sync(cx, false)) break;
     }
     if (!cx.ok && threadIdx.x == 0) *stop = 1;   // the producer stops issuing and drains
 }

@@ -42,3 +42,18 @@ def f16_ulp_diff(a_bits, b_bits):
     a = np.where(a & 0x8000, -(a & 0x7FFF), a)
     b = np.where(b & 0x8000, -(b & 0x7FFF), b)
     return np.abs(a - b)
+
+
+def scale_q4_0(W, shift):
+    """The same Q4_0 matrix (raw 18-byte blocks) with every block scale multiplied by
+    2^-shift, exactly: the binary16 exponent field is lowered by `shift`, which every scale
+    must survive as a normal number.  Used to keep a stack of random-weight layers' residual
+    stream near one layer's output scale, so the absolute tolerance keeps its meaning."""
+    blocks = np.asarray(W).reshape(-1, 18).copy()
+    d = blocks[:, 0].astype(np.uint16) | (blocks[:, 1].astype(np.uint16) << 8)
+    e = (d >> 10) & 0x1F
+    assert np.all(e > shift) and np.all(e < 31), "a scale would leave the normal range"
+    d = d - np.uint16(shift << 10)
+    blocks[:, 0] = (d & 0xFF).astype(np.uint8)
+    blocks[:, 1] = (d >> 8).astype(np.uint8)
+    return blocks.reshape(np.asarray(W).shape)

@@ -87,3 +87,43 @@ def test_python_binding_imports_and_wraps(lib):
     with pytest.raises(gem.GemError) as e:
         gem._check(3, "x")
     assert "unsupported shape" in str(e.value)
+
+
+def test_status_from_flags_and_control_range_checks(lib):
+    """Host-only mappings and range checks of the failure-detection controls (no CUDA call)."""
+    f = lib.gem_status_from_flags
+    f.restype = C.c_int
+    f.argtypes = [C.c_int32]
+    assert f(0) == 0
+    assert f(1) == 5          # GEM_DEVFLAG_POS_RANGE -> GEM_ERR_DEVICE_FLAG
+    assert f(2) == 6          # GEM_DEVFLAG_TIMEOUT -> GEM_ERR_TIMEOUT
+    assert f(3) == 6          # timeout wins over other bits
+    w = lib.gem_set_wait_limit
+    w.restype = C.c_int
+    w.argtypes = [C.c_uint64]
+    assert w(999) == 1        # below 1 us
+    assert w(61_000_000_000) == 1
+    inj = lib.gem_set_test_injection
+    inj.restype = C.c_int
+    inj.argtypes = [C.c_int]
+    assert inj(4) == 1        # unknown bit
+
+
+def test_gemv_workspace_query_and_checks(lib):
+    q = lib.gem_q4_0_gemv_workspace
+    q.restype = C.c_size_t
+    q.argtypes = [C.c_int, C.c_int64]
+    assert q(1, 2048) == 0                 # one row: no records
+    n2 = q(2, 2048)
+    assert n2 > 0 and n2 % 256 == 0
+    assert q(8, 2048) == n2                # records hold 8 rows' operands whatever B
+    assert q(8, 4096) > n2
+    f = lib.gem_q4_0_gemv_ws
+    f.restype = C.c_int
+    f.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_int64,
+                  C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+    d = C.c_void_p(0x1000)
+    assert f(d, 64, 2048, d, 2048, 2, d, 64, None, None, 0, None) == 7             # no workspace
+    assert f(d, 64, 2048, d, 2048, 2, d, 64, None, d, n2 - 256, None) == 7         # too small
+    assert f(d, 64, 2048, d, 2048, 2, d, 64, None, C.c_void_p(0x1010), n2, None) == 2   # misaligned
+    assert f(d, 64, 33, d, 64, 2, d, 64, None, d, n2, None) == 3                  # K % 32 != 0

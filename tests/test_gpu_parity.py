@@ -435,6 +435,39 @@ def _layer_parity(shape, tens, x, pos, got, gk, gv, what):
     return nflip, ref
 
 
+def _oracle_follow_gpu(shape, tens, x, pos, k_cache, v_cache, gk, gv, what):
+    """One oracle layer step from x on caches (k_cache, v_cache: the state before the step;
+    updated in place with the GPU's appended rows), following the GPU's binary16 rounding
+    decisions of the new rows where they are ambiguous (gk, gv: the GPU's caches after the
+    step).  Returns the oracle's output (fp64)."""
+    xin = np.ascontiguousarray(x, dtype=np.float64)
+    kc, vc = k_cache.copy(), v_cache.copy()
+    ref, kvn = oracle.decode_layer(shape, tens, xin, pos, kc, vc, kvnew=True)
+    B, n_kv, d = len(pos), shape.n_kv, shape.d
+    flip = np.zeros((B, 2, n_kv, d), np.int8)
+    for b in range(B):
+        p = int(pos[b])
+        slot = p % shape.window if shape.window else p
+        for which, gbits, obits in ((0, gk, kc), (1, gv, vc)):
+            g, o = gbits[b, :, slot], obits[b, :, slot]
+            for j, i in np.argwhere(g != o):
+                v = kvn[b, which, j, i]
+                rms = float(np.sqrt(np.mean(kvn[b, which, j] ** 2)))
+                assert _code_in_band(int(g[j, i]), v, rms), \
+                    "%s: appended code outside the fp32 precision band of the value" % what
+                if g[j, i] == oracle.other_half_via_f32(v):
+                    flip[b, which, j, i] = 1
+        k_cache[b, :, slot] = gk[b, :, slot]
+        v_cache[b, :, slot] = gv[b, :, slot]
+    nflip = int(flip.sum())
+    assert nflip <= max(2, 0.01 * flip.size), "%s: %d rounding decisions differ" % (what, nflip)
+    if nflip:
+        kc, vc = k_cache.copy(), v_cache.copy()
+        # (the GPU's rows are already in place; the oracle rewrites them with the same codes)
+        ref = oracle.decode_layer(shape, tens, xin, pos, kc, vc, flip=flip)
+    return ref
+
+
 LAYER_CASES = [
     ("tiny", configs.TINY, 1, [128]),
     ("qwen3-1.7b", configs.QWEN3_1_7B, 1, [4096]),

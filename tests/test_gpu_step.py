@@ -2,8 +2,8 @@
 
 A one-layer step is compared with the fp64 oracle exactly as the per-layer chain is (same
 tolerances and binary16 rounding-band rule, tests/test_gpu_parity.py); a stack of layers is
-compared with the per-layer chain (gem_decode_layer, itself checked against the oracle)
-within the same tolerance, and with itself across repeated calls."""
+compared with the oracle run layer by layer at the same tolerances, and with itself across
+repeated calls."""
 from dataclasses import replace
 
 import numpy as np
@@ -11,8 +11,8 @@ import pytest
 
 import gem_synth
 from gem_synth import configs
-from parity import assert_close
-from test_gpu_parity import _bits, _cu, _half_cache, _layer_parity
+from parity import assert_close, scale_q4_0
+from test_gpu_parity import _bits, _cu, _half_cache, _layer_parity, _oracle_follow_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -64,46 +64,39 @@ def _stack(g, t, wl, seed):
     return layers, kcs, vcs
 
 
-def test_step_stack_matches_layer_chain(env):
+def test_step_stack_matches_oracle(env):
+    """Four layers in one persistent launch against the oracle run layer by layer (following
+    the GPU's binary16 rounding of each appended row where it is ambiguous), at the stated
+    tolerance.  The O and down projections' block scales are divided by 8 (exactly), which
+    keeps this stack's residual stream near the scale of one layer's output; with the
+    unscaled synthetic weights it grows to ~1e4 after four layers, where fp32 rounding of the
+    residual alone approaches the absolute bound."""
     g, t = env
     wl = configs.with_layers(configs.workload("qwen3-1.7b"), 4)
     wl = replace(wl, pos=1024, cache_cap=(1025,) * 4)
-    layers, kcs, vcs = _stack(g, t, wl, 5)
-    pos = _cu(t, np.full(wl.B, wl.pos, np.int32))
+    pos = np.full(wl.B, wl.pos, np.int32)
+    tens_l, layers = [], []
+    for li, (shape, cap) in enumerate(zip(wl.layers, wl.cache_cap)):
+        tn = configs.layer_tensors(shape, wl.B, cap, 5, li)
+        tn.w_o = scale_q4_0(tn.w_o, 3)
+        tn.w_down = scale_q4_0(tn.w_down, 3)
+        tens_l.append(tn)
+        layers.append(g.DeviceLayer(shape, tn))
     x0 = gem_synth.normal_f32(0, gem_synth.tid(0, gem_synth.ROLE_X), (wl.B, wl.layers[0].H))
-    # per-layer chain
-    xc = _cu(t, x0)
-    kc_c = [_half_cache(t, k) for k in kcs]
-    vc_c = [_half_cache(t, v) for v in vcs]
-    for dl, k, v, cap in zip(layers, kc_c, vc_c, wl.cache_cap):
-        ws = t.empty(g.decode_layer_workspace(dl, wl.B, cap), dtype=t.uint8, device="cuda")
-        g.decode_layer(dl, xc, k, v, pos, ws)
-    # one persistent launch
+    kc = [_half_cache(t, tn.k_cache) for tn in tens_l]
+    vc = [_half_cache(t, tn.v_cache) for tn in tens_l]
+    plan = g.StepPlan(layers, wl.B, kc, vc)
     xs = _cu(t, x0)
-    kc_s = [_half_cache(t, k) for k in kcs]
-    vc_s = [_half_cache(t, v) for v in vcs]
-    plan = g.StepPlan(layers, wl.B, kc_s, vc_s)
     status = t.zeros(1, dtype=t.int32, device="cuda")
-    plan.step(xs, pos, status=status)
+    plan.step(xs, _cu(t, pos), status=status)
     t.cuda.synchronize()
     assert int(status.item()) == 0
-    # Both sides are fp32 with different summation orders; after four random-weight layers
-    # the residual stream reaches ~1e4, where one fp32 unit is ~1e-3, so the absolute bound
-    # grows with the output scale (8 units at the largest magnitude).
-    ref = xc.cpu().numpy()
-    assert_close(xs.cpu().numpy(), ref, "step vs chain, 4 layers",
-                 max_abs=2e-3 + 8 * 2.0 ** -23 * float(np.abs(ref).max()))
-    slot = wl.pos
-    for li in range(4):
-        a, b = _bits(kc_s[li]), _bits(kc_c[li])
-        mask = np.ones(a.shape[2], bool)
-        mask[slot] = False
-        assert np.array_equal(a[:, :, mask], b[:, :, mask]), "layer %d: K rows other than the new one" % li
-        assert np.array_equal(_bits(vc_s[li])[:, :, mask], _bits(vc_c[li])[:, :, mask])
-        # the new rows: binary16 of (nearly) the same fp32 values; at most one unit apart
-        for new_a, new_b in ((a[:, :, slot], b[:, :, slot]), (_bits(vc_s[li])[:, :, slot], _bits(vc_c[li])[:, :, slot])):
-            d = np.abs(new_a.astype(np.int32) - new_b.astype(np.int32))
-            assert int(d.max()) <= 1 and int((d > 0).sum()) <= max(2, new_a.size // 100), "layer %d new row" % li
+    x = x0.astype(np.float64)
+    for li, (shape, tn) in enumerate(zip(wl.layers, tens_l)):
+        x = _oracle_follow_gpu(shape, tn, x, pos, tn.k_cache.copy(), tn.v_cache.copy(), _bits(kc[li]),
+                               _bits(vc[li]), "step layer %d" % li)
+    assert float(np.abs(x).max()) < 2048, "the scaled stack's residual stream is larger than intended"
+    assert_close(xs.cpu().numpy(), x, "persistent step, 4 layers, vs oracle")
     plan.close()
 
 

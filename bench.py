@@ -2,27 +2,36 @@
 
 One step = one new token through every layer of the workload (all steps of the hot path:
 norm, Q4_0 QKV, QK-norm, RoPE, KV append, split-K GQA attention, O + residual, norm,
-gate/up + gated activation, down + residual).  Default workload: the Qwen3-1.7B-shape
-decode step at batch 1 (28 layers, hidden 2048, 16/8 heads of 128, FFN 6144, 4096
-cached positions), whose 1.26 GB of weights and KV per step exceed the 129 MB L2, so
-nothing is flushed between steps.
+gate/up + gated activation, down + residual).  Default workload (the headline line): the
+Qwen3-1.7B-shape decode step at batch 1 (28 layers, hidden 2048, 16/8 heads of 128, FFN
+6144, 4096 cached positions), whose 1.27 GB of weights and KV per step exceed the 129 MB
+L2, so nothing is flushed between steps.  The same run adds sub-records for the other
+workloads: the Qwen3-4B-shape step at B = 8 (36 layers, 2048 cached positions per
+sequence), one Gemma-4-31B-shape group (5 sliding-window layers + 1 full-attention layer,
+32768 cached positions), the tiny layer, and the 31B FFN-shape GEMV at B = 1 and 8.
 
 Prints one JSON line.  `value` is achieved HBM GB/s over the step's algorithmic bytes
-(Q4_0 weights + KV cache read + activations), with inputs resident; `e2e` is the same
-metric through the C ABI with the step's input copied from pinned host memory and the
-output read back inside the timed region.  --impl reference times the fp64 oracle on the
-host cores on a bounded sample of the same workload.
+(Q4_0 weights + KV cache read + appended rows + activations), with inputs resident; `e2e`
+is the same metric through the C ABI with the step's input copied from pinned host memory
+and the output read back inside the timed region.  --impl reference times the fp64 oracle
+on the host cores on a bounded sample of the same workload.
+
+Synthetic inputs: seeded Q4_0 weights (codes uniform 0..15, binary16 scales uniform
+[0.002, 0.02]), N(0,1) binary16 KV caches, N(0,1) fp32 activations, norm weights
+1 + N(0, 0.1).  Every layer has its own weight and cache buffers; the timing-only stacks
+fill them from a few distinct seeded draws per layer shape (`distinct` in each record),
+since generating every layer's draws on the host would dominate the run.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -38,14 +47,16 @@ METRIC = "Q4_0 decode GEMV+attn HBM GB/s (% of ~8 TB/s); decode layer-step tok/s
 UNIT = "GB/s"
 
 
-# ---- helpers ------------------------------------------------------------------------------
+# ---- algorithmic bytes ------------------------------------------------------------------------
+
+def q4_bytes(n, k):
+    return n * (k // 32) * 18
+
 
 def layer_bytes(shape, B: int, T: int) -> dict:
     """Algorithmic bytes of one layer step: every byte the method must move once."""
-    def q4(n, k):
-        return n * (k // 32) * 18
-    w = (q4(shape.n_qkv, shape.H) + q4(shape.H, shape.n_q * shape.d) + 2 * q4(shape.F, shape.H)
-         + q4(shape.H, shape.F))
+    w = (q4_bytes(shape.n_qkv, shape.H) + q4_bytes(shape.H, shape.n_q * shape.d) + 2 * q4_bytes(shape.F, shape.H)
+         + q4_bytes(shape.H, shape.F))
     kv = B * shape.n_kv * T * shape.d * 2 * 2
     kv_write = B * shape.n_kv * shape.d * 2 * 2
     act = 4 * B * (2 * shape.H + shape.n_qkv * 2 + 2 * shape.n_q * shape.d + 3 * shape.F + 4 * shape.H)
@@ -56,8 +67,17 @@ def attn_bytes(shape, B, T):
     return B * shape.n_kv * T * shape.d * 2 * 2 + 4 * B * 2 * shape.n_q * shape.d
 
 
-def gemv_bytes(N, K, B):
-    return N * (K // 32) * 18 + 4 * B * (K + N)
+def gemv_bytes(N, K, B, nmat=1):
+    return nmat * q4_bytes(N, K) + 4 * B * (K + N)
+
+
+def attended(shape, pos):
+    T = pos + 1
+    return min(T, shape.window) if shape.window else T
+
+
+def step_bytes(wl):
+    return sum(layer_bytes(s, wl.B, attended(s, wl.pos))["total"] for s in wl.layers)
 
 
 def measured_peaks():
@@ -83,67 +103,88 @@ def device_record(torch, index: int) -> dict:
     return rec
 
 
-class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# ---- clocks during the timed region -----------------------------------------------------------
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []   # (wall time, csv line)
-        self.t0 = self.t1 = None
+class Clocks:
+    """SM clock, its maximum and the clock-event (throttle) reasons, read through NVML
+    (libnvidia-ml, part of the driver) as often as every millisecond while a timed region
+    runs, so even a short region carries samples.  Read-only: no setting is changed.  Falls
+    back to one nvidia-smi query at each end of the region when NVML cannot be opened."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __enter__(self):
+    def __init__(self, index: int, pci_bus_id: str | None = None):
+        self.nvml = None
+        self.handle = ctypes.c_void_p()
+        self.samples = []   # (sm_mhz, max_mhz, reasons mask)
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-            deadline = time.time() + 2.0   # the sampler is running before the timed region starts
-            while not self.lines and time.time() < deadline:
-                time.sleep(0.01)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() == 0:
+                ok = pci_bus_id is not None and lib.nvmlDeviceGetHandleByPciBusId_v2(
+                    pci_bus_id.encode(), ctypes.byref(self.handle)) == 0
+                if not ok:
+                    ok = lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) == 0
+                if ok:
+                    self.nvml = lib
+                    self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                        getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
         except Exception:
-            self.proc = None
-        self.t0 = time.time()
-        return self
+            self.nvml = None
+        self.index = index
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+    def sample(self):
+        if self.nvml is not None:
+            sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            if (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(sm)) == 0 and
+                    self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0 and
+                    self.reasons_fn(self.handle, ctypes.byref(rs)) == 0):
+                self.samples.append((float(sm.value), float(mx.value), int(rs.value)))
+            return
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                                  "clocks_event_reasons.active", "--format=csv,noheader,nounits"],
+                                 capture_output=True, text=True, timeout=20).stdout.strip().split(",")
+            self.samples.append((float(out[0]), float(out[1]), int(out[2].strip(), 16)))
+        except Exception:
+            pass
 
-    def __exit__(self, *a):
-        self.t1 = time.time()
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+    def run_timed(self, torch, enqueue, steps, stream):
+        """Record an event, enqueue `steps` units of work, record an event, and sample the clocks
+        until the second event has completed.  Returns the elapsed milliseconds."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        every = max(1, steps // 50)
+        e0.record(stream)
+        for i in range(steps):
+            enqueue()
+            if i % every == 0:
+                self.sample()
+        e1.record(stream)
+        while not e1.query():
+            self.sample()
+            time.sleep(0.001)
+        self.sample()   # the region's end
+        return e0.elapsed_time(e1)
 
     def summary(self):
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        inside = [ln for t, ln in self.lines if self.t0 is not None and self.t0 <= t <= (self.t1 or t) + 0.15]
-        for ln in inside:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = max(mx, float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for _, _, m in self.samples:
+            for bit, name in self.REASONS.items():
+                if m & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "nvml" if self.nvml is not None else "nvidia-smi"}
+
+
+def pci_bus_id(torch, index: int):
+    """The device's PCI bus id in NVML's form, when torch reports it."""
+    pr = torch.cuda.get_device_properties(index)
+    try:
+        return "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except AttributeError:
+        return None
 
 
 def traffic_record(kernel_key: str):
@@ -175,23 +216,40 @@ def whole_job_gbs(step_bytes: int, world: int, ms: float) -> float:
 # ---- device setup -----------------------------------------------------------------------------
 
 class Model:
-    def __init__(self, gem, torch, wl, seed=0):
+    """Every layer of a workload on the device, with its own weight, cache and workspace
+    buffers.  The first `distinct` layers of each shape get their own seeded draws; later
+    layers of that shape are device copies of them (distinct buffers, same values)."""
+
+    def __init__(self, gem, torch, wl, seed=0, distinct=None):
         self.gem, self.t, self.wl = gem, torch, wl
         self.B = wl.B
         self.layers, self.kc, self.vc, self.ws = [], [], [], []
+        seen = {}   # (shape, cap) -> list of (DeviceLayer, k, v)
         for li, (shape, cap) in enumerate(zip(wl.layers, wl.cache_cap)):
-            tens = configs.layer_tensors(shape, wl.B, cap, seed, li)
-            dl = gem.DeviceLayer(shape, tens)
+            key = (shape, cap)
+            made = seen.setdefault(key, [])
+            if distinct is None or len(made) < distinct:
+                tens = configs.layer_weights(shape, seed, li)
+                dl = gem.DeviceLayer(shape, tens)
+                k, v = configs.kv_cache(shape, wl.B, cap, seed, li)
+                kc = torch.from_numpy(k.view(np.int16)).cuda()
+                vc = torch.from_numpy(v.view(np.int16)).cuda()
+                made.append((dl, kc, vc))
+                del tens, k, v
+            else:
+                src, ks, vs = made[li % len(made)]
+                dl = gem.DeviceLayer.clone(src)
+                kc, vc = ks.clone(), vs.clone()
             self.layers.append(dl)
-            self.kc.append(torch.from_numpy(tens.k_cache.view(np.int16)).cuda())
-            self.vc.append(torch.from_numpy(tens.v_cache.view(np.int16)).cuda())
+            self.kc.append(kc)
+            self.vc.append(vc)
             self.ws.append(torch.empty(max(1, gem.decode_layer_workspace(dl, wl.B, cap)),
                                        dtype=torch.uint8, device="cuda"))
-            del tens
         H = wl.layers[0].H
         self.x0 = configs.layer_input(H, wl.B, seed)
         self.x = torch.from_numpy(self.x0.copy()).cuda()
         self.pos = torch.full((wl.B,), wl.pos, dtype=torch.int32, device="cuda")
+        self.distinct = distinct
 
     def step(self):
         for dl, k, v, w in zip(self.layers, self.kc, self.vc, self.ws):
@@ -202,6 +260,8 @@ class Model:
         for s, cap in zip(self.wl.layers, self.wl.cache_cap):
             fused = s.d <= 256 and s.n_q // s.n_kv <= 4   # QK-norm/RoPE/append inside attention
             n += (5 if fused else 6) + (2 if s.post_norms else 0)
+            if self.B >= 2:
+                n += 4   # one activation prep launch per GEMV
             if self.gem.gqa_decode_attn_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.window) > 0:
                 n += 1
         return n
@@ -235,12 +295,74 @@ def time_graph(torch, g, reps, warmup=3):
     return e0.elapsed_time(e1) / reps
 
 
+# ---- the layer's ops, each as the chain launches it -------------------------------------------
+
+def op_callers(gem, torch, model, idx):
+    """One closure per op of the layer step over the layers `idx`, each calling the same fused
+    kernel (same plan) the layer chain runs for it: QKV (pre-norm fused), attention (QK-norm,
+    RoPE and the KV append fused where the shape allows), O (+ residual), gate/up (pre-norm,
+    pair, gated activation), down (+ residual).  Returns {name: (fn, bytes per launch)}."""
+    wl = model.wl
+    s, cap, B = wl.layers[idx[0]], wl.cache_cap[idx[0]], wl.B
+    nqd = s.n_q * s.d
+    x = torch.randn((B, s.H), device="cuda")
+    qkv = torch.randn((B, s.n_qkv), device="cuda")
+    att = torch.randn((B, nqd), device="cuda")
+    act = torch.randn((B, s.F), device="cuda")
+    y = torch.empty((B, max(s.H, s.F, s.n_qkv)), device="cuda")
+    aws_n = gem.gqa_decode_attn_workspace(B, s.n_q, s.n_kv, s.d, cap, s.window)
+    aws = torch.empty(max(1, aws_n), dtype=torch.uint8, device="cuda")
+    gws = torch.empty(max(1, gem.q4_0_gemv_workspace(B, max(s.H, s.F, nqd))), dtype=torch.uint8, device="cuda")
+    L = [model.layers[i] for i in idx]
+    T = attended(s, wl.pos)
+    gq = None if not s.qk_norm else [dl.g_q for dl in L]
+    gk = None if not s.qk_norm else [dl.g_k for dl in L]
+
+    def qkv_fn():
+        for dl in L:
+            gem.q4_0_gemv_fused(dl.w_qkv, None, s.n_qkv, s.H, x, qkv, gamma=dl.g_attn, eps=s.eps, workspace=gws)
+
+    def attn_fn():
+        for j, i in enumerate(idx):
+            gem.gqa_decode_attn_fused(qkv, s.n_q, s.n_kv, s.d, gq[j] if gq else None, gk[j] if gk else None,
+                                      1 if s.v_from_k else 0, s.eps, model.pos, s.theta, s.rope_dim,
+                                      model.kc[i], model.vc[i], s.window, float(s.scale), att,
+                                      aws if aws_n else None)
+
+    def o_fn():
+        for dl in L:
+            gem.q4_0_gemv_fused(dl.w_o, None, s.H, nqd, att, y, residual=x, workspace=gws)
+
+    def gate_up_fn():
+        for dl in L:
+            gem.q4_0_gemv_fused(dl.w_gate, dl.w_up, s.F, s.H, x, act, gamma=dl.g_ffn, eps=s.eps, act=s.act,
+                                workspace=gws)
+
+    def down_fn():
+        for dl in L:
+            gem.q4_0_gemv_fused(dl.w_down, None, s.H, s.F, act, y, residual=x, workspace=gws)
+
+    return {
+        "q4_0_gemv_qkv": (qkv_fn, gemv_bytes(s.n_qkv, s.H, B)),
+        "gqa_decode_attn": (attn_fn, attn_bytes(s, B, T) + B * s.n_kv * s.d * 4),
+        "q4_0_gemv_o": (o_fn, gemv_bytes(s.H, nqd, B) + 4 * B * s.H),
+        "q4_0_gemv_gate_up": (gate_up_fn, gemv_bytes(s.F, s.H, B, nmat=2)),
+        "q4_0_gemv_down": (down_fn, gemv_bytes(s.H, s.F, B) + 4 * B * s.H),
+    }
+
+
+def same_shape_layers(wl):
+    s0, c0 = wl.layers[0], wl.cache_cap[0]
+    return [i for i in range(len(wl.layers)) if wl.layers[i] == s0 and wl.cache_cap[i] == c0]
+
+
 # ---- arms -------------------------------------------------------------------------------------
 
 def run_kernel_only(args):
-    """A single op on its own (for ncu captures): `gemv` = a 31B FFN projection over --mats
+    """A single op on its own (for profiler captures): `gemv` = a 31B FFN projection over --mats
     rotated matrices at --batch (--gemv-shape up: K=5376 -> N=21504; down: K=21504 -> N=5376);
-    `attn` = GQA decode attention over the workload's first --layers caches."""
+    `op` = one op of the workload's layer step (--op), as the chain launches it, over the
+    workload's first --layers layers."""
     import torch
     import q4_gemv_gqa_gb300 as gem
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
@@ -253,32 +375,21 @@ def run_kernel_only(args):
                 for i in range(args.mats)]
         x = torch.from_numpy(gem_synth.normal_f32(0, 6000, (B, K))).cuda()
         y = torch.empty((B, N), device="cuda")
+        ws = torch.empty(max(1, gem.q4_0_gemv_workspace(B, K)), dtype=torch.uint8, device="cuda")
 
         def run():
             for W in mats:
-                gem.q4_0_gemv(W, N, K, x, y)
+                gem.q4_0_gemv(W, N, K, x, y, workspace=ws)
         b = gemv_bytes(N, K, B)
         n = len(mats)
     else:
-        wl = configs.workload(args.workload)
-        wl = configs.with_layers(wl, args.layers or 2)
-        s0, cap = wl.layers[0], wl.cache_cap[0]
-        kcs = [torch.from_numpy(gem_synth.normal_f16_bits(0, 100 + i, (wl.B, s0.n_kv, cap, s0.d)).view(np.int16)).cuda()
-               for i in range(len(wl.layers))]
-        vcs = [torch.from_numpy(gem_synth.normal_f16_bits(0, 200 + i, (wl.B, s0.n_kv, cap, s0.d)).view(np.int16)).cuda()
-               for i in range(len(wl.layers))]
-        q = torch.from_numpy(gem_synth.normal_f32(0, 7, (wl.B, s0.n_q * s0.d))).cuda()
-        out = torch.empty_like(q)
-        pos = torch.full((wl.B,), wl.pos, dtype=torch.int32, device="cuda")
-        ws = torch.empty(max(1, gem.gqa_decode_attn_workspace(wl.B, s0.n_q, s0.n_kv, s0.d, cap, s0.window)),
-                         dtype=torch.uint8, device="cuda")
-
-        def run():
-            for kc, vc in zip(kcs, vcs):
-                gem.gqa_decode_attn(q, kc, vc, s0.n_q, s0.n_kv, s0.d, pos, s0.window, float(s0.scale), out, ws)
-        T = min(wl.pos + 1, s0.window) if s0.window else wl.pos + 1
-        b = attn_bytes(s0, wl.B, T)
-        n = len(kcs)
+        wl = configs.with_layers(configs.workload(args.workload), args.layers or 2)
+        model = Model(gem, torch, wl, distinct=1)
+        idx = same_shape_layers(wl)
+        fn, b = op_callers(gem, torch, model, idx)[args.op]
+        res["op"], res["workload"] = args.op, wl.name
+        run = fn
+        n = len(idx)
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize()
@@ -294,6 +405,36 @@ def run_kernel_only(args):
     print(json.dumps(res), flush=True)
 
 
+def config_of(wl):
+    return {"workload": wl.name, "layers": len(wl.layers), "B": wl.B, "n_kv": wl.pos,
+            "hidden": wl.layers[0].H, "heads": [wl.layers[0].n_q, wl.layers[0].n_kv],
+            "head_dim": wl.layers[0].d, "ffn": wl.layers[0].F, "bytes_per_step": step_bytes(wl),
+            "l2": "inputs larger than L2 (%.2f GB streamed per step vs 129 MB L2)" % (step_bytes(wl) / 1e9),
+            "parallelism": "single GPU"}
+
+
+def workload_record(gem, torch, name, reps, peak, distinct):
+    """One step of another workload, captured as a CUDA graph and replayed: ms per step,
+    us per layer, tokens/s and GB/s over its algorithmic bytes."""
+    wl = configs.workload(name)
+    model = Model(gem, torch, wl, distinct=distinct)
+    g = capture(torch, model.step)
+    ms = time_graph(torch, g, reps, warmup=3)
+    flags = gem.device_status()
+    sb = step_bytes(wl)
+    gbs = sb / (ms * 1e-3) / 1e9
+    rec = {"layers": len(wl.layers), "B": wl.B, "n_kv": wl.pos, "ms_per_step": round(ms, 4),
+           "us_per_layer": round(ms * 1e3 / len(wl.layers), 3), "tok_s": round(wl.B / (ms * 1e-3), 1),
+           "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "bytes_per_step": sb,
+           "replays": reps, "distinct_draws_per_shape": distinct, "device_flags": flags}
+    if len(wl.layers) > 1:
+        nL = len(wl.layers)
+        rec["note"] = "%d-layer step" % nL
+    del g, model
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_gem(args):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -306,13 +447,13 @@ def run_gem(args):
         dist.init_process_group("nccl")
     import q4_gemv_gqa_gb300 as gem
 
+    peak, peak_kind = measured_peaks()
     wl = configs.workload(args.workload)
     if args.layers:
         wl = configs.with_layers(wl, args.layers)
-    T = wl.pos + 1
     model = Model(gem, torch, wl)
     nL = len(wl.layers)
-    step_bytes = sum(layer_bytes(s, wl.B, min(T, s.window) if s.window else T)["total"] for s in wl.layers)
+    sbytes = step_bytes(wl)
 
     g = capture(torch, model.step)
     for _ in range(args.warmup):
@@ -322,15 +463,9 @@ def run_gem(args):
         dist.barrier()
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        e0.record(st)
-        for _ in range(args.steps):
-            g.replay()
-        e1.record(st)
-        e1.synchronize()
+    clk = Clocks(local, pci_bus_id(torch, local))
+    ms = clk.run_timed(torch, g.replay, args.steps, st) / args.steps
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
     if dist:
         ms = max_over_ranks(dist, torch, ms, "cuda")
         dist.barrier()
@@ -361,45 +496,30 @@ def run_gem(args):
     e2e_ms = e2.elapsed_time(e3) / args.steps
     e2e_wall_ms = (time.perf_counter() - t0) * 1e3 / args.steps
 
-    # per-kernel roofline: each op of the layer timed alone over the data of every layer that
-    # has the first layer's shape and cache capacity (a mixed stack's other layers differ)
-    shape0, cap0 = wl.layers[0], wl.cache_cap[0]
-    same = [i for i in range(nL) if wl.layers[i] == shape0 and wl.cache_cap[i] == cap0]
-    nS = len(same)
+    # per-op roofline: each op of the layer, launched as the chain launches it (same fused
+    # kernel), timed alone over every layer shaped like the first (graph, CUDA events)
+    idx = same_shape_layers(wl)
     kern = {}
-    q = torch.randn((wl.B, shape0.n_q * shape0.d), device="cuda")
-    out = torch.empty_like(q)
-    aws = torch.empty(max(1, gem.gqa_decode_attn_workspace(wl.B, shape0.n_q, shape0.n_kv, shape0.d, cap0,
-                                                           shape0.window)), dtype=torch.uint8, device="cuda")
-
-    def attn_all():
-        for i in same:
-            k, v = model.kc[i], model.vc[i]
-            gem.gqa_decode_attn(q, k, v, shape0.n_q, shape0.n_kv, shape0.d, model.pos, shape0.window,
-                                float(shape0.scale), out, aws)
-    ga = capture(torch, attn_all)
-    ms_a = time_graph(torch, ga, max(5, args.steps)) / nS
-    Ta = min(T, shape0.window) if shape0.window else T
-    kern["gqa_decode_attn"] = {"us": ms_a * 1e3, "bytes": attn_bytes(shape0, wl.B, Ta)}
-
-    xin = torch.randn((wl.B, max(shape0.H, shape0.F, shape0.n_q * shape0.d)), device="cuda")
-    layers0 = [model.layers[i] for i in same]
-    gate_up = [torch.cat([dl.w_gate, dl.w_up]) for dl in layers0]
-    yb = torch.empty((wl.B, 2 * shape0.F), device="cuda")
-    for name, mats, N, K in [("q4_0_gemv_gate_up", gate_up, 2 * shape0.F, shape0.H),
-                             ("q4_0_gemv_qkv", [dl.w_qkv for dl in layers0], shape0.n_qkv, shape0.H),
-                             ("q4_0_gemv_down", [dl.w_down for dl in layers0], shape0.H, shape0.F),
-                             ("q4_0_gemv_o", [dl.w_o for dl in layers0], shape0.H, shape0.n_q * shape0.d)]:
-        xk = xin[:, :K].contiguous()
-        yk = torch.empty((wl.B, N), device="cuda")
-
-        def gemv_all(mats=mats, N=N, K=K, xk=xk, yk=yk):
-            for W in mats:
-                gem.q4_0_gemv(W, N, K, xk, yk)
-        gg = capture(torch, gemv_all)
-        ms_g = time_graph(torch, gg, max(5, args.steps)) / nS
-        kern[name] = {"us": ms_g * 1e3, "bytes": gemv_bytes(N, K, wl.B)}
-    del gate_up, yb
+    for name, (fn, b) in op_callers(gem, torch, model, idx).items():
+        gg = capture(torch, fn)
+        us = time_graph(torch, gg, max(5, min(args.steps, 200))) / len(idx) * 1e3
+        kern[name] = {"us": us, "bytes": b, "gbs": b / us / 1e3, "frac": b / us / 1e3 / peak}
+        del gg
+    dom = max(kern, key=lambda k: kern[k]["us"])
+    dk = kern[dom]
+    persistent = None
+    try:
+        plan = gem.StepPlan(model.layers, wl.B, model.kc, model.vc)
+        gp = capture(torch, lambda: plan.step(model.x, model.pos))
+        ms_p = time_graph(torch, gp, max(5, min(args.steps, 200)))
+        persistent = {"ms_per_step": round(ms_p, 4), "us_per_layer": round(ms_p * 1e3 / nL, 3)}
+        del gp
+        plan.close()
+    except gem.GemError as e:
+        persistent = {"unsupported": str(e)}
+    launches = model.launches_per_step()
+    del g, model
+    torch.cuda.empty_cache()
 
     # the 31B FFN projection (5376 -> 21504), 8 distinct matrices (520 MB) rotated
     gemv31 = {}
@@ -407,44 +527,31 @@ def run_gem(args):
     for B in (1, 8):
         x31 = torch.from_numpy(gem_synth.normal_f32(0, 6000, (B, 5376))).cuda()
         y31 = torch.empty((B, 21504), device="cuda")
+        ws31 = torch.empty(max(1, gem.q4_0_gemv_workspace(B, 5376)), dtype=torch.uint8, device="cuda")
 
-        def g31(x31=x31, y31=y31):
+        def g31(x31=x31, y31=y31, ws31=ws31):
             for W in W31:
-                gem.q4_0_gemv(W, 21504, 5376, x31, y31)
+                gem.q4_0_gemv(W, 21504, 5376, x31, y31, workspace=ws31)
         gg = capture(torch, g31)
-        us = time_graph(torch, gg, max(5, args.steps)) / len(W31) * 1e3
+        us = time_graph(torch, gg, max(5, min(args.steps, 200))) / len(W31) * 1e3
         b = gemv_bytes(21504, 5376, B)
-        gemv31["b%d" % B] = {"us": us, "gbs": b / us / 1e3}
+        gemv31["b%d" % B] = {"us": round(us, 3), "gbs": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)}
+        del gg
     del W31
+    torch.cuda.empty_cache()
 
-    # the same step as one persistent launch (gem_decode_step), where the layers allow it
-    persistent = None
-    try:
-        plan = gem.StepPlan(model.layers, wl.B, model.kc, model.vc)
-        gp = capture(torch, lambda: plan.step(model.x, model.pos))
-        ms_p = time_graph(torch, gp, max(5, args.steps))
-        persistent = {"ms_per_step": round(ms_p, 4), "us_per_layer": round(ms_p * 1e3 / nL, 3)}
-        plan.close()
-    except gem.GemError as e:
-        persistent = {"unsupported": str(e)}
-
-    peak, peak_kind = measured_peaks()
-    for k in kern.values():
-        k["gbs"] = k["bytes"] / k["us"] / 1e3
-        k["frac"] = k["gbs"] / peak
-    for v in gemv31.values():
-        v["frac"] = v["gbs"] / peak
-    # dominant kernel: largest time per step inside the layer chain
-    per_step_us = {"gqa_decode_attn": kern["gqa_decode_attn"]["us"],
-                   "q4_0_gemv_gate_up": kern["q4_0_gemv_gate_up"]["us"],
-                   "q4_0_gemv_qkv": kern["q4_0_gemv_qkv"]["us"],
-                   "q4_0_gemv_down": kern["q4_0_gemv_down"]["us"],
-                   "q4_0_gemv_o": kern["q4_0_gemv_o"]["us"]}
-    dom = max(per_step_us, key=per_step_us.get)
-    dk = kern[dom]
+    # the other workloads' steps
+    subs = {}
+    if not args.no_workloads and rank == 0:
+        reps = max(10, min(args.steps, 100))
+        for name, distinct in (("qwen3-4b-b8", 4), ("gemma4-31b-group", 2), ("tiny", 1)):
+            if name == wl.name:
+                continue
+            subs[name] = workload_record(gem, torch, name, reps, peak, distinct)
+        subs["tiny"]["note"] = "one 0.4 MB layer: launch-latency bound, reported in us (no roofline)"
 
     tokens = wl.B * world
-    value = whole_job_gbs(step_bytes, world, ms)
+    value = whole_job_gbs(sbytes, world, ms)
     if rank == 0:
         cpu = cpu_baseline(wl, args) if world == 1 else None
         line = {
@@ -452,12 +559,7 @@ def run_gem(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded Q4_0 weights, N(0,1) fp16 KV cache and fp32 activations)",
-            "config": {"workload": wl.name, "layers": nL, "B": wl.B, "n_kv": wl.pos,
-                       "hidden": wl.layers[0].H, "heads": [wl.layers[0].n_q, wl.layers[0].n_kv],
-                       "head_dim": wl.layers[0].d, "ffn": wl.layers[0].F,
-                       "bytes_per_step": step_bytes,
-                       "l2": "inputs larger than L2 (%.2f GB streamed per step vs 129 MB L2)" % (step_bytes / 1e9),
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": config_of(wl),
             "tok_s": round(tokens / (ms * 1e-3), 1),
             "us_per_layer": round(ms * 1e3 / nL, 3),
             "frac_of_peak": round(value / world / peak, 4),
@@ -467,15 +569,16 @@ def run_gem(args):
                          "us_per_launch": round(dk["us"], 3)},
             "kernels": {k: {"us": round(v["us"], 3), "gbs": round(v["gbs"], 1), "frac": round(v["frac"], 4)}
                         for k, v in kern.items()},
-            "kernels_layers": "the %d of %d layers shaped like the first" % (nS, nL),
+            "kernels_how": "each op as the layer chain launches it (same fused kernel), alone over the %d "
+                           "layers shaped like the first, CUDA graph, CUDA events" % len(idx),
             "persistent_step_kernel": persistent,
-            "gemv_k5376_n21504": {k: {"us": round(v["us"], 3), "gbs": round(v["gbs"], 1),
-                                      "frac": round(v["frac"], 4)} for k, v in gemv31.items()},
-            "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "gemv_k5376_n21504": gemv31,
+            "workloads": subs,
+            "e2e": {"value": round(sbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 4), "wall_ms_per_step": round(e2e_wall_ms, 4),
                     "h2d_bytes_per_step": int(hx.numel() * 4 + hpos.numel() * 4),
                     "d2h_bytes_per_step": int(hout.numel() * 4)},
-            "gpu_launches": model.launches_per_step() * args.steps,
+            "gpu_launches": launches * args.steps,
             "clocks": clk.summary(),
             "device": device_record(torch, local),
             "device_flags": flags,
@@ -494,7 +597,6 @@ def _oracle_sample(wl, budget_s, max_cached=4):
     """Oracle layer steps on the workload's layers, in order and cycling over the first
     `max_cached` of them (tensors built once), until ~budget_s of CPU work (at least one step)."""
     import oracle
-    T = wl.pos + 1
     pos = np.full(wl.B, wl.pos, np.int32)
     done, bytes_done, t_spent = 0, 0, 0.0
     x = configs.layer_input(wl.layers[0].H, wl.B, 0).astype(np.float64)
@@ -509,17 +611,29 @@ def _oracle_sample(wl, budget_s, max_cached=4):
         x = oracle.decode_layer(wl.layers[li], tens, x, pos, tens.k_cache, tens.v_cache)
         t_spent += time.perf_counter() - t0
         s = wl.layers[li]
-        bytes_done += layer_bytes(s, wl.B, min(T, s.window) if s.window else T)["total"]
+        bytes_done += layer_bytes(s, wl.B, attended(s, wl.pos))["total"]
         done += 1
     return done, bytes_done, t_spent, oracle.num_threads()
 
 
 def cpu_baseline(wl, args):
-    done, b, t, cores = _oracle_sample(wl, args.cpu_budget)
+    """The oracle as it stands on the host cores: OpenMP over output rows / heads on every
+    core, then single-threaded (the same arithmetic; per-row sums are sequential either way)."""
+    import oracle
+    done, b, t, cores = _oracle_sample(wl, args.cpu_budget * 2 / 3)
+    nthreads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        d1, b1, t1, _ = _oracle_sample(wl, args.cpu_budget / 3)
+    finally:
+        oracle.set_num_threads(nthreads)
     return {"value": round(b / t / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "%d layer steps of %s (its first %d layers in turn; fp64 scalar C, OpenMP over "
                       "rows/heads), %.1f s" % (done, wl.name, min(4, len(wl.layers)), t),
-            "ms_per_layer": round(t * 1e3 / done, 1)}
+            "ms_per_layer": round(t * 1e3 / done, 1),
+            "single_thread": {"value": round(b1 / t1 / 1e9, 3), "unit": UNIT, "cores": 1,
+                              "ms_per_layer": round(t1 * 1e3 / d1, 1),
+                              "sample": "%d layer steps, %.1f s" % (d1, t1)}}
 
 
 def run_reference(args):
@@ -544,7 +658,7 @@ def run_reference(args):
             "ms_per_step": round(tot_t * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded inputs as the GPU arm)",
-            "config": {"workload": wl.name, "layers": len(wl.layers), "B": wl.B, "n_kv": wl.pos},
+            "config": config_of(wl),
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "kind": "oracle", "cores": cores,
                              "sample": "%d layer steps of %s per %d steps" % (done, wl.name, args.steps)},
             "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -561,8 +675,12 @@ def main():
                     choices=["tiny", "qwen3-1.7b", "qwen3-4b-b8", "gemma4-31b-group"])
     ap.add_argument("--layers", type=int, default=0, help="use only the first n layers")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
-    ap.add_argument("--kernel", choices=["step", "gemv", "attn"], default="step",
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' sub-records")
+    ap.add_argument("--kernel", choices=["step", "gemv", "op"], default="step",
                     help="time one op alone (for profiler captures) instead of the step")
+    ap.add_argument("--op", default="gqa_decode_attn",
+                    choices=["q4_0_gemv_qkv", "gqa_decode_attn", "q4_0_gemv_o", "q4_0_gemv_gate_up",
+                             "q4_0_gemv_down"], help="--kernel op: which op of the layer step")
     ap.add_argument("--batch", type=int, default=1, help="--kernel gemv: activation rows")
     ap.add_argument("--mats", type=int, default=8, help="--kernel gemv: rotated matrices")
     ap.add_argument("--gemv-shape", choices=["up", "down"], default="up",

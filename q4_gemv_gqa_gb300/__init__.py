@@ -292,8 +292,25 @@ class DeviceLayer:
         self.g_k = up(tensors.g_k, torch.float32)
         self.g_post_attn = up(tensors.g_post_attn, torch.float32)
         self.g_post_ffn = up(tensors.g_post_ffn, torch.float32)
+        self._make_desc()
+
+    _TENSORS = ("w_qkv", "w_o", "w_gate", "w_up", "w_down", "g_attn", "g_ffn", "g_q", "g_k",
+                "g_post_attn", "g_post_ffn")
+
+    @classmethod
+    def clone(cls, src: "DeviceLayer") -> "DeviceLayer":
+        """A layer with its own device copies of src's weights (same values, new buffers)."""
+        obj = cls.__new__(cls)
+        obj.shape = src.shape
+        for name in cls._TENSORS:
+            t = getattr(src, name)
+            setattr(obj, name, None if t is None else t.clone())
+        obj._make_desc()
+        return obj
+
+    def _make_desc(self):
         ptr = lambda t: None if t is None else t.data_ptr()
-        s = shape
+        s = self.shape
         self.desc = LayerDesc(
             H=s.H, n_q=s.n_q, n_kv=s.n_kv, d=s.d, F=s.F, eps=s.eps, theta=s.theta,
             scale=float(s.scale), rope_dim=s.rope_dim, window=s.window, act=s.act,

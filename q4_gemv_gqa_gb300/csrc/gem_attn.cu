@@ -28,6 +28,7 @@
 #include <cmath>
 #include <map>
 #include <mutex>
+#include <tuple>
 
 #include "gem_device.cuh"
 
@@ -63,53 +64,10 @@ struct AttnParams {
     float eps;
     int rope_dim, v_mode;
     uint16_t *k_out, *v_out;
-    // flash kernel: the grid's splits of one (sequence, KV head) form a thread-block cluster and
-    // merge their states through distributed shared memory (no partials, no merge launch)
-    int cluster;
+    // flash kernel: one arrival counter per (sequence, KV head) in the workspace, zero between
+    // calls (the CTA that merges resets it)
+    unsigned* cnt;
 };
-
-constexpr int kMaxClusterSplits = 16;   // largest cluster the flash splits of one KV head form
-
-// Every thread of every CTA of the cluster arrives, then waits (release / acquire).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// The same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
-// Cluster merge of the splits of one (sequence, KV head): CTA `rank` combines output elements
-// [rank * chunk, ...) of the G heads, over splits 0 .. nsplit - 1 in ascending order:
-// M = max_s m_s,  out = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.  exp = this CTA's export
-// area [G][D + 2] (o[0..D), m, l), filled before the call by CTAs with split < nsplit.
-// Every CTA of the cluster calls it exactly once (it holds two cluster barriers).
-__device__ void cluster_merge(const float* exp, int G, int D, int nsplit, uint32_t rank, uint32_t csize,
-                              float* out) {
-    cluster_sync_all();   // every split's export written
-    const int n = nsplit > 1 ? G * D : 0;   // one split: its CTA wrote the output itself
-    const int chunk = (n + static_cast<int>(csize) - 1) / static_cast<int>(csize);
-    const int lo = static_cast<int>(rank) * chunk, hi = min(n, lo + chunk);
-    for (int e = lo + static_cast<int>(threadIdx.x); e < hi; e += static_cast<int>(blockDim.x)) {
-        const int h = e / D, i = e - h * D;
-        const float* eh = exp + h * (D + 2);
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, ld_cluster_f32(eh + D, static_cast<uint32_t>(sp)));
-        float L = 0.f, O = 0.f;
-        for (int sp = 0; sp < nsplit; ++sp) {
-            const float f = expf(ld_cluster_f32(eh + D, static_cast<uint32_t>(sp)) - M);
-            L = fmaf(f, ld_cluster_f32(eh + D + 1, static_cast<uint32_t>(sp)), L);
-            O = fmaf(f, ld_cluster_f32(eh + i, static_cast<uint32_t>(sp)), O);
-        }
-        out[static_cast<int64_t>(h) * D + i] = O / L;
-    }
-    cluster_sync_all();   // peers are done reading this CTA's export
-}
 
 __host__ __device__ __forceinline__ int tile_slots(int d) { return d <= 64 ? 128 : (d <= 128 ? 64 : 32); }
 
@@ -385,40 +343,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid
 }
 
 // ---- per-warp flash variant (d <= 256, G <= 4) -------------------------------------------
-// Each warp of the CTA owns every fourth 16-slot tile of the split and streams its K and V
-// tiles through a private 2-stage TMA ring.  Per tile: S^T = K Q^T on mma (positions are the
-// M rows; the N columns are (head, hi/lo) pairs of the pre-scaled query), an online softmax
-// per head held in registers (head t lives in lane quad position t), P^T through a 384-byte
-// per-warp buffer, and O^T += V^T P^T on mma (head t's hi and lo columns land in the same
-// thread and are summed at the end).  The four warps' states are merged once per CTA.
+// Each of the CTA's W warps owns every W-th 16-slot tile of the split and streams its K and V
+// tiles through a private 2-stage TMA ring.  The grid holds about as many CTAs as the SMs can
+// keep resident at once, so a split is a few tiles per warp and most of them are in flight
+// before the first is consumed (inside the layer chain they are requested before
+// griddepcontrol.wait).  Per tile: S^T = K Q^T on mma (positions are the M rows; the N
+// columns are (head, hi/lo) pairs of the pre-scaled query), an online softmax per head held
+// in registers (head t lives in lane quad position t), P^T through a 384-byte per-warp
+// buffer, and O^T += V^T P^T on mma (head t's hi and lo columns land in the same thread and
+// are summed at the end).  The W warps' states are merged once per CTA (ascending warp
+// order).  A split then writes its (max, denominator, unnormalised output) to the workspace
+// and takes a ticket from its (sequence, KV head) arrival counter; the CTA that takes the
+// last ticket combines every split in ascending split order (so the result does not depend
+// on which CTA arrives last), writes the output and sets the counter back to zero.
 constexpr int kFlashTile = 16;
-constexpr int kFlashWarps = 4;
 constexpr int kFlashStages = 2;
+constexpr int kPbufPitch = 24;        // halves per P^T row (16 used; padding avoids bank conflicts)
+constexpr int kMaxFlashSplits = 64;   // splits of one (sequence, KV head) at most
 
-struct FlashSmem {
-    static constexpr int kPbufPitch = 24;  // halves per P^T row (16 used; padding avoids bank conflicts)
-};
-
-template <int D>
-__global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                                        const __grid_constant__ CUtensorMap tmV,
-                                                                        const AttnParams P,
-                                                                        const __grid_constant__ RopeFreq fr) {
+template <int D, int W>
+__global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV,
+                                                               const AttnParams P,
+                                                               const __grid_constant__ RopeFreq fr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr int kNT = W * 32;
     constexpr int kTileBytes = kFlashTile * D * 2;            // one K or V tile
     constexpr int kStageBytes = 2 * kTileBytes;               // K + V
     constexpr int kWarpRing = kFlashStages * kStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFlashWarps * kWarpRing);       // [warp][stage]
-    __half* pbuf = reinterpret_cast<__half*>(smem + kFlashWarps * kWarpRing + 128);    // [warp][8][24]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + W * kWarpRing);                   // [warp][stage]
+    __half* pbuf = reinterpret_cast<__half*>(smem + W * kWarpRing + 128);                 // [warp][8][24]
     float* comb = reinterpret_cast<float*>(smem);             // reuses the ring after the tile loop
     // fused path: rotated query heads [4][D], cos / sin of the rotated pairs, new K / V rows
-    float* qs = reinterpret_cast<float*>(smem + kFlashWarps * kWarpRing + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2);
+    float* qs = reinterpret_cast<float*>(smem + W * kWarpRing + 128 + W * 8 * kPbufPitch * 2);
     float* kbuf = qs + 4 * D;
     float* cs = kbuf + D;
     float* sn = cs + D / 2;
     uint16_t* knew = reinterpret_cast<uint16_t*>(sn + D / 2);
     uint16_t* vnew = knew + D;
+    __shared__ int last_sh;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int t_id = threadIdx.x, lane = t_id & 31, warp = t_id >> 5;
@@ -436,17 +400,12 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     const int T = P.window ? min(P.window, p + 1) : p + 1;
     int nsplit, t0, t1;
     split_range(T, kFlashTile, P.nsplit_max, split, nsplit, t0, t1);
-    // cluster merge: export area after the combine buffers (inside the idle rings)
-    float* cexp = reinterpret_cast<float*>(smem) + 2 * kFlashWarps * 4 + kFlashWarps * 4 * D;
     if (split >= nsplit) {   // no tiles in this split (short prefix)
         if (P.early) pdl_wait_trigger();
-        if (P.cluster)
-            cluster_merge(cexp, G, D, nsplit, static_cast<uint32_t>(split), gridDim.x,
-                          P.out + b * P.ldo + static_cast<int64_t>(g * G) * D);
         return;
     }
     const int ntile = t1 - t0;
-    const int nmy = ntile > warp ? (ntile - warp + kFlashWarps - 1) / kFlashWarps : 0;  // my tiles
+    const int nmy = ntile > warp ? (ntile - warp + W - 1) / W : 0;  // my tiles
     const int slot_p = P.window ? p % P.window : p;
     const int64_t row0 = (static_cast<int64_t>(b) * P.n_kv + g) * P.cap;
     uint8_t* ring = smem + warp * kWarpRing;
@@ -458,7 +417,7 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     __syncwarp();
     const uint64_t policy = l2_policy_evict_first();
     auto issue = [&](int it) {  // my it-th tile into stage it % kFlashStages (lane 0)
-        const int tile = t0 + warp + it * kFlashWarps;
+        const int tile = t0 + warp + it * W;
         const int st = it % kFlashStages;
         uint8_t* dst = ring + st * kStageBytes;
         fence_proxy_async_smem();
@@ -477,11 +436,11 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     }
     const int R = P.rope_dim, half = R / 2;
     if (P.fuse)   // positions are not written by the preceding kernel: build the table now
-        for (int i = t_id; i < half; i += kFlashWarps * 32) {
-            float c, s;
-            rope_cos_sin(static_cast<double>(p) * fr.w[i], c, s);
+        for (int i = t_id; i < half; i += kNT) {
+            float c, sv;
+            rope_cos_sin(static_cast<double>(p) * fr.w[i], c, sv);
             cs[i] = c;
-            sn[i] = s;
+            sn[i] = sv;
         }
     if (P.early) pdl_wait_trigger();
 
@@ -524,14 +483,14 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
         if (owner) {   // the new token's K and V rows: into the cache and into shared memory
             const int64_t crow = (row0 + slot_p) * D;
             const float* krow = qrow0 + static_cast<int64_t>(P.n_q + g) * D;
-            if (warp == 0) {
+            if (warp == W - 2) {
                 rotate(krow, P.g_k, kbuf);
                 for (int e = lane; e < D; e += 32) {
                     const uint16_t h = __half_as_ushort(__float2half_rn(kbuf[e]));
                     knew[e] = h;
                     P.k_out[crow + e] = h;
                 }
-            } else if (warp == 1) {
+            } else if (warp == W - 1) {
                 if (P.v_mode == 1) {   // V = unweighted RMSNorm of the raw K row
                     float ss = 0.f;
                     for (int e = lane; e < D; e += 32) ss = fmaf(krow[e], krow[e], ss);
@@ -586,12 +545,12 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     for (int m = 0; m < D / 16; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     const bool head_ok = tq < G;
-    __half* pb = pbuf + warp * 8 * FlashSmem::kPbufPitch;
+    __half* pb = pbuf + warp * 8 * kPbufPitch;
     bool ok = true;
 
     for (int it = 0; it < nmy; ++it) {
         const int st = it % kFlashStages;
-        const int tile = t0 + warp + it * kFlashWarps;
+        const int tile = t0 + warp + it * W;
         uint8_t* kt = ring + st * kStageBytes;
         uint8_t* vt = kt + kTileBytes;
         if (ok) ok = mbar_wait(&wbar[st], static_cast<uint32_t>((it / kFlashStages) & 1), P.status);
@@ -648,16 +607,16 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
             __half h0, l0, h1, l1;
             split_hi_lo(p0, h0, l0);
             split_hi_lo(p1, h1, l1);
-            pb[(2 * tq) * FlashSmem::kPbufPitch + gq] = h0;
-            pb[(2 * tq + 1) * FlashSmem::kPbufPitch + gq] = l0;
-            pb[(2 * tq) * FlashSmem::kPbufPitch + gq + 8] = h1;
-            pb[(2 * tq + 1) * FlashSmem::kPbufPitch + gq + 8] = l1;
+            pb[(2 * tq) * kPbufPitch + gq] = h0;
+            pb[(2 * tq + 1) * kPbufPitch + gq] = l0;
+            pb[(2 * tq) * kPbufPitch + gq + 8] = h1;
+            pb[(2 * tq + 1) * kPbufPitch + gq + 8] = l1;
         }
         __syncwarp();
         uint32_t pb0, pb1;
         {
             const int n = lane & 7, kk = ((lane >> 3) & 1) * 8;
-            ldmatrix_x2(pb0, pb1, smem_u32(pb + n * FlashSmem::kPbufPitch + kk));
+            ldmatrix_x2(pb0, pb1, smem_u32(pb + n * kPbufPitch + kk));
         }
         // O^T += V^T P^T
         const uint32_t vb = smem_u32(vt);
@@ -673,11 +632,11 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
     }
     if (!ok && lane == 0) drain_stages(wbar, kFlashStages, max(0, nmy - kFlashStages), nmy - 1);
 
-    // ---- merge the four warps' states (ascending warp order) --------------------------------
+    // ---- merge the W warps' states (ascending warp order) -----------------------------------
     __syncthreads();  // all rings idle: reuse them for the combine buffers
-    float* cm = comb;                                    // [warp][4] max
-    float* cl = comb + kFlashWarps * 4;                  // [warp][4] denominators
-    float* co = comb + 2 * kFlashWarps * 4;              // [warp][4][D] outputs
+    float* cm = comb;                        // [warp][4] max
+    float* cl = comb + W * 4;                // [warp][4] denominators
+    float* co = comb + 2 * W * 4;            // [warp][4][D] outputs
     if (gq == 0 && head_ok) {
         cm[warp * 4 + tq] = nmy ? m_run : -INFINITY;
         cl[warp * 4 + tq] = nmy ? l_run : 0.f;
@@ -690,27 +649,22 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
         }
     }
     __syncthreads();
-    for (int e = t_id; e < G * D; e += kFlashWarps * 32) {
+    const int64_t pstride = static_cast<int64_t>(P.nsplit_max) * (D + 2);   // one head's splits
+    float* part0 = P.part + (static_cast<int64_t>(b) * P.n_q + g * G) * pstride;
+    for (int e = t_id; e < G * D; e += kNT) {
         const int h = e / D, i = e - h * D;
         float M = -INFINITY;
-        for (int w = 0; w < kFlashWarps; ++w) M = fmaxf(M, cm[w * 4 + h]);
+        for (int w = 0; w < W; ++w) M = fmaxf(M, cm[w * 4 + h]);
         float L = 0.f, O = 0.f;
-        for (int w = 0; w < kFlashWarps; ++w) {
+        for (int w = 0; w < W; ++w) {
             const float f = expf(cm[w * 4 + h] - M);   // warps without tiles: e^-inf = 0
             L += f * cl[w * 4 + h];
             O += f * co[(w * 4 + h) * D + i];
         }
-        const int hg = g * G + h;
         if (nsplit == 1) {
-            P.out[b * P.ldo + static_cast<int64_t>(hg) * D + i] = O / L;
-        } else if (P.cluster) {
-            cexp[h * (D + 2) + i] = O;
-            if (i == 0) {
-                cexp[h * (D + 2) + D] = M;
-                cexp[h * (D + 2) + D + 1] = L;
-            }
+            P.out[b * P.ldo + static_cast<int64_t>(g * G + h) * D + i] = O / L;
         } else {
-            float* dst = P.part + ((static_cast<int64_t>(b) * P.n_q + hg) * P.nsplit_max + split) * (D + 2);
+            float* dst = part0 + h * pstride + static_cast<int64_t>(split) * (D + 2);
             dst[i] = O;
             if (i == 0) {
                 dst[D] = M;
@@ -718,9 +672,68 @@ __global__ void __launch_bounds__(kFlashWarps * 32, 1) gqa_flash_kernel(const __
             }
         }
     }
-    if (P.cluster)
-        cluster_merge(cexp, G, D, nsplit, static_cast<uint32_t>(split), gridDim.x,
-                      P.out + b * P.ldo + static_cast<int64_t>(g * G) * D);
+    if (nsplit == 1) return;
+
+    // ---- the last split of this (sequence, KV head) to arrive combines all of them ----------
+    // The barrier orders every thread's partial-state writes before thread 0's ticket, whose
+    // release (cumulative) publishes them device-wide; its acquire orders the merging CTA's
+    // reads of the other splits' states after their tickets.
+    __syncthreads();
+    unsigned* cnt = P.cnt + b * P.n_kv + g;
+    if (t_id == 0) {
+        unsigned ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(cnt) : "memory");
+        last_sh = ticket == static_cast<unsigned>(nsplit - 1);
+    }
+    __syncthreads();
+    if (!last_sh) return;
+    // Split weights per head, one warp per head: lane s holds split s (s < nsplit <= 32 per
+    // round); the maximum and the weighted denominator are fixed shuffle trees over the lanes,
+    // so the result is the same whichever CTA merges.
+    float* wsm = comb;                                // [G][kMaxFlashSplits]: e^(m_s - M_h)
+    float* lsm = comb + 4 * kMaxFlashSplits;          // [G]: the combined denominators
+    if (warp < G) {
+        const int h = warp;
+        const float* hs = part0 + h * pstride + D;
+        float mv[kMaxFlashSplits / 32], lv[kMaxFlashSplits / 32];
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMaxFlashSplits / 32; ++r) {
+            const int sp = lane + 32 * r;
+            mv[r] = sp < nsplit ? __ldcg(hs + static_cast<int64_t>(sp) * (D + 2)) : -INFINITY;
+            lv[r] = sp < nsplit ? __ldcg(hs + static_cast<int64_t>(sp) * (D + 2) + 1) : 0.f;
+            M = fmaxf(M, mv[r]);
+        }
+        M = warp_max(M);
+        float L = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxFlashSplits / 32; ++r) {
+            const int sp = lane + 32 * r;
+            const float f = sp < nsplit ? expf(mv[r] - M) : 0.f;
+            if (sp < nsplit) wsm[h * kMaxFlashSplits + sp] = f;
+            L = fmaf(f, lv[r], L);
+        }
+        L = warp_sum(L);
+        if (lane == 0) lsm[h] = L;
+    }
+    __syncthreads();
+    // every split's output element loaded in one round, then summed in ascending split order
+    for (int e = t_id; e < G * D; e += kNT) {
+        const int h = e / D, i = e - h * D;
+        const float* src = part0 + h * pstride + i;
+        const float* wh = wsm + h * kMaxFlashSplits;
+        float O = 0.f;
+        for (int s0 = 0; s0 < nsplit; s0 += 16) {
+            float a[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) a[u] = s0 + u < nsplit ? __ldcg(src + static_cast<int64_t>(s0 + u) * (D + 2)) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (s0 + u < nsplit) O = fmaf(wh[s0 + u], a[u], O);
+        }
+        P.out[b * P.ldo + static_cast<int64_t>(g * G + h) * D + i] = O / lsm[h];
+    }
+    if (t_id == 0) *cnt = 0u;   // ready for the next call (which follows this kernel's completion)
 }
 
 // Ordered merge of split states:  M = max_s m_s,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s
@@ -793,93 +806,78 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const AttnPara
 
 struct Plan {
     bool flash;
-    bool cluster;   // flash splits merged inside a thread-block cluster (no workspace)
+    int W;          // flash: warps per CTA
     int tp, nsplit_max, ltile, ns;
     uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off;
-    size_t smem, ws;
+    size_t smem, ws, cnt_off;   // cnt_off: byte offset of the flash arrival counters in the workspace
 };
 
 bool use_flash(int n_q, int n_kv, int d) { return d <= 256 && n_q / n_kv <= 4; }
 
-size_t flash_smem(int d) {
-    const size_t ring = static_cast<size_t>(kFlashWarps) * kFlashStages * 2 * kFlashTile * d * 2;
-    // + the fused path's rotated query heads, K row, rotation table and new K/V rows (28 d bytes)
-    return align_up(ring + 128 + kFlashWarps * 8 * FlashSmem::kPbufPitch * 2 + 28ull * d, 1024) + 1024;
+size_t flash_smem(int d, int W) {
+    const size_t ring = static_cast<size_t>(W) * kFlashStages * 2 * kFlashTile * d * 2;
+    // + barriers, P^T buffers, the fused path's query heads, K row, rotation table, new K/V rows
+    return align_up(ring + 128 + static_cast<size_t>(W) * 8 * kPbufPitch * 2 + 28ull * d, 1024) + 1024;
 }
 
-const void* pick(int d, bool flash);
+const void* pick(int d, bool flash, int W);
 gem_status ensure_smem_attn(const void* fn, int device, size_t bytes);
 
-// Largest cluster of flash CTAs (16, non-portable, or 8) the device can schedule for head
-// dimension d; 1 when none.  Queried once per (device, d).  Used for d <= 128 only: at d = 256
-// (two CTAs per SM) the clustered splits measured slower than the merge launch (Gemma
-// sliding-window layer, 16 KV heads x 1024 slots: 19.3 us against 12.3 us).
-int flash_cluster_max(int d, int device) {
-    if (d > 128) return 1;
+// Resident flash CTAs per SM for (d, W) on this device (occupancy query, cached).
+int flash_ctas_per_sm(int d, int W, int device) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, int> done;
+    static std::map<std::tuple<int, int, int>, int> done;
     std::lock_guard<std::mutex> lk(mu);
-    auto it = done.find({device, d});
+    auto it = done.find({device, d, W});
     if (it != done.end()) return it->second;
-    int best = 1;
-    const void* fn = pick(d, true);
-    const size_t smem = flash_smem(d);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess) {
-        for (int cs : {kMaxClusterSplits, 8}) {
-            if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-                (void)cudaGetLastError();
-                continue;
-            }
-            cudaLaunchConfig_t cfg{};
-            cfg.gridDim = dim3(cs, 1, 1);
-            cfg.blockDim = dim3(kFlashWarps * 32);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute a[1];
-            a[0].id = cudaLaunchAttributeClusterDimension;
-            a[0].val.clusterDim.x = cs;
-            a[0].val.clusterDim.y = 1;
-            a[0].val.clusterDim.z = 1;
-            cfg.attrs = a;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) {
-                best = cs;
-                break;
-            }
-            (void)cudaGetLastError();
-        }
+    int n = 1;
+    const void* fn = pick(d, true, W);
+    const size_t smem = flash_smem(d, W);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) ==
+            cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, W * 32, smem) == cudaSuccess && n >= 1) {
     } else {
         (void)cudaGetLastError();
+        n = 1;
     }
-    done[{device, d}] = best;
-    return best;
+    done[{device, d, W}] = n;
+    return n;
 }
 
-Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num_sms, int cluster_max) {
+Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num_sms, int device) {
     Plan pl{};
     pl.flash = use_flash(n_q, n_kv, d);
     pl.tp = pl.flash ? kFlashTile : tile_slots(d);
     const int64_t tmax = window ? std::min<int64_t>(window, cap) : cap;
     const int64_t nt_max = std::max<int64_t>(1, (tmax + pl.tp - 1) / pl.tp);
-    const int64_t target = 2LL * num_sms;
-    int64_t ns = std::max<int64_t>(1, (target + static_cast<int64_t>(B) * n_kv - 1) / (static_cast<int64_t>(B) * n_kv));
-    ns = std::min(ns, nt_max);
-    if (!pl.flash) {
-        const int max_tiles = kMaxSplitSlots / pl.tp;
-        if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
-    }
-    ns = std::min<int64_t>(ns, kMaxSplits);
-    // flash: the splits of one (sequence, KV head) merge in a cluster when the device allows one
-    // of that many CTAs (the split count is capped at the cluster size)
-    pl.cluster = pl.flash && ns > 1 && cluster_max >= 2;
-    if (pl.cluster) ns = std::min<int64_t>(ns, cluster_max);
-    pl.nsplit_max = static_cast<int>(ns);
-    pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
-    pl.ws = pl.cluster ? 0 : static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float);
+    const int64_t pairs = static_cast<int64_t>(B) * n_kv;
     if (pl.flash) {
-        pl.smem = flash_smem(d);
+        // Eight warps per CTA while there are few (sequence, KV head) pairs, else four (smaller
+        // CTAs, more of them resident per SM); as many splits as fill the SMs' resident slots.
+        pl.W = (d <= 128 && pairs * 8 <= num_sms) ? 8 : 4;
+        const int64_t slots = static_cast<int64_t>(flash_ctas_per_sm(d, pl.W, device)) * num_sms;
+        int64_t ns = std::max<int64_t>(1, slots / pairs);
+        ns = std::min<int64_t>(std::min<int64_t>(ns, nt_max), kMaxFlashSplits);
+        pl.nsplit_max = static_cast<int>(ns);
+        pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
+        pl.smem = flash_smem(d, pl.W);
+        if (ns > 1) {
+            const size_t part = static_cast<size_t>(B) * n_q * ns * (d + 2) * sizeof(float);
+            pl.cnt_off = align_up(part, 256);
+            pl.ws = pl.cnt_off + align_up(static_cast<size_t>(pairs) * sizeof(unsigned), 256);
+        }
         return pl;
     }
+    const int64_t target = 2LL * num_sms;
+    int64_t ns = std::max<int64_t>(1, (target + pairs - 1) / pairs);
+    ns = std::min(ns, nt_max);
+    const int max_tiles = kMaxSplitSlots / pl.tp;
+    if ((nt_max + ns - 1) / ns > max_tiles) ns = (nt_max + max_tiles - 1) / max_tiles;
+    ns = std::min<int64_t>(ns, kMaxSplits);
+    pl.nsplit_max = static_cast<int>(ns);
+    pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
+    pl.ws = ns > 1 ? static_cast<size_t>(B) * n_q * pl.nsplit_max * (d + 2) * sizeof(float) : 0;
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
     pl.ns = d >= 512 ? 3 : 4;
     pl.ns = static_cast<int>(std::min<int64_t>(pl.ns, 2 * pl.ltile));
@@ -900,12 +898,14 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
     return pl;
 }
 
-const void* pick(int d, bool flash) {
+const void* pick(int d, bool flash, int W) {
     if (flash) {
         switch (d) {
-            case 64: return reinterpret_cast<const void*>(gqa_flash_kernel<64>);
-            case 128: return reinterpret_cast<const void*>(gqa_flash_kernel<128>);
-            default: return reinterpret_cast<const void*>(gqa_flash_kernel<256>);
+            case 64: return W == 8 ? reinterpret_cast<const void*>(gqa_flash_kernel<64, 8>)
+                                   : reinterpret_cast<const void*>(gqa_flash_kernel<64, 4>);
+            case 128: return W == 8 ? reinterpret_cast<const void*>(gqa_flash_kernel<128, 8>)
+                                    : reinterpret_cast<const void*>(gqa_flash_kernel<128, 4>);
+            default: return reinterpret_cast<const void*>(gqa_flash_kernel<256, 4>);
         }
     }
     switch (d) {
@@ -927,14 +927,15 @@ gem_status ensure_smem_attn(const void* fn, int device, size_t bytes) {
     return GEM_OK;
 }
 
-gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool fuse) {
+// chain: launched right after the library's QKV projection, which clears the flash arrival
+// counters; otherwise (stand-alone calls) they are cleared here, on the stream, first.
+gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool fuse, bool chain) {
     gem_status st = attn_check(op);
     if (st != GEM_OK || op.B == 0 || op.n_q == 0) return st;
     DeviceInfo di;
     if ((st = device_info(&di)) != GEM_OK) return st;
-    const int cmax = use_flash(op.n_q, op.n_kv, op.d) ? flash_cluster_max(op.d, di.device) : 1;
-    const Plan pl = make_plan(op.B, op.n_q, op.n_kv, op.d, op.cache_cap, op.window, di.num_sms, cmax);
-    if (pl.nsplit_max > 1 && !pl.cluster && (!op.workspace || op.ws_bytes < pl.ws)) return GEM_ERR_WORKSPACE;
+    const Plan pl = make_plan(op.B, op.n_q, op.n_kv, op.d, op.cache_cap, op.window, di.num_sms, di.device);
+    if (pl.nsplit_max > 1 && (!op.workspace || op.ws_bytes < pl.ws)) return GEM_ERR_WORKSPACE;
     if (pl.smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
     AttnParams P{};
     P.q = op.q;
@@ -964,7 +965,9 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     P.pa_off = pl.pa_off;
     P.st_off = pl.st_off;
     P.status = op.status ? op.status : di.status_word;
-    P.cluster = pl.cluster ? 1 : 0;
+    P.cnt = pl.flash && pl.nsplit_max > 1
+                ? reinterpret_cast<unsigned*>(static_cast<char*>(op.workspace) + pl.cnt_off)
+                : nullptr;
     RopeFreq fr{};
     if (fuse) {
         if (!pl.flash) return GEM_ERR_UNSUPPORTED_SHAPE;
@@ -993,18 +996,15 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     if ((st = make_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, op.v_cache, op.d, rows,
                                  static_cast<uint64_t>(op.d) * 2, 64, pl.tp, CU_TENSOR_MAP_SWIZZLE_128B)) != GEM_OK)
         return st;
-    const void* fn = pick(op.d, pl.flash);
+    const void* fn = pick(op.d, pl.flash, pl.W);
     if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
+    if (P.cnt && !chain)
+        GEM_CUDA_TRY(cudaMemsetAsync(P.cnt, 0, static_cast<size_t>(op.B) * op.n_kv * sizeof(unsigned), stream));
     dim3 grid(pl.nsplit_max, op.n_kv, op.B);
     void* args[] = {&tmK, &tmV, &P, &fr};   // the split kernel takes the first three
-    if (pl.cluster) {
-        if (pl.nsplit_max > 8)
-            GEM_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-        return launch_pdl_cluster(fn, grid, dim3(kFlashWarps * 32), pl.smem, stream, args, pl.nsplit_max);
-    }
-    if ((st = launch_pdl(fn, grid, dim3(pl.flash ? kFlashWarps * 32 : kAttnThreads), pl.smem, stream, args)) != GEM_OK)
+    if ((st = launch_pdl(fn, grid, dim3(pl.flash ? pl.W * 32 : kAttnThreads), pl.smem, stream, args)) != GEM_OK)
         return st;
-    if (pl.nsplit_max > 1) {
+    if (!pl.flash && pl.nsplit_max > 1) {
         int D = op.d;
         void* margs[] = {&P, &D};
         st = launch_pdl(reinterpret_cast<const void*>(gqa_merge_kernel), dim3(op.B * op.n_q), dim3(kMergeThreads), 0,
@@ -1017,11 +1017,22 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
 
 size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window) {
     if (B <= 0 || n_q <= 0 || n_kv <= 0 || cache_cap <= 0) return 0;
+    if (d != 64 && d != 128 && d != 256 && d != 512) return 0;
     DeviceInfo di;
     if (device_info(&di) != GEM_OK) return 0;
-    const int cmax = use_flash(n_q, n_kv, d) ? flash_cluster_max(d, di.device) : 1;
-    const Plan pl = make_plan(B, n_q, n_kv, d, cache_cap, window, di.num_sms, cmax);
-    return pl.nsplit_max > 1 && !pl.cluster ? align_up(pl.ws, 256) : 0;
+    const Plan pl = make_plan(B, n_q, n_kv, d, cache_cap, window, di.num_sms, di.device);
+    return pl.nsplit_max > 1 ? align_up(pl.ws, 256) : 0;
+}
+
+size_t attn_counter_offset(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window, size_t* bytes) {
+    *bytes = 0;
+    if (B <= 0 || n_q <= 0 || n_kv <= 0 || cache_cap <= 0 || !use_flash(n_q, n_kv, d)) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != GEM_OK) return 0;
+    const Plan pl = make_plan(B, n_q, n_kv, d, cache_cap, window, di.num_sms, di.device);
+    if (pl.nsplit_max <= 1) return 0;
+    *bytes = static_cast<size_t>(B) * n_kv * sizeof(unsigned);
+    return pl.cnt_off;
 }
 
 gem_status attn_check(const AttnOp& op) {
@@ -1041,13 +1052,15 @@ gem_status attn_check(const AttnOp& op) {
     return GEM_OK;
 }
 
-gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, false, false); }
-gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, false); }
+gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, false, false, false); }
+gem_status attn_enqueue_in_chain(const AttnOp& op, cudaStream_t stream) {
+    return attn_launch(op, stream, true, false, false);
+}
 bool attn_fusable(int n_q, int n_kv, int d) { return n_kv > 0 && n_q % n_kv == 0 && use_flash(n_q, n_kv, d); }
-gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, true); }
+gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream) { return attn_launch(op, stream, true, true, true); }
 // The fused form as a stand-alone call: nothing is read before griddepcontrol.wait.
 gem_status attn_enqueue_fused_standalone(const AttnOp& op, cudaStream_t stream) {
-    return attn_launch(op, stream, false, true);
+    return attn_launch(op, stream, false, true, false);
 }
 
 // ---- split-partial scratch owned by the library (gem_gqa_decode_attn_noalloc) --------------

@@ -119,6 +119,12 @@ __device__ __forceinline__ void drain_stages(uint64_t* bars, int ns, int first, 
     for (int s = first; s <= last; ++s) (void)mbar_wait(&bars[s % ns], static_cast<uint32_t>((s / ns) & 1), nullptr);
 }
 
+// Words that a kernel sets to zero for a later launch (CTA 0's threads, after the wait).
+__device__ __forceinline__ void clear_words(unsigned* w, int n, int tid, int nthreads) {
+    if (w && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = tid; i < n; i += nthreads) w[i] = 0u;
+}
+
 // ---- TMA -------------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;

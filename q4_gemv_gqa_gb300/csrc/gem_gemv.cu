@@ -75,6 +75,8 @@ gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream) {
     p.gamma = op.norm_gamma;
     p.eps = op.eps;
     p.act = op.act;
+    p.clear = op.clear;
+    p.nclear = op.nclear;
 
     const uintptr_t wbits = reinterpret_cast<uintptr_t>(op.W0) | reinterpret_cast<uintptr_t>(op.W1);
     const uintptr_t xbits = reinterpret_cast<uintptr_t>(op.x) | reinterpret_cast<uintptr_t>(op.norm_gamma);

@@ -39,6 +39,8 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
     p.eps = op.eps;
     p.act = op.act;
     p.status = di.status_word;
+    p.clear = op.clear;
+    p.nclear = op.nclear;
     p.U = static_cast<int>((op.N + kUnitRows - 1) / kUnitRows);
     auto kernel_of = [&](int ks) {
         if (ks == 2)
@@ -64,7 +66,10 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
         off = align_up(off + red, 128);
         const size_t misc_off = off;
         off += 128 * 4;
+        const size_t bsc_off = off;
+        off += static_cast<size_t>(Gk) * 8 * 4;   // per block: 2^-e of its operand scale
         if (commit) {
+            p.bsc_off = static_cast<uint32_t>(bsc_off);
             p.stage_bytes = static_cast<uint32_t>(stage);
             p.full_off = static_cast<uint32_t>(full_off);
             p.empty_off = static_cast<uint32_t>(empty_off);

@@ -17,8 +17,10 @@
 //   elsewhere, so D[row][2t + h] is the dot product of the row's block t with the hi or lo part.
 //   Lane (g, t) ends a task holding rows g and g + 8 of its own block in hi and lo: one
 //   d * (hi + lo) per row.  All 8 columns are used, where a plain layout would use 2 of 8.
-// * The activation vector is scaled by one power of two (its largest magnitude to [2^13, 2^14)),
-//   undone exactly in the epilogue.
+// * Each 32-weight block of the activation vector is scaled by its own power of two (its largest
+//   magnitude to [2^13, 2^14)), undone exactly by folding the inverse into the block's scale d.
+//   The records are therefore built straight from the loads: one CTA-wide barrier between the
+//   activation loads and the first task; a fused RMSNorm's 1/rms only scales the epilogue.
 //
 // Reference: "Q4_0 dequant-matvec" (GGML block: fp16 d, 16 bytes of codes, value (q - 8) * d).
 #pragma once
@@ -62,8 +64,10 @@ struct Params {
     int nphase;
     int ns;
     int ncw;             // consumer warps = 2 * gps
-    uint32_t stage_bytes, full_off, empty_off, xf_off, red_off, misc_off;
+    uint32_t stage_bytes, full_off, empty_off, xf_off, red_off, misc_off, bsc_off;
     int* status;
+    unsigned* clear;     // words zeroed after the wait (see GemvOp)
+    int nclear;
 };
 
 // qs byte held in byte j of code word i of a lane's block.  Odd blocks: word i = bytes 4i..4i+3.
@@ -97,7 +101,7 @@ __device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank
 // 5 words in row g of row block 0 (row g + 8 is 8 rows further, row block r is r * rstride
 // further); xr = shared offset of the lane's 64-byte activation operand.
 template <bool ODD, int NR>
-__device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t rstride, uint32_t xr,
+__device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t rstride, uint32_t xr, float bs,
                                      float (&t0)[kMaxRps], float (&t1)[kMaxRps]) {
     const uint4* xp = reinterpret_cast<const uint4*>(smem + xr);
     uint4 xb[4];
@@ -150,9 +154,9 @@ __device__ __forceinline__ void task(const uint8_t* smem, uint32_t a, uint32_t r
         }
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        t0[r] = fmaf(da[r], d[r][0] + d[r][1], t0[r]);
-        t1[r] = fmaf(db[r], d[r][2] + d[r][3], t1[r]);
+    for (int r = 0; r < NR; ++r) {   // bs: 2^-e of the block's operand scale (exact)
+        t0[r] = fmaf(da[r] * bs, d[r][0] + d[r][1], t0[r]);
+        t1[r] = fmaf(db[r] * bs, d[r][2] + d[r][3], t1[r]);
     }
 }
 
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + p.empty_off);
     float* red = reinterpret_cast<float*>(smem + p.red_off);    // [row of pass][warp]
-    float* misc = reinterpret_cast<float*>(smem + p.misc_off);  // [0, 2 ncw): reductions; [64], [65]: scales
+    float* misc = reinterpret_cast<float*>(smem + p.misc_off);  // [warp]: partial sums of squares
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ncw = p.ncw, nct = ncw * 32;
@@ -255,139 +259,146 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
 
     // ---------------- consumer warps ----------------
     pdl_wait_trigger();   // the activations (and residual) come from the previous kernel
+    clear_words(p.clear, p.nclear, tid, nct);
 
     const int K = G * 256, K4 = K / 4;
     // this CTA's records cover groups [gk0, gk0 + Gr): float4s [kr0, kr1) of the row
     const int kr0 = gk0 * 64, kr1 = (gk0 + Gr) * 64;
-    // Without a fused RMSNorm the CTAs of a K split scale their own range by their own power of
-    // two (exact) and unscale their partial sums before the cluster adds them, so each reads only
-    // its range; the norm's sum of squares needs the whole row.
-    const bool own_range = KS > 1 && !p.gamma;
-    const int sr0 = own_range ? kr0 : 0, sr1 = own_range ? kr1 : K4;   // float4s the statistics read
-    // Up to kProN float4 per consumer thread are read once and kept in registers; longer ranges
-    // are read twice (statistics, then the records).
+    float* bsc = reinterpret_cast<float*>(smem + p.bsc_off);   // [local block]: 2^-e of its operand scale
+    uint8_t* xf = smem + p.xf_off;
+    const float4* x4 = reinterpret_cast<const float4*>(p.x);
+    const float4* g4 = reinterpret_cast<const float4*>(p.gamma);
+    float ss = 0.f;   // sum of x^2 for a fused RMSNorm (whole row), needed only by the epilogue
+    // Every 32-weight block gets its own power of two taking its largest |gamma x| to
+    // [2^13, 2^14) (exact), undone by folding 2^-e into the block's scale d in the tasks, so the
+    // records are built straight from the loads with no CTA-wide reduction first.  The 8 float4
+    // of a block are held by 8 consecutive lanes: their maximum takes 3 shuffles.  Every lane
+    // of the warp calls this (valid or not); it returns 2^e.
+    auto block_scale = [&](float4 v, bool valid, int lb) -> float {
+        float m = valid ? fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) : 0.f;
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        int e = 0;
+        if (m > 0.f) e = 13 - (((__float_as_int(m) >> 23) & 0xff) - 127);
+        e = max(-126, min(126, e));
+        if (valid && (lane & 7) == 0) bsc[lb] = __int_as_float((127 - e) << 23);
+        return __int_as_float((127 + e) << 23);
+    };
+    // activation records: record (hg, column 2t + h), tile tau, register r holds the h part of
+    // the two elements of block 2t + (hg & 1) of group hg / 2 that lane t's k-slots of that
+    // register meet in the A operand (bytes j = r and r + 2 of code word tau / 2, nibble tau & 1).
+    // Float4 i of the row, scaled by sc, into its slots (element m of a block's nibble half goes
+    // to the slot of qs byte m).
+    auto scatter4 = [&](float4 v, float sc, int i) {
+        const int k0 = 4 * i;
+        const int blk = (k0 >> 5) & 7, e0 = k0 & 31;
+        const bool odd = blk & 1;
+        const uint32_t rec = static_cast<uint32_t>((2 * ((k0 >> 8) - gk0) + (odd ? 1 : 0)) * kRecBytes +
+                                                   (blk >> 1) * 128 + (e0 >> 4) * 8);
+        const float v4[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int ci, cj;
+            code_slot(odd, (e0 & 15) + e, ci, cj);
+            const uint32_t off = rec + ci * 16 + (cj & 1) * 4 + (cj >> 1) * 2;
+            __half h, l;
+            split_hi_lo(v4[e], h, l);
+            *reinterpret_cast<__half*>(xf + off) = h;
+            *reinterpret_cast<__half*>(xf + off + 64) = l;
+        }
+    };
+    // Up to kProN float4 per consumer thread are read once (loads first) and converted from
+    // registers; longer ranges are read twice (block scales, then a gather of the records).
     constexpr int kProN = KS > 1 ? kProSplit : kPro;
-    const bool onepass = sr1 - sr0 <= kProN * nct;
-    float4 xv[kProN];
-    // 1. largest |gamma * x| and sum of x^2 over the statistics' range
-    {
-        float mx = 0.f, ss = 0.f;
-        const float4* x4 = reinterpret_cast<const float4*>(p.x);
-        const float4* g4 = reinterpret_cast<const float4*>(p.gamma);
-        auto take = [&](float4 v, int i) {
+    if (kr1 - kr0 <= kProN * nct) {
+        float4 xv[kProN], gv[kProN];
+#pragma unroll
+        for (int u = 0; u < kProN; ++u) {
+            const int i = kr0 + tid + u * nct;
+            xv[u] = i < kr1 ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[u] = p.gamma && i < kr1 ? __ldg(g4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kProN; ++u) {
+            if (kr0 + u * nct >= kr1) break;   // uniform over the CTA
+            const int i = kr0 + tid + u * nct;
+            const bool valid = i < kr1;
+            float4 v = xv[u];
             ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-            if (p.gamma) {
+            v.x *= gv[u].x; v.y *= gv[u].y; v.z *= gv[u].z; v.w *= gv[u].w;
+            const float sc = block_scale(v, valid, (i - kr0) >> 3);
+            if (valid) scatter4(v, sc, i);
+        }
+    } else {
+        for (int i0 = kr0; i0 < kr1; i0 += nct) {   // block scales (uniform trip count)
+            const int i = i0 + tid;
+            const bool valid = i < kr1;
+            float4 v = valid ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            if (p.gamma && valid) {
                 const float4 gm = __ldg(g4 + i);
                 v.x *= gm.x; v.y *= gm.y; v.z *= gm.z; v.w *= gm.w;
             }
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-            return v;
-        };
-        if (onepass) {
+            (void)block_scale(v, valid, (i - kr0) >> 3);
+        }
+        gemv_mma::consumer_sync(nct);   // block scales visible
+        // gather: four registers per thread and round, their loads issued before converting
+        const int nreg = 2 * Gr * 64;   // (local hg, t, tau, r)
+        for (int i0 = tid; i0 < nreg; i0 += 4 * nct) {
+            float v0[4], v1[4], sc[4];
+            uint32_t off[4];
 #pragma unroll
-            for (int u = 0; u < kProN; ++u) {
-                const int i = sr0 + tid + u * nct;
-                xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < sr1) xv[u] = take(__ldg(x4 + i), i);
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * nct;
+                v0[u] = v1[u] = 0.f;
+                sc[u] = 1.f;
+                off[u] = 0;
+                if (i < nreg) {
+                    const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
+                    const bool odd = hg & 1;
+                    const int lb = (hg >> 1) * 8 + 2 * t + (odd ? 1 : 0);
+                    const int base = ((hg >> 1) + gk0) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
+                    const int k0 = base + code_byte(odd, tau >> 1, r);
+                    const int k1 = base + code_byte(odd, tau >> 1, r + 2);
+                    v0[u] = __ldg(p.x + k0);
+                    v1[u] = __ldg(p.x + k1);
+                    if (p.gamma) {
+                        v0[u] *= __ldg(p.gamma + k0);
+                        v1[u] *= __ldg(p.gamma + k1);
+                    }
+                    sc[u] = __int_as_float(0x7F000000 - __float_as_int(bsc[lb]));   // 2^e, exact
+                    off[u] = static_cast<uint32_t>(hg * kRecBytes + (2 * t) * 64 + tau * 8 + r * 4);
+                }
             }
-        } else {
-#pragma unroll 4
-            for (int i = sr0 + tid; i < sr1; i += nct) (void)take(__ldg(x4 + i), i);
-        }
-        mx = warp_max(mx);
-        ss = warp_sum(ss);
-        if (lane == 0) {
-            misc[warp] = mx;
-            misc[ncw + warp] = ss;
-        }
-        gemv_mma::consumer_sync(nct);
-        if (warp == 0) {
-            float m = lane < ncw ? misc[lane] : 0.f;
-            float q = lane < ncw ? misc[ncw + lane] : 0.f;
-            m = warp_max(m);
-            q = warp_sum(q);
-            if (lane == 0) {
-                int e = 0;   // power of two taking the largest magnitude to [2^13, 2^14)
-                if (m > 0.f) e = 13 - (((__float_as_int(m) >> 23) & 0xff) - 127);
-                e = max(-126, min(126, e));
-                float out = __int_as_float((127 - e) << 23);
-                if (p.gamma) out *= rsqrtf(q / static_cast<float>(K) + p.eps);
-                misc[64] = __int_as_float((127 + e) << 23);
-                misc[65] = out;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + u * nct < nreg) {
+                    __half h0, l0, h1, l1;
+                    split_hi_lo(v0[u] * sc[u], h0, l0);
+                    split_hi_lo(v1[u] * sc[u], h1, l1);
+                    *reinterpret_cast<__half2*>(xf + off[u]) = __halves2half2(h0, h1);
+                    *reinterpret_cast<__half2*>(xf + off[u] + 64) = __halves2half2(l0, l1);
+                }
             }
         }
-        gemv_mma::consumer_sync(nct);
     }
-    // 2. activation records: record (hg, column 2t + h), tile tau, register r holds the h part of
-    // the two elements of block 2t + (hg & 1) of group hg / 2 that lane t's k-slots of that register
-    // meet in the A operand (bytes j = r and r + 2 of code word tau / 2, nibble tau & 1).
-    uint8_t* xf = smem + p.xf_off;
-    {
-        const float sc = misc[64];
-        if (onepass) {
-            // scatter my float4s: element m of a block's nibble half goes to the slot of qs byte m
-#pragma unroll
-            for (int u = 0; u < kProN; ++u) {
-                const int i = sr0 + tid + u * nct;
-                if (i >= kr0 && i < kr1) {
-                    const int k0 = 4 * i;
-                    const int blk = (k0 >> 5) & 7, e0 = k0 & 31;
-                    const bool odd = blk & 1;
-                    const uint32_t rec = static_cast<uint32_t>((2 * ((k0 >> 8) - gk0) + (odd ? 1 : 0)) * kRecBytes +
-                                                               (blk >> 1) * 128 + (e0 >> 4) * 8);
-                    const float v4[4] = {xv[u].x * sc, xv[u].y * sc, xv[u].z * sc, xv[u].w * sc};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        int ci, cj;
-                        code_slot(odd, (e0 & 15) + e, ci, cj);
-                        const uint32_t off = rec + ci * 16 + (cj & 1) * 4 + (cj >> 1) * 2;
-                        __half h, l;
-                        split_hi_lo(v4[e], h, l);
-                        *reinterpret_cast<__half*>(xf + off) = h;
-                        *reinterpret_cast<__half*>(xf + off + 64) = l;
-                    }
-                }
+    if (KS > 1 && p.gamma)   // the norm needs the whole row: the sum of squares outside this range
+        for (int i = tid; i < K4; i += nct)
+            if (i < kr0 || i >= kr1) {
+                const float4 v = __ldg(x4 + i);
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
-        } else {
-            // gather: four registers per thread and round, their loads issued before converting
-            const int nreg = 2 * Gr * 64;   // (local hg, t, tau, r)
-            for (int i0 = tid; i0 < nreg; i0 += 4 * nct) {
-                float v0[4], v1[4];
-                uint32_t off[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + u * nct;
-                    v0[u] = v1[u] = 0.f;
-                    off[u] = 0;
-                    if (i < nreg) {
-                        const int hg = i >> 6, t = (i >> 4) & 3, tau = (i >> 1) & 7, r = i & 1;
-                        const bool odd = hg & 1;
-                        const int base = ((hg >> 1) + gk0) * 256 + (2 * t + (odd ? 1 : 0)) * 32 + (tau & 1) * 16;
-                        const int k0 = base + code_byte(odd, tau >> 1, r);
-                        const int k1 = base + code_byte(odd, tau >> 1, r + 2);
-                        v0[u] = __ldg(p.x + k0);
-                        v1[u] = __ldg(p.x + k1);
-                        if (p.gamma) {
-                            v0[u] *= __ldg(p.gamma + k0);
-                            v1[u] *= __ldg(p.gamma + k1);
-                        }
-                        off[u] = static_cast<uint32_t>(hg * kRecBytes + (2 * t) * 64 + tau * 8 + r * 4);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (i0 + u * nct < nreg) {
-                        __half h0, l0, h1, l1;
-                        split_hi_lo(v0[u] * sc, h0, l0);
-                        split_hi_lo(v1[u] * sc, h1, l1);
-                        *reinterpret_cast<__half2*>(xf + off[u]) = __halves2half2(h0, h1);
-                        *reinterpret_cast<__half2*>(xf + off[u] + 64) = __halves2half2(l0, l1);
-                    }
-                }
-            }
-        }
-        if (tid < kZeroBytes / 4) reinterpret_cast<uint32_t*>(xf + 2 * Gr * kRecBytes)[tid] = 0u;
-        gemv_mma::consumer_sync(nct);
+    ss = warp_sum(ss);
+    if (lane == 0) misc[warp] = ss;
+    if (tid < kZeroBytes / 4) reinterpret_cast<uint32_t*>(xf + 2 * Gr * kRecBytes)[tid] = 0u;
+    gemv_mma::consumer_sync(nct);   // records, block scales and partial sums of squares complete
+    // the fused RMSNorm's 1 / rms, summed in the same order in every thread
+    float out = 1.f;
+    if (p.gamma) {
+        float q = 0.f;
+        for (int w = 0; w < ncw; ++w) q += misc[w];
+        out = rsqrtf(q / static_cast<float>(K) + p.eps);
     }
 
     const int g = lane >> 2, t = lane & 3;
@@ -421,9 +432,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                     if (ok) ok = mbar_wait(&full[slot], par, p.status);
                     if (mine && ok) {
                         const uint32_t a = static_cast<uint32_t>(slot) * stage_bytes + aoff;
-                        if (nr == 3) task<ODD, 3>(smem, a, rstride, xr, t0, t1);
-                        else if (nr == 2) task<ODD, 2>(smem, a, rstride, xr, t0, t1);
-                        else task<ODD, 1>(smem, a, rstride, xr, t0, t1);
+                        const float bs = bsc[(ph * gps + jg) * 8 + 2 * t + (ODD ? 1 : 0)];
+                        if (nr == 3) task<ODD, 3>(smem, a, rstride, xr, bs, t0, t1);
+                        else if (nr == 2) task<ODD, 2>(smem, a, rstride, xr, bs, t0, t1);
+                        else task<ODD, 1>(smem, a, rstride, xr, bs, t0, t1);
                     }
                     __syncwarp();
                     if (lane == 0) gemv_mma::mbar_arrive(&empty[slot]);
@@ -454,18 +466,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                 }
             }
             gemv_mma::consumer_sync(nct);   // every partial sum of the pass written
-            const float out = misc[65];
             const int rows_in_pass = nrb * kUnitRows;
             if constexpr (KS > 1) {
-                // this CTA's sums over its K range per row (unscaled when the CTA scaled its own
-                // range), into the (now idle) records; the cluster then adds its ks ranges in rank
-                // order
+                // this CTA's sums over its K range per row, into the (now idle) records; the
+                // cluster then adds its ks ranges in rank order
                 float* part = reinterpret_cast<float*>(smem + p.xf_off);
-                const float pscale = own_range ? out : 1.f;
                 for (int row = tid; row < rows_in_pass; row += nct) {
                     float v = 0.f;
                     for (int w = 0; w < ncw; ++w) v += red[row * ncw + w];
-                    part[row] = v * pscale;
+                    part[row] = v;
                 }
                 cluster_sync_all();
                 const int nout = nrb / NMAT * kUnitRows;   // output rows of the pass
@@ -479,7 +488,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_b1_kernel(const __gr
                     for (int r = 0; r < ks; ++r) v += ld_cluster_f32(part + row, static_cast<uint32_t>(r));
                     if (NMAT == 2)
                         for (int r = 0; r < ks; ++r) uv += ld_cluster_f32(part + row + kUnitRows, static_cast<uint32_t>(r));
-                    const float cs = own_range ? 1.f : out;
+                    const float cs = out;
                     v *= cs;
                     if (NMAT == 1) {
                         if (p.residual) v += p.residual[n];

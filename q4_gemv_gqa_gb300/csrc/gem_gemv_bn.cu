@@ -223,6 +223,8 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     pp.B = B;
     pp.nchunk = std::max(1, std::min((32 * p.G + kPrepThreads - 1) / kPrepThreads, std::max(1, 152 / B)));
     pp.rec = rec;
+    pp.clear = op.clear;
+    pp.nclear = op.nclear;
     pp.rowinfo = reinterpret_cast<float2*>(rec + rec_bytes - 8 * sizeof(float2));
     void* pargs[] = {&pp};
     if ((st = launch_pdl(reinterpret_cast<const void*>(act_prep_kernel), dim3(pp.nchunk, B), dim3(kPrepThreads), 0,

@@ -51,10 +51,13 @@ struct PrepParams {
     int nchunk;          // CTAs per activation row
     uint8_t* rec;
     float2* rowinfo;
+    unsigned* clear;     // words zeroed after the wait (see GemvOp)
+    int nclear;
 };
 
 __global__ void __launch_bounds__(kPrepThreads) act_prep_kernel(const PrepParams p) {
     pdl_wait_trigger();
+    clear_words(p.clear, p.nclear, static_cast<int>(threadIdx.x), kPrepThreads);
     __shared__ float red_m[kPrepThreads / 32], red_s[kPrepThreads / 32];
     __shared__ float sc_sh;
     const int b = blockIdx.y, chunk = blockIdx.x;

@@ -19,6 +19,8 @@ struct GemvParams {
     const float* gamma;
     float eps;
     int act;
+    unsigned* clear;     // words zeroed after the wait (see GemvOp)
+    int nclear;
 };
 
 __device__ __forceinline__ float act_fn(float g, int act) {
@@ -37,6 +39,7 @@ __global__ void __launch_bounds__(256) q4_0_gemv_generic_kernel(const uint8_t* _
     __shared__ float red[8][8];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     pdl_wait_trigger();
+    clear_words(p.clear, p.nclear, static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x));
     if (p.gamma) {
         for (int b = 0; b < BATCH; ++b) {
             float part = 0.f;

@@ -55,6 +55,8 @@ gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceI
     p.eps = op.eps;
     p.act = op.act;
     p.status = di.status_word;
+    p.clear = op.clear;
+    p.nclear = op.nclear;
     p.U = static_cast<int>((op.N + kUnitRows - 1) / kUnitRows);
     const int C = std::min(di.num_sms, p.U);
     const int umax = (p.U + C - 1) / C;

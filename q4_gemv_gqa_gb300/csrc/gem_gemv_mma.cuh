@@ -61,6 +61,8 @@ struct Params {
     uint32_t stage_bytes;
     uint32_t full_off, empty_off, xf_off, xf_bytes, xsc_off, rstd_off, red_off, ssq_off;
     int* status;
+    unsigned* clear;     // words zeroed after the wait (see GemvOp)
+    int nclear;
 };
 
 __device__ __forceinline__ float act_fn(float g, int act) {
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_mma_kernel(const __g
 
     // ---------------- consumer warps ----------------
     pdl_wait_trigger();  // activations and residual come from the previous kernel
+    clear_words(p.clear, p.nclear, tid, nct);
 
     const int g = lane >> 2, t = lane & 3;
     const int jg = warp >> 1, eta = warp & 1;   // my half group inside every stage

@@ -62,6 +62,8 @@ struct GemvOp {
     int act;                              // pair mode: 0 SiLU, 1 GELU-tanh
     void* act_ws;                         // nullable: operand records of a 2..8-row call
     size_t act_ws_bytes;                  //   (gemv_rec_bytes); else the library's own array
+    unsigned* clear;                      // nullable: words set to zero after the wait (by CTA 0);
+    int nclear;                           //   the layer chain clears the next attention's counters
 };
 gem_status gemv_check(const GemvOp& op);
 gem_status gemv_enqueue(const GemvOp& op, cudaStream_t stream);
@@ -133,6 +135,9 @@ struct RopeFreq {
     double w[kMaxHeadDim / 2];
 };
 size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window);
+// Byte offset (in the attention workspace) and size of the flash kernel's arrival counters;
+// *bytes = 0 when the plan has none.  The counters are zero between calls.
+size_t attn_counter_offset(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window, size_t* bytes);
 gem_status attn_check(const AttnOp& op);
 gem_status attn_enqueue(const AttnOp& op, cudaStream_t stream);
 // Same, for use right after the RoPE/append kernel of a layer step: positions and the

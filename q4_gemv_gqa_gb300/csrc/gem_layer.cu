@@ -151,6 +151,15 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
         attn.k_out = k_cache;
         attn.v_out = v_cache;
     }
+    if (fused) {   // the QKV projection clears the attention's arrival counters for it
+        size_t cbytes = 0;
+        const size_t coff = attn_counter_offset(B, static_cast<int>(nq), static_cast<int>(nkv), static_cast<int>(d),
+                                                cache_cap, L->window, &cbytes);
+        if (cbytes) {
+            qkv.clear = reinterpret_cast<unsigned*>(static_cast<char*>(w.attn_ws) + coff);
+            qkv.nclear = static_cast<int>(cbytes / sizeof(unsigned));
+        }
+    }
     if ((st = gemv_check(qkv)) != GEM_OK || (st = gemv_check(oproj)) != GEM_OK ||
         (st = gemv_check(gateup)) != GEM_OK || (st = gemv_check(down)) != GEM_OK ||
         (st = rope_check(rope)) != GEM_OK || (st = attn_check(attn)) != GEM_OK)

@@ -79,7 +79,7 @@ def test_gemv_fused_rejects_pair_with_residual(env):
 ATTN_FUSED_CASES = [
     # (n_q, n_kv, d, rope_dim, theta, v_mode, window, positions, cap, scale)
     (4, 2, 64, 64, 1e6, 0, 0, [128], 129, 0.125),                        # one launch
-    (16, 8, 128, 128, 1e6, 0, 0, [4096], 4097, 128 ** -0.5),             # one launch, cluster merge
+    (16, 8, 128, 128, 1e6, 0, 0, [4096], 4097, 128 ** -0.5),             # one launch, splits merged by the last to finish
     (32, 8, 128, 128, 1e6, 0, 0, [2048, 0, 17, 700], 2049, 128 ** -0.5),  # ragged batch
     (8, 2, 128, 32, 1e6, 1, 0, [300], 301, 1.0),                         # V from K, partial RoPE
     (32, 16, 256, 256, 1e4, 0, 64, [200, 30], 64, 1.0),                  # ring

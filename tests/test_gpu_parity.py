@@ -353,13 +353,37 @@ def test_attention_deterministic_repeat_flash(gem, torch_mod):
     vc = _half_cache(t, gem_synth.normal_f16_bits(11, 3, (1, n_kv, cap, d)))
     pos = _cu(t, np.array([cap - 1], np.int32))
     need = gem.gqa_decode_attn_workspace(1, n_q, n_kv, d, cap, 0)
-    ws = t.empty(max(need, 1), dtype=t.uint8, device="cuda")
-    o1 = t.empty((1, n_q * d), device="cuda")
-    o2 = t.empty((1, n_q * d), device="cuda")
-    gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o1, ws if need else None)
-    gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o2, ws if need else None)
+    # the workspace starts as garbage: the call clears the split arrival counters itself
+    ws = t.full((max(need, 1),), 0xFF, dtype=t.uint8, device="cuda")
+    outs = [t.empty((1, n_q * d), device="cuda") for _ in range(10)]
+    for o in outs:   # which split merges varies from call to call; the result must not
+        gem.gqa_decode_attn(q, kc, vc, n_q, n_kv, d, pos, 0, 1.0, o, ws if need else None)
     t.cuda.synchronize()
-    assert t.equal(o1, o2)
+    for o in outs[1:]:
+        assert t.equal(outs[0], o)
+    ref = oracle.gqa_attention(q.cpu().numpy().reshape(n_q, d), _bits(kc)[0], _bits(vc)[0], cap - 1, 0, 1.0)
+    assert_close(outs[0].cpu().numpy()[0], ref.reshape(-1), "attention after a garbage workspace")
+
+
+def test_decode_layer_workspace_may_start_as_garbage(gem, torch_mod):
+    """The layer chain's QKV projection clears the attention's arrival counters, so a layer
+    workspace that starts as arbitrary bytes gives the same result as a zeroed one."""
+    t = torch_mod
+    shape, B, pos_l = configs.QWEN3_1_7B, 1, [1024]
+    pos = np.array(pos_l, np.int32)
+    cap = 1025
+    tens = configs.layer_tensors(shape, B, cap, 3, 0)
+    x = gem_synth.normal_f32(3, gem_synth.tid(0, gem_synth.ROLE_X), (B, shape.H))
+    dl = gem.DeviceLayer(shape, tens)
+    outs = []
+    for fill in (0, 0xFF, 0x01):
+        dx = _cu(t, x)
+        dk, dv = _half_cache(t, tens.k_cache), _half_cache(t, tens.v_cache)
+        ws = t.full((gem.decode_layer_workspace(dl, B, cap),), fill, dtype=t.uint8, device="cuda")
+        gem.decode_layer(dl, dx, dk, dv, _cu(t, pos), ws)
+        outs.append(dx)
+    t.cuda.synchronize()
+    assert t.equal(outs[0], outs[1]) and t.equal(outs[0], outs[2])
 
 
 def test_attention_needs_workspace(gem, torch_mod):

@@ -118,6 +118,29 @@ def q4_0_matrix(seed: int, tid: int, n_rows: int, k: int,
     return out.reshape(n_rows, (k // Q4_0_BLOCK_ELEMS) * Q4_0_BLOCK_BYTES)
 
 
+Q8_0_BLOCK_BYTES = 34
+
+
+def q8_0_matrix(seed: int, tid: int, n_rows: int, k: int,
+                scale_lo: float = 0.0002, scale_hi: float = 0.002) -> np.ndarray:
+    """Random Q8_0 matrix bytes, shape (n_rows, k // 32 * 34), uint8.
+
+    Each block's 32 code bytes come from four u64 draws (every code uniform on the 256
+    int8 values); its scale is uniform on [scale_lo, scale_hi] rounded to binary16 and
+    stored little-endian in the block's first two bytes.
+    """
+    if k % Q4_0_BLOCK_ELEMS:
+        raise ValueError("k must be a multiple of 32")
+    nb = n_rows * (k // Q4_0_BLOCK_ELEMS)
+    out = np.empty((nb, Q8_0_BLOCK_BYTES), dtype=np.uint8)
+    payload = draws(seed, tid, 4 * nb)                       # 32 bytes per block
+    out[:, 2:] = payload.view(np.uint8).reshape(nb, 32)
+    u = draws(seed, tid, nb, start=4 * nb)
+    sc = scale_lo + (scale_hi - scale_lo) * ((u >> np.uint64(11)).astype(np.float64) * (2.0 ** -53))
+    out[:, 0:2] = sc.astype(np.float16).view(np.uint8).reshape(nb, 2)
+    return out.reshape(n_rows, (k // Q4_0_BLOCK_ELEMS) * Q8_0_BLOCK_BYTES)
+
+
 def norm_weight(seed: int, tid: int, n: int) -> np.ndarray:
     """RMSNorm weight ~ 1 + N(0, 0.1), fp32."""
     return normal_f32(seed, tid, (n,), mean=1.0, std=0.1)

@@ -36,6 +36,7 @@ class LayerShape:
     v_from_k: bool    # V = unweighted RMSNorm of the K projection (no V rows)
     post_norms: bool  # RMSNorm of attention / FFN outputs before the residual adds
     eps: float = 1e-6
+    compact_kv: bool = False   # full-attention layer whose cache keeps the V rows only
 
     @property
     def n_qkv(self) -> int:
@@ -69,6 +70,10 @@ GEMMA31_FULL = LayerShape(H=5376, n_q=32, n_kv=4, d=512, F=21504, theta=1e6, rop
                           v_from_k=True, post_norms=True)
 
 
+# The same full-attention layer with the compact cache (V rows only; K rebuilt from V).
+GEMMA31_FULL_COMPACT = replace(GEMMA31_FULL, compact_kv=True)
+
+
 def _cap(shape: LayerShape, pos: int) -> int:
     return shape.window if shape.window else pos + 1
 
@@ -85,6 +90,9 @@ def workload(name: str) -> Workload:
         pos, B = 2048, 8
     elif name == "gemma4-31b-group":
         layers = (GEMMA31_SWA,) * 5 + (GEMMA31_FULL,)
+        pos, B = 32768, 1
+    elif name == "gemma4-31b-group-compact":
+        layers = (GEMMA31_SWA,) * 5 + (GEMMA31_FULL_COMPACT,)
         pos, B = 32768, 1
     else:
         raise KeyError(name)

@@ -44,7 +44,7 @@ class Layer(C.Structure):
                 ("w_up", C.c_void_p), ("w_down", C.c_void_p),
                 ("g_attn", C.c_void_p), ("g_ffn", C.c_void_p), ("g_q", C.c_void_p),
                 ("g_k", C.c_void_p), ("g_post_attn", C.c_void_p),
-                ("g_post_ffn", C.c_void_p)]
+                ("g_post_ffn", C.c_void_p), ("compact_kv", C.c_int)]
 
 
 def lib():
@@ -81,6 +81,13 @@ def lib():
             L.gem_oracle_other_half_via_f32.argtypes = [C.c_double]
             L.gem_oracle_argmax.restype = C.c_int64
             L.gem_oracle_argmax.argtypes = [p, C.c_int64]
+            L.gem_oracle_q8_0_dequant.argtypes = [p, C.c_int64, C.c_int64, p]
+            L.gem_oracle_gqa_attention_compact.restype = C.c_int
+            L.gem_oracle_gqa_attention_compact.argtypes = [p, p, p, C.c_int, C.c_int, C.c_int, C.c_int64,
+                                                           C.c_int64, C.c_int, C.c_double, C.c_double, p]
+            L.gem_oracle_q8_0_gemv_f64.restype = C.c_int
+            L.gem_oracle_q8_0_gemv_f64.argtypes = [p, C.c_int64, C.c_int64, p, C.c_int64, C.c_int, p,
+                                                   C.c_int64]
             L.gem_oracle_num_threads.restype = C.c_int
             L.gem_oracle_set_num_threads.argtypes = [C.c_int]
             _lib = L
@@ -168,12 +175,48 @@ def gqa_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, pos: 
     return (out, probs) if return_probs else out
 
 
+def gqa_attention_compact(q: np.ndarray, v_cache: np.ndarray, gamma_k: np.ndarray | None, pos: int,
+                          rope_dim: int, theta: float, scale: float) -> np.ndarray:
+    """One sequence over a compact full-attention cache (V rows only, binary16 bits
+    [n_kv, cap, d]): K_j = RoPE_j(V_j * gamma_k) rebuilt in fp64.  q [n_q, d] rotated at pos."""
+    q = _c(q, np.float64)
+    vc = _c(v_cache, np.uint16)
+    g = _c(gamma_k, np.float32)
+    n_q, d = q.shape
+    n_kv, cap, _ = vc.shape
+    out = np.empty((n_q, d), dtype=np.float64)
+    rc = lib().gem_oracle_gqa_attention_compact(_ptr(q), _ptr(vc), _ptr(g), n_q, n_kv, d, cap, pos,
+                                                rope_dim, theta, scale, _ptr(out))
+    if rc:
+        raise ValueError("oracle compact attention rejected arguments (rc=%d)" % rc)
+    return out
+
+
 def silu(g: float) -> float:
     return lib().gem_oracle_silu(float(g))
 
 
 def gelu_tanh(g: float) -> float:
     return lib().gem_oracle_gelu_tanh(float(g))
+
+
+def q8_0_dequant(W: np.ndarray, N: int, K: int) -> np.ndarray:
+    W = _c(W, np.uint8)
+    out = np.empty((N, K), dtype=np.float64)
+    lib().gem_oracle_q8_0_dequant(_ptr(W), N, K, _ptr(out))
+    return out
+
+
+def q8_0_gemv(W: np.ndarray, N: int, K: int, x: np.ndarray) -> np.ndarray:
+    """y[b] = deq(W) @ x[b] in fp64 (Q8_0 rows).  x: [B, K]."""
+    W = _c(W, np.uint8)
+    x = _c(np.atleast_2d(x), np.float64)
+    B = x.shape[0]
+    y = np.empty((B, N), dtype=np.float64)
+    rc = lib().gem_oracle_q8_0_gemv_f64(_ptr(W), N, K, _ptr(x), K, B, _ptr(y), N)
+    if rc:
+        raise ValueError("oracle Q8_0 gemv rejected arguments (rc=%d)" % rc)
+    return y
 
 
 def argmax(v: np.ndarray) -> int:
@@ -206,7 +249,8 @@ def make_layer(shape, t) -> tuple:
               g_q=keep[7].ctypes.data if keep[7] is not None else None,
               g_k=keep[8].ctypes.data if keep[8] is not None else None,
               g_post_attn=keep[9].ctypes.data if keep[9] is not None else None,
-              g_post_ffn=keep[10].ctypes.data if keep[10] is not None else None)
+              g_post_ffn=keep[10].ctypes.data if keep[10] is not None else None,
+              compact_kv=int(getattr(shape, "compact_kv", False)))
     return L, keep
 
 
@@ -219,8 +263,8 @@ def decode_layer(shape, tensors, x: np.ndarray, pos: np.ndarray, k_cache: np.nda
     flip (int8 [B, 2, n_kv, d]) selects the other binary16 neighbour for those elements."""
     L, keep = make_layer(shape, tensors)
     B = x.shape[0]
-    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
-    cap = k_cache.shape[2]
+    assert (k_cache is None or k_cache.flags.c_contiguous) and v_cache.flags.c_contiguous
+    cap = v_cache.shape[2]
     pos = _c(pos, np.int32)
     out = np.empty((B, shape.H), dtype=np.float64)
     qkv = np.empty((B, shape.n_qkv), dtype=np.float64) if stages else None

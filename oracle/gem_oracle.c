@@ -149,6 +149,50 @@ int gem_oracle_q4_0_gemv_f32(const uint8_t *W, int64_t N, int64_t K, const float
     return rc;
 }
 
+/* ---- Q8_0 --------------------------------------------------------------------------
+ * [GEM] "Verified model facts": the published layout keeps the token embedding (tied with
+ * the output projection) as Q8_0.  A block is a 34-byte record: binary16 scale d (little
+ * endian), then 32 signed 8-bit codes q (two's complement); weight j = q[j] * d.  Reading
+ * (the pages name the type only): the GGML Q8_0 record, element j in byte 2 + j.
+ */
+static inline const uint8_t *q8_block(const uint8_t *W, int64_t K, int64_t n, int64_t b)
+{
+    return W + (n * (K / 32) + b) * 34;
+}
+
+void gem_oracle_q8_0_dequant(const uint8_t *W, int64_t N, int64_t K, double *out)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const uint8_t *blk = q8_block(W, K, n, b);
+            double d = gem_oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+            for (int j = 0; j < 32; ++j)
+                out[n * K + 32 * b + j] = (double)(int8_t)blk[2 + j] * d;
+        }
+}
+
+/* y[b][n] = sum_k deq(W)[n][k] * x[b][k], k in order, fp64. */
+int gem_oracle_q8_0_gemv_f64(const uint8_t *W, int64_t N, int64_t K, const double *x,
+                             int64_t ldx, int B, double *y, int64_t ldy)
+{
+    if (K % 32 || N < 0 || B < 0)
+        return 1;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int64_t n = 0; n < N; ++n) {
+            const double *xb = x + b * ldx;
+            double acc = 0.0;
+            for (int64_t blk = 0; blk < K / 32; ++blk) {
+                const uint8_t *p = q8_block(W, K, n, blk);
+                double d = gem_oracle_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
+                for (int j = 0; j < 32; ++j)
+                    acc += (double)(int8_t)p[2 + j] * d * xb[32 * blk + j];
+            }
+            y[b * ldy + n] = acc;
+        }
+    return 0;
+}
+
 /* ---- RMSNorm -----------------------------------------------------------------------
  * [GEM] "weighted RMSNorm over one or many heads"; [GELO] 05 apply_qk_norm.
  * Readings: eps is a caller parameter (1e-6 in the workloads); gamma multiplies as
@@ -246,6 +290,75 @@ int gem_oracle_gqa_attention(const double *q, const uint16_t *k_cache,
     return rc;
 }
 
+/* ---- Compact full-attention cache ---------------------------------------------------------
+ * [GEM] "Verified model facts": on a full-attention layer (V = unweighted RMSNorm of the K
+ * projection, K = key_norm-weighted RMSNorm of it, then RoPE) the cache can hold the V row
+ * alone; the historical K row is rebuilt inside the attention as V * key_norm.  Reading (the
+ * pages leave the rotation implicit): the rebuilt row is rotated at the row's own position,
+ *   K_j = RoPE_j(V16_j * gamma_k),
+ * evaluated in fp64 from the binary16 V row, since the standard cache stores the rotated K.
+ * Full attention only: slot j holds position j.  q: [n_q][d] (already normalised and rotated
+ * at pos); out: [n_q][d].
+ */
+int gem_oracle_gqa_attention_compact(const double *q, const uint16_t *v_cache, const float *gamma_k,
+                                     int n_q, int n_kv, int d, int64_t cap, int64_t pos,
+                                     int rope_dim, double theta, double scale, double *out)
+{
+    if (n_kv <= 0 || n_q % n_kv || pos < 0 || pos >= cap || rope_dim < 0 || rope_dim > d ||
+        (rope_dim & 1))
+        return 1;
+    const int64_t T = pos + 1;
+    const int G = n_q / n_kv;
+    int rc = 0;
+#pragma omp parallel for schedule(static)
+    for (int g = 0; g < n_kv; ++g) {
+        double *s = malloc(sizeof(double) * (size_t)T * (size_t)G);
+        double *k = malloc(sizeof(double) * (size_t)d);
+        if (!s || !k) {
+            free(s);
+            free(k);
+            rc = 3;
+            continue;
+        }
+        const uint16_t *vg = v_cache + (int64_t)g * cap * d;
+        for (int64_t j = 0; j < T; ++j) {   /* rebuild K_j, then every head's score */
+            for (int i = 0; i < d; ++i)
+                k[i] = gem_oracle_half_to_double(vg[j * d + i]) * (gamma_k ? (double)gamma_k[i] : 1.0);
+            gem_oracle_rope_neox(k, d, rope_dim, (double)j, theta);
+            for (int hh = 0; hh < G; ++hh) {
+                const double *qh = q + (int64_t)(g * G + hh) * d;
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i)
+                    acc += qh[i] * k[i];
+                s[hh * T + j] = scale * acc;
+            }
+        }
+        for (int hh = 0; hh < G; ++hh) {
+            double *sh = s + hh * T;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < T; ++j)
+                if (sh[j] > m)
+                    m = sh[j];
+            double den = 0.0;
+            for (int64_t j = 0; j < T; ++j) {
+                sh[j] = exp(sh[j] - m);
+                den += sh[j];
+            }
+            double *oh = out + (int64_t)(g * G + hh) * d;
+            for (int i = 0; i < d; ++i)
+                oh[i] = 0.0;
+            for (int64_t j = 0; j < T; ++j) {
+                const double w = sh[j] / den;
+                for (int i = 0; i < d; ++i)
+                    oh[i] += w * gem_oracle_half_to_double(vg[j * d + i]);
+            }
+        }
+        free(s);
+        free(k);
+    }
+    return rc;
+}
+
 /* ---- FFN activations --------------------------------------------------------------------
  * [GELO] 04/05: Qwen3 SwiGLU, silu(g) = g / (1 + e^-g).  [GELO] 04 (Gemma):
  * gelu_pytorch_tanh, 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
@@ -293,7 +406,7 @@ int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x
     for (int b = 0; b < B; ++b) {
         const double *x = x_in + (int64_t)b * H;
         int64_t p = pos[b];
-        uint16_t *kc = k_cache + (int64_t)b * nkv * cap * d;
+        uint16_t *kc = k_cache ? k_cache + (int64_t)b * nkv * cap * d : NULL;
         uint16_t *vc = v_cache + (int64_t)b * nkv * cap * d;
         /* a1 pre-attention RMSNorm, a2 QKV projection */
         gem_oracle_rmsnorm(x, H, L->g_attn, L->eps, xn);
@@ -326,9 +439,10 @@ int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x
             if (!L->v_from_k)
                 memcpy(qkv_out + (int64_t)b * nqkv + qdim + kdim, vrow, sizeof(double) * kdim);
         }
-        /* a5 KV append at the new token's slot, rounded to binary16 via binary32 */
+        /* a5 KV append at the new token's slot, rounded to binary16 via binary32 (a compact
+         * cache keeps the V row only) */
         int64_t slot = L->window ? p % L->window : p;
-        if (slot >= cap || p < 0) {
+        if (slot >= cap || p < 0 || (L->compact_kv && (L->window || !L->v_from_k))) {
             rc = 2;
             goto done;
         }
@@ -336,9 +450,10 @@ int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x
             for (int64_t i = 0; i < d; ++i) {
                 const int64_t fk = (((int64_t)b * 2 + 0) * nkv + j) * d + i;
                 const int64_t fv = (((int64_t)b * 2 + 1) * nkv + j) * d + i;
-                kc[(j * cap + slot) * d + i] = (flip && flip[fk])
-                    ? gem_oracle_other_half_via_f32(k[j * d + i])
-                    : gem_oracle_double_to_half_via_f32(k[j * d + i]);
+                if (!L->compact_kv)
+                    kc[(j * cap + slot) * d + i] = (flip && flip[fk])
+                        ? gem_oracle_other_half_via_f32(k[j * d + i])
+                        : gem_oracle_double_to_half_via_f32(k[j * d + i]);
                 vc[(j * cap + slot) * d + i] = (flip && flip[fv])
                     ? gem_oracle_other_half_via_f32(vrow[j * d + i])
                     : gem_oracle_double_to_half_via_f32(vrow[j * d + i]);
@@ -348,8 +463,12 @@ int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x
                 }
             }
         /* a6 attention */
-        rc = gem_oracle_gqa_attention(q, kc, vc, (int)nq, (int)nkv, (int)d, cap, p,
-                                      L->window, L->scale, att, NULL);
+        if (L->compact_kv)
+            rc = gem_oracle_gqa_attention_compact(q, vc, L->g_k, (int)nq, (int)nkv, (int)d, cap, p,
+                                                  L->rope_dim, L->theta, L->scale, att);
+        else
+            rc = gem_oracle_gqa_attention(q, kc, vc, (int)nq, (int)nkv, (int)d, cap, p,
+                                          L->window, L->scale, att, NULL);
         if (rc)
             goto done;
         if (attn_out)
@@ -415,14 +534,16 @@ int gem_oracle_decode_layer(const gem_oracle_layer *L, int B, const float *x_in,
     return rc;
 }
 
-/* [GEM] sampler note: equal logits are broken by token id (lowest wins). */
+/* [GEM] sampler note: equal logits are broken by token id (lowest wins).  Reading for
+ * entries that are not numbers (the pages do not say): a NaN is never chosen; all NaN
+ * (or n == 0) gives 0. */
 int64_t gem_oracle_argmax(const double *v, int64_t n)
 {
-    int64_t best = 0;
-    for (int64_t i = 1; i < n; ++i)
-        if (v[i] > v[best])
+    int64_t best = -1;
+    for (int64_t i = 0; i < n; ++i)
+        if (!isnan(v[i]) && (best < 0 || v[i] > v[best]))
             best = i;
-    return best;
+    return best < 0 ? 0 : best;
 }
 
 int gem_oracle_num_threads(void)

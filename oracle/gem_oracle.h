@@ -71,6 +71,8 @@ typedef struct {
     int qk_norm, v_from_k, post_norms;
     const uint8_t *w_qkv, *w_o, *w_gate, *w_up, *w_down;
     const float *g_attn, *g_ffn, *g_q, *g_k, *g_post_attn, *g_post_ffn;
+    int compact_kv; /* full-attention layer with V from K: the cache keeps V only (k_cache may be
+                       NULL); attention rebuilds K_j = RoPE_j(V_j * g_k) */
 } gem_oracle_layer;
 
 /* x_in: [B][H] fp32; caches: [B][n_kv][cap][d] binary16 (the new row is written);
@@ -105,8 +107,19 @@ int gem_oracle_decode_layer_ex(const gem_oracle_layer *L, int B, const double *x
  * (equal to the RNE code when fp32(v) is exactly representable). */
 uint16_t gem_oracle_other_half_via_f32(double v);
 
+/* Attention over a compact full-attention cache (V rows only): K_j = RoPE_j(V16_j * gamma_k)
+ * rebuilt in fp64, then softmax(scale q.K) V as gem_oracle_gqa_attention (window 0). */
+int gem_oracle_gqa_attention_compact(const double *q, const uint16_t *v_cache, const float *gamma_k,
+                                     int n_q, int n_kv, int d, int64_t cap, int64_t pos,
+                                     int rope_dim, double theta, double scale, double *out);
+
 /* Index of the largest value; ties go to the lowest index. */
 int64_t gem_oracle_argmax(const double *v, int64_t n);
+
+/* Q8_0: 34-byte blocks (binary16 scale, 32 int8 codes), weight = q * d. */
+void gem_oracle_q8_0_dequant(const uint8_t *W, int64_t N, int64_t K, double *out);
+int gem_oracle_q8_0_gemv_f64(const uint8_t *W, int64_t N, int64_t K, const double *x,
+                             int64_t ldx, int B, double *y, int64_t ldy);
 
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
 int gem_oracle_num_threads(void);

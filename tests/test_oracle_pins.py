@@ -469,3 +469,120 @@ def test_layer_flip_changes_only_the_flipped_code():
     assert diff.sum() == 1 and diff[0, 1, w.pos, 5]
     assert vc2[0, 1, w.pos, 5] == oracle.other_half_via_f32(kvn[0, 1, 1, 5])
     assert not np.array_equal(out0, out1)
+
+
+# ---- Q8_0 block format (tied embedding / logit projection) ------------------------------
+
+def _q8_block(scale_bits: int, qs: bytes) -> np.ndarray:
+    assert len(qs) == 32
+    return np.frombuffer(bytes([scale_bits & 0xFF, scale_bits >> 8]) + qs, dtype=np.uint8).reshape(1, 34)
+
+
+def test_q8_0_hand_built_blocks():
+    g = json.load(open(os.path.join(GOLDEN, "q8_0_blocks.json")))
+    for blk in g["blocks"]:
+        W = _q8_block(int(blk["scale_bits"], 16), bytes.fromhex(blk["qs"]))
+        got = oracle.q8_0_dequant(W, 1, 32)[0]
+        assert np.array_equal(got, np.array(blk["expect"], dtype=np.float64)), blk["name"]
+
+
+@pytest.mark.parametrize("j", [0, 1, 15, 16, 30, 31])
+def test_q8_0_element_order_one_hot(j):
+    qs = bytearray(32)
+    qs[j] = 0xFD   # -3
+    W = _q8_block(0x3400, bytes(qs))   # d = 0.25
+    expect = np.zeros(32)
+    expect[j] = -0.75
+    assert np.array_equal(oracle.q8_0_dequant(W, 1, 32)[0], expect)
+
+
+def test_q8_0_gemv_equals_dense_matmul_on_independently_decoded_weights():
+    # the test decodes the blocks itself from the format definition (numpy binary16 and int8
+    # views), then compares the oracle GEMV with a plain fp64 matmul
+    N, K, B = 7, 96, 3
+    W = gem_synth.q8_0_matrix(5, 9, N, K)
+    blocks = W.reshape(N, K // 32, 34)
+    d = blocks[:, :, 0:2].copy().view(np.float16).astype(np.float64)[:, :, 0]
+    q = blocks[:, :, 2:].view(np.int8).astype(np.float64)
+    dense = (q * d[:, :, None]).reshape(N, K)
+    x = gem_synth.normal(5, 10, B * K).reshape(B, K)
+    got = oracle.q8_0_gemv(W, N, K, x)
+    assert np.allclose(got, x @ dense.T, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(oracle.q8_0_dequant(W, N, K), dense)
+
+
+def test_argmax_ignores_nan():
+    nan = float("nan")
+    assert oracle.argmax(np.array([nan, 1.0, 2.0, 2.0])) == 2
+    assert oracle.argmax(np.array([nan, nan])) == 0
+    assert oracle.argmax(np.array([-np.inf, -5.0])) == 1
+
+
+# ---- compact full-attention cache: K rebuilt from V ----------------------------------------
+
+def _np_rope(v, R, pos, theta):
+    """NeoX rotation of the first R dims by pos * theta^(-2i/R), written out with numpy."""
+    out = v.copy()
+    half = R // 2
+    i = np.arange(half)
+    ang = pos * theta ** (-2.0 * i / R)
+    c, s = np.cos(ang), np.sin(ang)
+    out[:half] = v[:half] * c - v[half:R] * s
+    out[half:R] = v[:half] * s + v[half:R] * c
+    return out
+
+
+def test_compact_attention_equals_brute_force_over_rebuilt_keys():
+    n_q, n_kv, d, R, theta, pos, cap = 4, 2, 16, 8, 1e4, 9, 12
+    G = n_q // n_kv
+    v16 = gem_synth.normal_f16_bits(41, 1, (n_kv, cap, d))
+    gamma = gem_synth.norm_weight(41, 2, d)
+    q = gem_synth.normal(41, 3, n_q * d).reshape(n_q, d)
+    scale = 0.25
+    got = oracle.gqa_attention_compact(q, v16, gamma, pos, R, theta, scale)
+    vals = v16.view(np.float16).astype(np.float64)
+    ref = np.empty((n_q, d))
+    for h in range(n_q):
+        g = h // G
+        K = np.stack([_np_rope(vals[g, j] * gamma.astype(np.float64), R, j, theta) for j in range(pos + 1)])
+        sc = scale * (K @ q[h])
+        w = np.exp(sc - sc.max())
+        w /= w.sum()
+        ref[h] = w @ vals[g, :pos + 1]
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_compact_attention_without_rotation_or_weight_is_attention_with_k_equal_v():
+    n_q, n_kv, d, pos, cap = 6, 3, 32, 20, 24
+    v16 = gem_synth.normal_f16_bits(42, 1, (n_kv, cap, d))
+    q = gem_synth.normal(42, 2, n_q * d).reshape(n_q, d)
+    got = oracle.gqa_attention_compact(q, v16, None, pos, 0, 1e6, 0.125)
+    ref = oracle.gqa_attention(q, v16, v16, pos, 0, 0.125)
+    assert np.array_equal(got, ref)
+
+
+def test_compact_layer_appends_v_only_and_tracks_the_standard_layer():
+    """A compact full-attention layer writes the same V row as the standard one, leaves no K
+    cache, and differs from the standard layer only by the binary16 rounding of the cached K
+    rows (which the compact layer rebuilds from V instead)."""
+    from dataclasses import replace
+    shape = replace(configs.GEMMA31_FULL, H=512, n_q=8, n_kv=2, d=64, F=1024, rope_dim=16)
+    compact = replace(shape, compact_kv=True)
+    B, cap, pos = 1, 40, np.array([37], np.int32)
+    tens = configs.layer_tensors(shape, B, cap, 43, 0)
+    x = configs.layer_input(shape.H, B, 43)
+    # a cache consistent with the compact layout: K rows rounded from the rebuilt keys
+    v = tens.v_cache
+    k = np.empty_like(v)
+    for g in range(shape.n_kv):
+        for j in range(cap):
+            kk = _np_rope(v[0, g, j].view(np.float16).astype(np.float64) * tens.g_k.astype(np.float64),
+                          shape.rope_dim, j, shape.theta)
+            k[0, g, j] = kk.astype(np.float32).astype(np.float16).view(np.uint16)
+    vs, ks = v.copy(), k.copy()
+    ref = oracle.decode_layer(shape, tens, x, pos, ks, vs)
+    vc = v.copy()
+    got = oracle.decode_layer(compact, tens, x, pos, None, vc)
+    assert np.array_equal(vc, vs)                   # same appended V row, nothing else touched
+    assert np.allclose(got, ref, rtol=1e-3, atol=1e-3)
+    assert not np.array_equal(got, ref)             # the K rows really are rebuilt, not read

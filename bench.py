@@ -57,14 +57,16 @@ def layer_bytes(shape, B: int, T: int) -> dict:
     """Algorithmic bytes of one layer step: every byte the method must move once."""
     w = (q4_bytes(shape.n_qkv, shape.H) + q4_bytes(shape.H, shape.n_q * shape.d) + 2 * q4_bytes(shape.F, shape.H)
          + q4_bytes(shape.H, shape.F))
-    kv = B * shape.n_kv * T * shape.d * 2 * 2
-    kv_write = B * shape.n_kv * shape.d * 2 * 2
+    rows = 1 if getattr(shape, "compact_kv", False) else 2   # a compact cache keeps V rows only
+    kv = B * shape.n_kv * T * shape.d * 2 * rows
+    kv_write = B * shape.n_kv * shape.d * 2 * rows
     act = 4 * B * (2 * shape.H + shape.n_qkv * 2 + 2 * shape.n_q * shape.d + 3 * shape.F + 4 * shape.H)
     return {"weights": w, "kv": kv + kv_write, "act": act, "total": w + kv + kv_write + act}
 
 
 def attn_bytes(shape, B, T):
-    return B * shape.n_kv * T * shape.d * 2 * 2 + 4 * B * 2 * shape.n_q * shape.d
+    rows = 1 if getattr(shape, "compact_kv", False) else 2
+    return B * shape.n_kv * T * shape.d * 2 * rows + 4 * B * 2 * shape.n_q * shape.d
 
 
 def gemv_bytes(N, K, B, nmat=1):
@@ -232,14 +234,14 @@ class Model:
                 tens = configs.layer_weights(shape, seed, li)
                 dl = gem.DeviceLayer(shape, tens)
                 k, v = configs.kv_cache(shape, wl.B, cap, seed, li)
-                kc = torch.from_numpy(k.view(np.int16)).cuda()
+                kc = None if shape.compact_kv else torch.from_numpy(k.view(np.int16)).cuda()
                 vc = torch.from_numpy(v.view(np.int16)).cuda()
                 made.append((dl, kc, vc))
                 del tens, k, v
             else:
                 src, ks, vs = made[li % len(made)]
                 dl = gem.DeviceLayer.clone(src)
-                kc, vc = ks.clone(), vs.clone()
+                kc, vc = (None if ks is None else ks.clone()), vs.clone()
             self.layers.append(dl)
             self.kc.append(kc)
             self.vc.append(vc)
@@ -258,12 +260,16 @@ class Model:
     def launches_per_step(self):
         n = 0
         for s, cap in zip(self.wl.layers, self.wl.cache_cap):
-            fused = s.d <= 256 and s.n_q // s.n_kv <= 4   # QK-norm/RoPE/append inside attention
+            # QK-norm/RoPE/append inside attention (never for a compact cache)
+            fused = s.d <= 256 and s.n_q // s.n_kv <= 4 and not s.compact_kv
             n += (5 if fused else 6) + (2 if s.post_norms else 0)
             if self.B >= 2:
                 n += 4   # one activation prep launch per GEMV
-            if self.gem.gqa_decode_attn_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.window) > 0:
-                n += 1
+            if s.compact_kv:
+                split = self.gem.gqa_decode_attn_compact_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.rope_dim) > 0
+            else:
+                split = self.gem.gqa_decode_attn_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.window) > 0
+            n += 1 if split else 0
         return n
 
 
@@ -367,7 +373,60 @@ def run_kernel_only(args):
     import q4_gemv_gqa_gb300 as gem
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     res = {"kernel": args.kernel}
-    if args.kernel == "gemv":
+    if args.kernel == "attn_full":
+        # the Gemma 4 31B full-attention layer's attention at 32,769 positions (--batch
+        # sequences) over two cache copies: --cache standard (K and V rows; QK-norm, RoPE and
+        # the append in the separate launch before it, as the layer chain runs it) or compact
+        # (V rows only, K rebuilt inside the attention)
+        s = configs.GEMMA31_FULL_COMPACT if args.cache == "compact" else configs.GEMMA31_FULL
+        B, P = args.batch, 32768
+        cap = P + 1
+        res["shape"] = {"n_q": s.n_q, "n_kv": s.n_kv, "d": s.d, "B": B, "positions": cap, "cache": args.cache}
+        qkv = torch.randn((B, s.n_qkv), device="cuda")
+        att = torch.empty((B, s.n_q * s.d), device="cuda")
+        pos = torch.full((B,), P, dtype=torch.int32, device="cuda")
+        gq = torch.ones(s.d, device="cuda")
+        gk = torch.ones(s.d, device="cuda")
+        caches = []
+        for i in range(2):
+            v = torch.from_numpy(gem_synth.normal_f16_bits(0, 8000 + i, (B, s.n_kv, cap, s.d)).view(np.int16)).cuda()
+            k = None if args.cache == "compact" else torch.from_numpy(
+                gem_synth.normal_f16_bits(0, 8100 + i, (B, s.n_kv, cap, s.d)).view(np.int16)).cuda()
+            caches.append((k, v))
+        if args.cache == "compact":
+            wsn = gem.gqa_decode_attn_compact_workspace(B, s.n_q, s.n_kv, s.d, cap, s.rope_dim)
+        else:
+            wsn = gem.gqa_decode_attn_workspace(B, s.n_q, s.n_kv, s.d, cap, 0)
+        wsa = torch.empty(max(1, wsn), dtype=torch.uint8, device="cuda")
+
+        def run():
+            for k, v in caches:
+                if args.cache == "compact":
+                    gem.rmsnorm_qknorm_rope(qkv, s.n_q, s.n_kv, s.d, gq, gk, 1, s.eps, pos, s.theta, s.rope_dim,
+                                            None, v)
+                    gem.gqa_decode_attn_compact(qkv, v, s.n_q, s.n_kv, s.d, pos, float(s.scale), gk, s.rope_dim,
+                                                s.theta, att, wsa if wsn else None)
+                else:
+                    gem.gqa_decode_attn_fused(qkv, s.n_q, s.n_kv, s.d, gq, gk, 1, s.eps, pos, s.theta, s.rope_dim,
+                                              k, v, 0, float(s.scale), att, wsa if wsn else None)
+        b = attn_bytes(s, B, cap)
+        n = len(caches)
+    elif args.kernel == "q8":
+        # the tied Q8_0 logit projection (--vocab x 5376) and the device argmax of its logits
+        B, V, Hl = args.batch, args.vocab, 5376
+        res["shape"] = {"V": V, "H": Hl, "B": B}
+        Wq = torch.from_numpy(gem_synth.q8_0_matrix(0, 7000, V, Hl)).cuda()
+        xq = torch.from_numpy(gem_synth.normal_f32(0, 7001, (B, Hl))).cuda()
+        yq = torch.empty((B, V), device="cuda")
+        iq = torch.empty((B,), dtype=torch.int32, device="cuda")
+        wsq = torch.empty(max(1, gem.argmax_workspace(B, V)), dtype=torch.uint8, device="cuda")
+
+        def run():
+            gem.q8_0_gemv(Wq, V, Hl, xq, yq)
+            gem.argmax(yq, iq, wsq)
+        b = V * (Hl // 32) * 34 + 4 * B * (Hl + V)
+        n = 1
+    elif args.kernel == "gemv":
         B = args.batch
         N, K = (21504, 5376) if args.gemv_shape == "up" else (5376, 21504)
         res["shape"] = {"N": N, "K": K, "B": B}
@@ -540,11 +599,33 @@ def run_gem(args):
     del W31
     torch.cuda.empty_cache()
 
+    # the tied Q8_0 logit projection at the Gemma-4-31B embedding shape (262,144 x 5,376, 1.5 GB)
+    # and the device argmax of its logits
+    logits = {}
+    V, Hl = 262144, 5376
+    Wq8 = torch.from_numpy(gem_synth.q8_0_matrix(0, 7000, V, Hl)).cuda()
+    for B in (1, 8):
+        xl = torch.from_numpy(gem_synth.normal_f32(0, 7001, (B, Hl))).cuda()
+        yl = torch.empty((B, V), device="cuda")
+        il = torch.empty((B,), dtype=torch.int32, device="cuda")
+        aws = torch.empty(max(1, gem.argmax_workspace(B, V)), dtype=torch.uint8, device="cuda")
+        gl = capture(torch, lambda xl=xl, yl=yl: gem.q8_0_gemv(Wq8, V, Hl, xl, yl))
+        us = time_graph(torch, gl, max(5, min(args.steps, 50))) * 1e3
+        ga = capture(torch, lambda yl=yl, il=il, aws=aws: gem.argmax(yl, il, aws))
+        us_a = time_graph(torch, ga, max(5, min(args.steps, 200))) * 1e3
+        b = V * (Hl // 32) * 34 + 4 * B * (Hl + V)
+        logits["b%d" % B] = {"us": round(us, 2), "gbs": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
+                             "argmax_us": round(us_a, 2)}
+        del gl, ga
+    del Wq8
+    torch.cuda.empty_cache()
+
     # the other workloads' steps
     subs = {}
     if not args.no_workloads and rank == 0:
         reps = max(10, min(args.steps, 100))
-        for name, distinct in (("qwen3-4b-b8", 4), ("gemma4-31b-group", 2), ("tiny", 1)):
+        for name, distinct in (("qwen3-4b-b8", 4), ("gemma4-31b-group", 2), ("gemma4-31b-group-compact", 2),
+                               ("tiny", 1)):
             if name == wl.name:
                 continue
             subs[name] = workload_record(gem, torch, name, reps, peak, distinct)
@@ -573,6 +654,7 @@ def run_gem(args):
                            "layers shaped like the first, CUDA graph, CUDA events" % len(idx),
             "persistent_step_kernel": persistent,
             "gemv_k5376_n21504": gemv31,
+            "logits_q8_0_k5376_v262144": logits,
             "workloads": subs,
             "e2e": {"value": round(sbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 4), "wall_ms_per_step": round(e2e_wall_ms, 4),
@@ -672,17 +754,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gem", "reference"], default="gem")
     ap.add_argument("--workload", default="qwen3-1.7b",
-                    choices=["tiny", "qwen3-1.7b", "qwen3-4b-b8", "gemma4-31b-group"])
+                    choices=["tiny", "qwen3-1.7b", "qwen3-4b-b8", "gemma4-31b-group", "gemma4-31b-group-compact"])
     ap.add_argument("--layers", type=int, default=0, help="use only the first n layers")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' sub-records")
-    ap.add_argument("--kernel", choices=["step", "gemv", "op"], default="step",
+    ap.add_argument("--vocab", type=int, default=262144, help="--kernel q8: vocabulary rows")
+    ap.add_argument("--kernel", choices=["step", "gemv", "op", "q8", "attn_full"], default="step",
                     help="time one op alone (for profiler captures) instead of the step")
     ap.add_argument("--op", default="gqa_decode_attn",
                     choices=["q4_0_gemv_qkv", "gqa_decode_attn", "q4_0_gemv_o", "q4_0_gemv_gate_up",
                              "q4_0_gemv_down"], help="--kernel op: which op of the layer step")
     ap.add_argument("--batch", type=int, default=1, help="--kernel gemv: activation rows")
     ap.add_argument("--mats", type=int, default=8, help="--kernel gemv: rotated matrices")
+    ap.add_argument("--cache", choices=["standard", "compact"], default="compact",
+                    help="--kernel attn_full: the full-attention layer's cache layout")
     ap.add_argument("--gemv-shape", choices=["up", "down"], default="up",
                     help="--kernel gemv: 31B FFN up (5376 -> 21504) or down (21504 -> 5376) projection")
     args = ap.parse_args()

@@ -167,6 +167,36 @@ GEM_API gem_status gem_q4_0_gemv_fused(const void *W0, const void *W1, int64_t N
                                        void *stream);
 
 /*
+ * Q8_0 dequantise-and-matvec: the tied token embedding / output (logit) projection.
+ * [GEM] "Verified model facts" (the published layout keeps the tied embedding as Q8_0) and
+ * "Native Metal diagnostic: buffer ownership" (the Q8 logit matvec, one token, and the
+ * fixed-eight-row form for a verifier at the 5,376 x 262,144 shape).
+ *
+ *   y[b][n] = sum_{k<K} (q[n][k] * d[n][k/32]) * x[b][k]
+ *
+ *   W   N rows of K/32 blocks of 34 bytes: binary16 scale d (little endian), then 32 int8
+ *       codes q (element j of the block in byte 2 + j); 16-byte aligned (GEM_ERR_MISALIGNED).
+ *   K   a multiple of 256 (GEM_ERR_UNSUPPORTED_SHAPE otherwise); B in 0..8.
+ *   x   [B][ldx] fp32, ldx >= K, 16-byte aligned with ldx % 4 == 0 (GEM_ERR_MISALIGNED);
+ *   y   [B][ldy] fp32, ldy >= N.  Accumulation is fp32.
+ */
+GEM_API gem_status gem_q8_0_gemv(const void *W, int64_t N, int64_t K, const float *x, int64_t ldx,
+                                 int B, float *y, int64_t ldy, void *stream);
+
+/*
+ * Index of the largest value of each row: idx[b] = argmax_n y[b][n] (the next token of greedy
+ * decoding).  [GEM] sampler note: equal logits go to the lowest token id.  Reading where the
+ * pages are silent: a NaN is never chosen; a row of only NaN gives 0.
+ *   y    [B][ldy] fp32 (ldy >= N, N < 2^31);  idx  [B] int32 device.
+ *   workspace  gem_argmax_workspace(B, N) bytes, 256-byte aligned, contents need no
+ *        initialisation (the call clears its arrival counters with a memset on the stream).
+ *   Deterministic: chunk maxima are combined under a total order (value, then index).
+ */
+GEM_API size_t gem_argmax_workspace(int B, int64_t N);
+GEM_API gem_status gem_argmax(const float *y, int64_t ldy, int B, int64_t N, int32_t *idx,
+                              void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Weighted RMSNorm  [GEM] "weighted RMSNorm over one or many heads"; [GELO] 06 pre-norm.
  *   out[b][i] = x[b][i] / sqrt(mean_i x[b][i]^2 + eps) * gamma[i]   (gamma NULL: 1)
  * x, out: [B][H] fp32 (may alias).
@@ -191,6 +221,8 @@ GEM_API gem_status gem_rmsnorm(const float *x, int B, int64_t H, const float *ga
  *            nearest even, at slot p (window == 0) or p mod window (window > 0, a ring of
  *            `window` slots; requires window <= cache_cap).  Q and K in qkv are replaced by
  *            their normalised, rotated fp32 values.
+ *            v_mode 1 with k_cache NULL appends the V row only (a compact cache, see
+ *            gem_gqa_decode_attn_compact); K in qkv is still normalised and rotated.
  *   status   nullable device int32: receives GEM_DEVFLAG_POS_RANGE for a bad pos[b].
  */
 GEM_API gem_status gem_rmsnorm_qknorm_rope(float *qkv, int64_t ldqkv, int B, int n_q, int n_kv,
@@ -248,6 +280,32 @@ GEM_API gem_status gem_gqa_decode_attn_fused(const float *qkv, int64_t ldqkv, in
                                              int64_t cache_cap, int window, float scale,
                                              float *out, int64_t ldo, void *workspace,
                                              size_t ws_bytes, int32_t *status, void *stream);
+
+/*
+ * Decode attention over a compact full-attention cache that keeps V rows only.
+ *   [GEM] "Verified model facts": on a full-attention layer V is the unweighted RMSNorm of
+ *   the K projection and K is the same normalised row times key_norm (gamma_k), then RoPE, so
+ *   the cache can hold V alone and rebuild K inside the attention.  Reading (the record does
+ *   not spell out the rotation): the rebuilt row is rotated at its own position,
+ *     K_j = RoPE_j(V16_j * gamma_k)    (NeoX pairing on the first rope_dim dims, base theta),
+ *   then out as gem_gqa_decode_attn with window 0: softmax over slots 0..p of scale * q.K_j,
+ *   applied to V_j.  Half the cache bytes of the standard layout per position.
+ *   q        [B][ldq] fp32, query heads normalised and rotated at p (gem_rmsnorm_qknorm_rope).
+ *   v_cache  [B][n_kv][cache_cap][d] binary16, 16-byte aligned, already holding slot p.
+ *   gamma_k  [d] fp32 device.  rope_dim a multiple of 16, 0 <= rope_dim <= d; theta > 0.
+ *   d 64, 128, 256 or 512; n_q % n_kv == 0, n_q / n_kv <= 8.
+ *   workspace  gem_gqa_decode_attn_compact_workspace() bytes (0: none needed), 256-byte
+ *            aligned, no initialisation.  Splits are merged in ascending order (deterministic).
+ *   GEM_ERR_UNSUPPORTED_SHAPE where no split layout fits shared memory.
+ */
+GEM_API size_t gem_gqa_decode_attn_compact_workspace(int B, int n_q, int n_kv, int d,
+                                                     int64_t cache_cap, int rope_dim);
+GEM_API gem_status gem_gqa_decode_attn_compact(const float *q, int64_t ldq, const uint16_t *v_cache,
+                                               int B, int n_q, int n_kv, int d, int64_t cache_cap,
+                                               const int32_t *pos, float scale, const float *gamma_k,
+                                               int rope_dim, float theta, float *out, int64_t ldo,
+                                               void *workspace, size_t ws_bytes, int32_t *status,
+                                               void *stream);
 
 /*
  * gem_gqa_decode_attn without a caller-supplied workspace: the split partials live in a
@@ -317,10 +375,13 @@ typedef struct gem_layer_desc {
     int qk_norm, v_from_k, post_norms;
     const void *w_qkv, *w_o, *w_gate, *w_up, *w_down;
     const float *g_attn, *g_ffn, *g_q, *g_k, *g_post_attn, *g_post_ffn;
+    int compact_kv;   /* 1: compact full-attention cache (see gem_gqa_decode_attn_compact);
+                         requires v_from_k, qk_norm and window == 0; k_cache may be NULL */
 } gem_layer_desc;
 
 /*   x        [B][H] fp32 in/out (the residual stream).
- *   k_cache, v_cache  this layer's caches [B][n_kv][cache_cap][d] binary16.
+ *   k_cache, v_cache  this layer's caches [B][n_kv][cache_cap][d] binary16 (compact_kv: the
+ *            V cache alone; k_cache is ignored and may be NULL).
  *   pos      [B] int32 device positions of the new tokens.
  *   workspace  gem_decode_layer_workspace(L, B, cache_cap) bytes, 256-byte aligned;
  *            contents need no initialisation.

@@ -22,7 +22,7 @@ ACT_GELU_TANH = 1
 DEVFLAG_POS_RANGE = 1
 DEVFLAG_TIMEOUT = 2
 
-__all__ = ["GemError", "q4_0_gemv", "q4_0_gemv_workspace", "q4_0_gemv_fused", "rmsnorm", "rmsnorm_qknorm_rope", "gqa_decode_attn",
+__all__ = ["GemError", "q4_0_gemv", "q4_0_gemv_workspace", "q4_0_gemv_fused", "q8_0_gemv", "argmax", "argmax_workspace", "rmsnorm", "rmsnorm_qknorm_rope", "gqa_decode_attn",
            "gqa_decode_attn_workspace", "gqa_decode_attn_fused", "swiglu", "decode_layer", "decode_layer_workspace",
            "DeviceLayer", "device_status", "status_from_flags", "set_wait_limit",
            "set_test_injection", "LayerDesc"]
@@ -64,14 +64,17 @@ def _dev(t: torch.Tensor | None, dtype, name: str):
     return t.data_ptr()
 
 
-def _cache_shape(k: torch.Tensor, v: torch.Tensor, B: int, n_kv: int, d: int) -> int:
-    """Caches must be [B, n_kv, cap, d] (the kernels address them from these sizes)."""
+def _cache_shape(k: torch.Tensor | None, v: torch.Tensor, B: int, n_kv: int, d: int) -> int:
+    """Caches must be [B, n_kv, cap, d] (the kernels address them from these sizes); k may be
+    None for a compact (V-only) cache."""
     for name, c in (("k_cache", k), ("v_cache", v)):
+        if c is None and name == "k_cache":
+            continue
         if c.dim() != 4 or c.shape[0] != B or c.shape[1] != n_kv or c.shape[3] != d:
             raise ValueError("%s must be [B=%d, n_kv=%d, cap, d=%d], got %s" % (name, B, n_kv, d, tuple(c.shape)))
-    if v.shape != k.shape:
+    if k is not None and v.shape != k.shape:
         raise ValueError("k_cache and v_cache shapes differ")
-    return int(k.shape[2])
+    return int(v.shape[2])
 
 
 def _q4_bytes(W: torch.Tensor, N: int, K: int) -> None:
@@ -170,6 +173,40 @@ def q4_0_gemv_fused(W0: torch.Tensor, W1: torch.Tensor | None, N: int, K: int, x
     return y
 
 
+def q8_0_gemv(W: torch.Tensor, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
+              stream=None) -> torch.Tensor:
+    """Tied Q8_0 embedding / logit projection: y[b] = deq(W) @ x[b].  W: N x (K/32*34) bytes."""
+    B = x.shape[0] if x.dim() == 2 else 1
+    if K % 32 == 0 and W.numel() < N * (K // 32) * 34:
+        raise ValueError("W must hold N x K Q8_0 weights (%d bytes), has %d" % (N * (K // 32) * 34, W.numel()))
+    if x.shape[-1] < K or y.shape[-1] < N:
+        raise ValueError("x must have >= K columns and y >= N")
+    st = lib.gem_q8_0_gemv(_dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"), x.shape[-1], B,
+                           _dev(y, torch.float32, "y"), y.shape[-1], _stream(stream))
+    _check(st, "gem_q8_0_gemv")
+    return y
+
+
+def argmax_workspace(B: int, N: int) -> int:
+    return int(lib.gem_argmax_workspace(B, N))
+
+
+def argmax(y: torch.Tensor, idx: torch.Tensor, workspace: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """idx[b] = index of the largest y[b][n] (lowest index on ties; NaN never chosen)."""
+    B = y.shape[0] if y.dim() == 2 else 1
+    N = y.shape[-1]
+    if idx.numel() < B:
+        raise ValueError("idx must hold B indices")
+    need = argmax_workspace(B, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=y.device)
+    st = lib.gem_argmax(_dev(y, torch.float32, "y"), N, B, N, _dev(idx, torch.int32, "idx"),
+                        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "gem_argmax")
+    return idx
+
+
 def rmsnorm(x: torch.Tensor, gamma: torch.Tensor | None, eps: float, out: torch.Tensor,
             stream=None) -> torch.Tensor:
     B = x.shape[0] if x.dim() == 2 else 1
@@ -183,9 +220,11 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor | None, eps: float, out: torch.
 def rmsnorm_qknorm_rope(qkv: torch.Tensor, n_q: int, n_kv: int, d: int,
                         gamma_q: torch.Tensor | None, gamma_k: torch.Tensor | None, v_mode: int,
                         eps: float, pos: torch.Tensor, theta: float, rope_dim: int,
-                        k_cache: torch.Tensor, v_cache: torch.Tensor, window: int = 0,
+                        k_cache: torch.Tensor | None, v_cache: torch.Tensor, window: int = 0,
                         status: torch.Tensor | None = None, stream=None) -> None:
-    """qkv [B, ldqkv] fp32 in place; caches binary16 bits (int16/uint16) [B, n_kv, cap, d]; pos int32 [B]."""
+    """qkv [B, ldqkv] fp32 in place; caches binary16 bits (int16/uint16) [B, n_kv, cap, d]; pos int32 [B].
+
+    k_cache None with v_mode 1 appends the V row only (a compact full-attention cache)."""
     B = qkv.shape[0]
     cap = _cache_shape(k_cache, v_cache, B, n_kv, d)
     st = lib.gem_rmsnorm_qknorm_rope(
@@ -238,6 +277,28 @@ def gqa_decode_attn_fused(qkv: torch.Tensor, n_q: int, n_kv: int, d: int,
         workspace.numel() if workspace is not None else 0, _dev(status, torch.int32, "status"),
         _stream(stream))
     _check(st, "gem_gqa_decode_attn_fused")
+    return out
+
+
+def gqa_decode_attn_compact_workspace(B: int, n_q: int, n_kv: int, d: int, cache_cap: int,
+                                      rope_dim: int) -> int:
+    return int(lib.gem_gqa_decode_attn_compact_workspace(B, n_q, n_kv, d, cache_cap, rope_dim))
+
+
+def gqa_decode_attn_compact(q: torch.Tensor, v_cache: torch.Tensor, n_q: int, n_kv: int, d: int,
+                            pos: torch.Tensor, scale: float, gamma_k: torch.Tensor, rope_dim: int,
+                            theta: float, out: torch.Tensor, workspace: torch.Tensor | None = None,
+                            status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Attention over a V-only cache; K_j = RoPE_j(V_j * gamma_k) is rebuilt inside the kernel."""
+    B = q.shape[0]
+    cap = _cache_shape(None, v_cache, B, n_kv, d)
+    st = lib.gem_gqa_decode_attn_compact(
+        _dev(q, torch.float32, "q"), q.shape[-1], _dev(v_cache, _HALF_BITS, "v_cache"), B, n_q, n_kv,
+        d, cap, _dev(pos, torch.int32, "pos"), scale, _dev(gamma_k, torch.float32, "gamma_k"),
+        rope_dim, theta, _dev(out, torch.float32, "out"), out.shape[-1],
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel() if workspace is not None else 0,
+        _dev(status, torch.int32, "status"), _stream(stream))
+    _check(st, "gem_gqa_decode_attn_compact")
     return out
 
 
@@ -318,7 +379,8 @@ class DeviceLayer:
             w_qkv=ptr(self.w_qkv), w_o=ptr(self.w_o), w_gate=ptr(self.w_gate),
             w_up=ptr(self.w_up), w_down=ptr(self.w_down), g_attn=ptr(self.g_attn),
             g_ffn=ptr(self.g_ffn), g_q=ptr(self.g_q), g_k=ptr(self.g_k),
-            g_post_attn=ptr(self.g_post_attn), g_post_ffn=ptr(self.g_post_ffn))
+            g_post_attn=ptr(self.g_post_attn), g_post_ffn=ptr(self.g_post_ffn),
+            compact_kv=int(getattr(s, "compact_kv", False)))
 
     def weight_bytes(self) -> int:
         return sum(t.numel() for t in (self.w_qkv, self.w_o, self.w_gate, self.w_up, self.w_down))
@@ -328,10 +390,11 @@ def decode_layer_workspace(layer: DeviceLayer, B: int, cache_cap: int) -> int:
     return int(lib.gem_decode_layer_workspace(C.byref(layer.desc), B, cache_cap))
 
 
-def decode_layer(layer: DeviceLayer, x: torch.Tensor, k_cache: torch.Tensor,
+def decode_layer(layer: DeviceLayer, x: torch.Tensor, k_cache: torch.Tensor | None,
                  v_cache: torch.Tensor, pos: torch.Tensor, workspace: torch.Tensor,
                  status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """One layer step, in place on x [B, H] fp32; caches uint16 [B, n_kv, cap, d]."""
+    """One layer step, in place on x [B, H] fp32; caches uint16 [B, n_kv, cap, d] (a compact_kv
+    layer keeps the V cache alone: k_cache may be None)."""
     B = x.shape[0]
     s = layer.shape
     cap = _cache_shape(k_cache, v_cache, B, s.n_kv, s.d)

@@ -23,7 +23,7 @@ class LayerDesc(C.Structure):
                 ("qk_norm", i32), ("v_from_k", i32), ("post_norms", i32),
                 ("w_qkv", p), ("w_o", p), ("w_gate", p), ("w_up", p), ("w_down", p),
                 ("g_attn", p), ("g_ffn", p), ("g_q", p), ("g_k", p),
-                ("g_post_attn", p), ("g_post_ffn", p)]
+                ("g_post_attn", p), ("g_post_ffn", p), ("compact_kv", i32)]
 
 
 # name -> (restype, argtypes); every symbol declared in include/gem.h
@@ -40,6 +40,9 @@ PROTOTYPES = {
     "gem_q4_0_gemv_ws": (i32, [p, i64, i64, p, i64, i32, p, i64, p, p, C.c_size_t, p]),
     "gem_q4_0_gemv_fused": (i32, [p, p, i64, i64, p, i64, i32, p, C.c_float, i32, p, i64, p, p,
                                   C.c_size_t, p]),
+    "gem_q8_0_gemv": (i32, [p, i64, i64, p, i64, i32, p, i64, p]),
+    "gem_argmax_workspace": (C.c_size_t, [i32, i64]),
+    "gem_argmax": (i32, [p, i64, i32, i64, p, p, C.c_size_t, p]),
     "gem_rmsnorm": (i32, [p, i32, i64, p, C.c_float, p, p]),
     "gem_rmsnorm_qknorm_rope": (i32, [p, i64, i32, i32, i32, i32, p, p, i32, C.c_float, p,
                                       C.c_float, i32, p, p, i64, i32, p, p]),
@@ -48,6 +51,9 @@ PROTOTYPES = {
                                   p, i64, p, C.c_size_t, p, p]),
     "gem_gqa_decode_attn_fused": (i32, [p, i64, i32, i32, i32, i32, p, p, i32, C.c_float, p, C.c_float,
                                         i32, p, p, i64, i32, C.c_float, p, i64, p, C.c_size_t, p, p]),
+    "gem_gqa_decode_attn_compact_workspace": (C.c_size_t, [i32, i32, i32, i32, i64, i32]),
+    "gem_gqa_decode_attn_compact": (i32, [p, i64, p, i32, i32, i32, i32, i64, p, C.c_float, p, i32,
+                                          C.c_float, p, i64, p, C.c_size_t, p, p]),
     "gem_gqa_decode_attn_noalloc": (i32, [p, i64, p, p, i32, i32, i32, i32, i64, p, i32,
                                           C.c_float, p, i64, p, p]),
     "gem_swiglu": (i32, [p, p, i32, i64, i32, p, p]),

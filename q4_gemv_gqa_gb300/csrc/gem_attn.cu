@@ -67,6 +67,8 @@ struct AttnParams {
     // flash kernel: one arrival counter per (sequence, KV head) in the workspace, zero between
     // calls (the CTA that merges resets it)
     unsigned* cnt;
+    // compact cache (V rows only): rebuilt-K buffers, offset table and tile anchors
+    uint32_t kr_off, tb_off, an_off;
 };
 
 __host__ __device__ __forceinline__ int tile_slots(int d) { return d <= 64 ? 128 : (d <= 128 ? 64 : 32); }
@@ -434,27 +436,37 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
         prefetch_tensormap(&tmV);
         for (int it = 0; it < npre; ++it) issue(it);
     }
-    const int R = P.rope_dim, half = R / 2;
-    if (P.fuse)   // positions are not written by the preceding kernel: build the table now
-        for (int i = t_id; i < half; i += kNT) {
+    if (P.early) pdl_wait_trigger();
+
+    const bool owner = slot_p >= t0 * kFlashTile && slot_p < t1 * kFlashTile;
+    if (P.fuse) {
+        // The raw rows a warp normalises and rotates (a query head for warps < G; the new K row
+        // for warp W - 2 and the new V row for warp W - 1 of the CTA holding the new slot) are
+        // loaded first, so their L2 round trip overlaps the rotation table.
+        const int R = P.rope_dim, half = R / 2;
+        const float* qrow0 = P.q + b * P.ldq;
+        const float* krow = qrow0 + static_cast<int64_t>(P.n_q + g) * D;
+        const float* vsrc = P.v_mode == 1 ? krow : qrow0 + static_cast<int64_t>(P.n_q + P.n_kv + g) * D;
+        const bool has_q = warp < G;
+        const bool has_k = owner && warp == W - 2, has_v = owner && warp == W - 1;
+        float rq[D / 32], rkv[D / 32];
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+            rq[k] = has_q ? qrow0[static_cast<int64_t>(g * G + warp) * D + lane + 32 * k] : 0.f;
+            rkv[k] = has_k ? krow[lane + 32 * k] : (has_v ? vsrc[lane + 32 * k] : 0.f);
+        }
+        for (int i = t_id; i < half; i += kNT) {   // rotation table of position p
             float c, sv;
             rope_cos_sin(static_cast<double>(p) * fr.w[i], c, sv);
             cs[i] = c;
             sn[i] = sv;
         }
-    if (P.early) pdl_wait_trigger();
-
-    const bool owner = slot_p >= t0 * kFlashTile && slot_p < t1 * kFlashTile;
-    if (P.fuse) {
-        // QK-norm + RoPE of a raw head row (warp-wide), result in sb[0..D)
-        auto rotate = [&](const float* src, const float* gamma, float* sb) {
-            float v[D / 32];
+        __syncthreads();   // rotation table complete
+        // QK-norm + RoPE of a raw head row held in registers (warp-wide), result in sb[0..D)
+        auto rotate = [&](float (&v)[D / 32], const float* gamma, float* sb) {
             float ss = 0.f;
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) {
-                v[k] = src[lane + 32 * k];
-                ss = fmaf(v[k], v[k], ss);
-            }
+            for (int k = 0; k < D / 32; ++k) ss = fmaf(v[k], v[k], ss);
             ss = warp_sum(ss);
             if (gamma) {
                 const float r = rsqrtf(ss / static_cast<float>(D) + P.eps);
@@ -477,36 +489,30 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
             for (int k = 0; k < D / 32; ++k) sb[lane + 32 * k] = v[k];
             __syncwarp();
         };
-        __syncthreads();   // rotation table complete
-        const float* qrow0 = P.q + b * P.ldq;
-        if (warp < G) rotate(qrow0 + static_cast<int64_t>(g * G + warp) * D, P.g_q, qs + warp * D);
-        if (owner) {   // the new token's K and V rows: into the cache and into shared memory
+        if (has_q) rotate(rq, P.g_q, qs + warp * D);
+        if (has_k || has_v) {   // the new token's K and V rows: into the cache and into shared memory
             const int64_t crow = (row0 + slot_p) * D;
-            const float* krow = qrow0 + static_cast<int64_t>(P.n_q + g) * D;
-            if (warp == W - 2) {
-                rotate(krow, P.g_k, kbuf);
+            if (has_k) {
+                rotate(rkv, P.g_k, kbuf);
                 for (int e = lane; e < D; e += 32) {
                     const uint16_t h = __half_as_ushort(__float2half_rn(kbuf[e]));
                     knew[e] = h;
                     P.k_out[crow + e] = h;
                 }
-            } else if (warp == W - 1) {
+            } else {
+                float r = 1.f;
                 if (P.v_mode == 1) {   // V = unweighted RMSNorm of the raw K row
                     float ss = 0.f;
-                    for (int e = lane; e < D; e += 32) ss = fmaf(krow[e], krow[e], ss);
-                    const float r = rsqrtf(warp_sum(ss) / static_cast<float>(D) + P.eps);
-                    for (int e = lane; e < D; e += 32) {
-                        const uint16_t h = __half_as_ushort(__float2half_rn(krow[e] * r));
-                        vnew[e] = h;
-                        P.v_out[crow + e] = h;
-                    }
-                } else {
-                    const float* vrow = qrow0 + static_cast<int64_t>(P.n_q + P.n_kv + g) * D;
-                    for (int e = lane; e < D; e += 32) {
-                        const uint16_t h = __half_as_ushort(__float2half_rn(vrow[e]));
-                        vnew[e] = h;
-                        P.v_out[crow + e] = h;
-                    }
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k) ss = fmaf(rkv[k], rkv[k], ss);
+                    r = rsqrtf(warp_sum(ss) / static_cast<float>(D) + P.eps);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) {
+                    const int e = lane + 32 * k;
+                    const uint16_t h = __half_as_ushort(__float2half_rn(P.v_mode == 1 ? rkv[k] * r : rkv[k]));
+                    vnew[e] = h;
+                    P.v_out[crow + e] = h;
                 }
             }
         }
@@ -734,6 +740,258 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
         P.out[b * P.ldo + static_cast<int64_t>(g * G + h) * D + i] = O / lsm[h];
     }
     if (t_id == 0) *cnt = 0u;   // ready for the next call (which follows this kernel's completion)
+}
+
+// ---- compact full-attention cache (V rows only) --------------------------------------------
+// "gem" research record, "Verified model facts": a full-attention layer's cache can keep the
+// unweighted normalised V row alone; the historical K row is rebuilt inside the attention as
+// V * key_norm, rotated at the row's own position: K_j = RoPE_j(V_j * gamma_k).  Half the
+// bytes of the standard layout per cached position.
+//
+// One CTA per split of the prefix; the split's V tiles (TP slots x D) all stay resident in
+// shared memory, requested before griddepcontrol.wait.  Scores: the dims >= R pass through
+// the rotation, so they are an mma of the binary16 V tile against (scale * q * gamma_k) (hi +
+// lo rows, as in gqa_split_kernel); for the R rotated dims each tile first rebuilds K in
+// shared memory (fp32 rotation by cos/sin of (j0 + t) w_i = anchor (fp64-reduced angle of the
+// tile's first position j0) combined with an offset table of t w_i, then split into binary16
+// hi + lo) and the mma runs against both parts.  Then the split's exact softmax and P V from
+// the same resident tiles; splits are merged by gqa_merge_kernel in ascending order.
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1) gqa_compact_kernel(const __grid_constant__ CUtensorMap tmV,
+                                                                      const AttnParams P,
+                                                                      const __grid_constant__ RopeFreq fr) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);   // [ltile]
+    __half* qa = reinterpret_cast<__half*>(smem + P.qa_off);          // [16][D + 8]
+    float* sc = reinterpret_cast<float*>(smem + P.sc_off);            // [G][L]
+    __half* pa = reinterpret_cast<__half*>(smem + P.pa_off);          // [16][L + 8]
+    float* st = reinterpret_cast<float*>(smem + P.st_off);            // [8][2]: max, denominator
+    __half* kr = reinterpret_cast<__half*>(smem + P.kr_off);          // [2][TP][R + 8]: rebuilt K hi, lo
+    float2* tb = reinterpret_cast<float2*>(smem + P.tb_off);          // [TP][R / 2]: cos, sin of t w_i
+    float2* an = reinterpret_cast<float2*>(smem + P.an_off);          // [R / 2]: cos, sin of j0 w_i
+    __shared__ int abort_flag;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int TP = P.tp;
+    const int L = P.ltile * TP;
+    const int QA = D + 8, PA = L + 8;
+    const int R = P.rope_dim, HR = R / 2, KP = R + 8;
+    const float* gk = P.g_k;
+
+    if (!P.early) pdl_wait_trigger();
+    const int p = P.pos[b];
+    if (p < 0 || static_cast<int64_t>(p) >= P.cap) {
+        if (P.early) pdl_wait_trigger();
+        if (t == 0 && split == 0 && g == 0) atomicOr(P.status, GEM_DEVFLAG_POS_RANGE);
+        return;
+    }
+    const int T = p + 1;
+    int nsplit, t0, t1;
+    split_range(T, TP, P.nsplit_max, split, nsplit, t0, t1);
+    if (split >= nsplit) {
+        if (P.early) pdl_wait_trigger();
+        return;
+    }
+    const int ntile = t1 - t0;   // <= ltile: every tile of the split gets its own slot
+    const int64_t row0 = (static_cast<int64_t>(b) * P.n_kv + g) * P.cap;
+    if (t == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < ntile; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tmV);
+        const uint64_t policy = l2_policy_evict_first();
+        for (int i = 0; i < ntile; ++i) {
+            uint8_t* dst = smem + static_cast<size_t>(i) * P.tile_bytes;
+            mbar_arrive_expect_tx(&bars[i], P.tile_bytes);
+            for (int j = 0; j < D / 64; ++j)
+                tma_load_2d(dst + j * TP * 128, &tmV, j * 64, static_cast<int32_t>(row0 + static_cast<int64_t>(t0 + i) * TP),
+                            &bars[i], policy);
+        }
+    }
+    // cos, sin of t * w_i for the offsets t inside a tile (the same for every tile)
+    for (int idx = t; idx < TP * HR; idx += kAttnThreads) {
+        const int tt = idx / HR, i = idx - tt * HR;
+        float c, sv;
+        rope_cos_sin(static_cast<double>(tt) * fr.w[i], c, sv);
+        tb[idx] = make_float2(c, sv);
+    }
+    if (P.early) pdl_wait_trigger();
+
+    // query rows (normalised and rotated at p by the preceding launch): A operand rows h (hi) and
+    // h + 8 (lo), scale folded in; the pass-through dims also carry gamma_k
+    for (int e = t; e < 8 * D; e += kAttnThreads) {
+        const int h = e / D, col = e - h * D;
+        float v = 0.f;
+        if (h < P.G) {
+            v = P.q[b * P.ldq + static_cast<int64_t>(g * P.G + h) * D + col] * P.scale;
+            if (col >= R) v *= gk[col];
+        }
+        __half hi, lo;
+        split_hi_lo(v, hi, lo);
+        qa[h * QA + col] = hi;
+        qa[(h + 8) * QA + col] = lo;
+    }
+    __syncthreads();
+    const int slot_p = p;
+
+    // ---- scores -----------------------------------------------------------------------------
+    const int gq = lane >> 2, tq = lane & 3;
+    for (int kt = 0; kt < ntile; ++kt) {
+        uint8_t* tile = smem + static_cast<size_t>(kt) * P.tile_bytes;
+        if (!mbar_wait(&bars[kt], 0u, P.status)) abort_flag = 1;
+        const int r = slot_p - (t0 + kt) * TP;   // the new row: written by the preceding launch
+        if (r >= 0 && r < TP)
+            for (int c = t * 8; c < D; c += kAttnThreads * 8)
+                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) = __ldcg(reinterpret_cast<const uint4*>(P.v_cache + (row0 + slot_p) * D + c));
+        if (t < HR) {   // anchor: the tile's first position
+            float c, sv;
+            rope_cos_sin(static_cast<double>((t0 + kt) * TP) * fr.w[t], c, sv);
+            an[t] = make_float2(c, sv);
+        }
+        __syncthreads();
+        if (abort_flag) {
+            if (t == 0) for (int i = kt; i < ntile; ++i) (void)mbar_wait(&bars[i], 0u, nullptr);
+            return;
+        }
+        // rebuilt K of the rotated dims, as binary16 hi + lo
+        for (int idx = t; idx < TP * HR; idx += kAttnThreads) {
+            const int tt = idx / HR, i = idx - tt * HR;
+            const float u = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i, TP))) * gk[i];
+            const float w = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i + HR, TP))) * gk[i + HR];
+            const float2 a0 = an[i], o = tb[idx];
+            const float c = a0.x * o.x - a0.y * o.y, sv = a0.y * o.x + a0.x * o.y;
+            const float k0 = u * c - w * sv, k1 = u * sv + w * c;
+            __half h0, l0, h1, l1;
+            split_hi_lo(k0, h0, l0);
+            split_hi_lo(k1, h1, l1);
+            kr[tt * KP + i] = h0;
+            kr[tt * KP + i + HR] = h1;
+            kr[(TP + tt) * KP + i] = l0;
+            kr[(TP + tt) * KP + i + HR] = l1;
+        }
+        __syncthreads();
+        const uint32_t tbase = smem_u32(tile), kbase = smem_u32(kr);
+        for (int n8 = warp; n8 < TP / 8; n8 += 4) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const int brow = n8 * 8 + (lane & 7), bsel = ((lane >> 3) & 1) * 8;
+            for (int k16 = 0; k16 < R / 16; ++k16) {
+                uint32_t a0, a1, a2, a3, b0, b1, e0, e1;
+                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
+                ldmatrix_x2(b0, b1, kbase + static_cast<uint32_t>((brow * KP + k16 * 16 + bsel) * 2));
+                ldmatrix_x2(e0, e1, kbase + static_cast<uint32_t>(((TP + brow) * KP + k16 * 16 + bsel) * 2));
+                mma_16816(c, a0, a1, a2, a3, b0, b1);
+                mma_16816(c, a0, a1, a2, a3, e0, e1);
+            }
+            for (int k16 = R / 16; k16 < D / 16; ++k16) {
+                uint32_t a0, a1, a2, a3, b0, b1;
+                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
+                ldmatrix_x2(b0, b1, tbase + swz(brow, k16 * 16 + bsel, TP));
+                mma_16816(c, a0, a1, a2, a3, b0, b1);
+            }
+            if (gq < P.G) {
+                const int col = kt * TP + n8 * 8 + 2 * tq;
+                const int s0 = (t0 + kt) * TP + n8 * 8 + 2 * tq;
+                sc[gq * L + col] = s0 < T ? c[0] + c[2] : -INFINITY;
+                sc[gq * L + col + 1] = s0 + 1 < T ? c[1] + c[3] : -INFINITY;
+            }
+        }
+        __syncthreads();   // the rebuilt-K buffer and the anchors are reused by the next tile
+    }
+
+    // ---- softmax over the split (exact: max first) -------------------------------------------
+    const int Ls = ntile * TP;
+    for (int h = warp; h < 8; h += 4) {
+        float m = -INFINITY, l = 0.f;
+        if (h < P.G) {
+            for (int j = lane; j < Ls; j += 32) m = fmaxf(m, sc[h * L + j]);
+            m = warp_max(m);
+            for (int j = lane; j < Ls; j += 32) {
+                const float e = expf(sc[h * L + j] - m);
+                l += e;
+                __half hi, lo;
+                split_hi_lo(e, hi, lo);
+                pa[h * PA + j] = hi;
+                pa[(h + 8) * PA + j] = lo;
+            }
+            l = warp_sum(l);
+        } else {
+            for (int j = lane; j < Ls; j += 32) {
+                pa[h * PA + j] = __float2half_rn(0.f);
+                pa[(h + 8) * PA + j] = __float2half_rn(0.f);
+            }
+        }
+        if (lane == 0) {
+            st[2 * h] = m;
+            st[2 * h + 1] = l;
+        }
+    }
+    // rows of the last tile beyond the prefix hold other slots: zero them for P V
+    {
+        const int kt = ntile - 1, valid = T - (t0 + kt) * TP;
+        uint8_t* tile = smem + static_cast<size_t>(kt) * P.tile_bytes;
+        if (valid < TP)
+            for (int e = t * 8; e < (TP - valid) * D; e += kAttnThreads * 8) {
+                const int r = valid + e / D, c = e % D;
+                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) = make_uint4(0, 0, 0, 0);
+            }
+    }
+    __syncthreads();
+
+    // ---- P V from the resident tiles ----------------------------------------------------------
+    constexpr int NW = D / 32;  // n8 tiles of output dims per warp
+    float acc[NW][4];
+#pragma unroll
+    for (int n = 0; n < NW; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int vt = 0; vt < ntile; ++vt) {
+        const uint32_t tbase = smem_u32(smem + static_cast<size_t>(vt) * P.tile_bytes);
+        for (int k16 = 0; k16 < TP / 16; ++k16) {
+            uint32_t a0, a1, a2, a3;
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = vt * TP + k16 * 16 + (lane >> 4) * 8;
+            ldmatrix_x4(a0, a1, a2, a3, smem_u32(pa + arow * PA + acol));
+#pragma unroll
+            for (int n = 0; n < NW; n += 2) {
+                const int d0 = (warp * NW + n) * 8;
+                uint32_t b0, b1, b2, b3;
+                const int vrow = k16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int vcol = d0 + (lane >> 4) * 8;
+                ldmatrix_x4_trans(b0, b1, b2, b3, tbase + swz(vrow, vcol, TP));
+                mma_16816(acc[n], a0, a1, a2, a3, b0, b1);
+                mma_16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+    }
+
+    // ---- output ------------------------------------------------------------------------------
+    if (gq < P.G) {
+        const int h = g * P.G + gq;
+        const float m = st[2 * gq], l = st[2 * gq + 1];
+        if (nsplit == 1) {
+            float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int n = 0; n < NW; ++n) {
+                const int dd = (warp * NW + n) * 8 + 2 * tq;
+                o[dd] = (acc[n][0] + acc[n][2]) * inv;
+                o[dd + 1] = (acc[n][1] + acc[n][3]) * inv;
+            }
+        } else {
+            float* o = P.part + ((static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max + split) * (D + 2);
+#pragma unroll
+            for (int n = 0; n < NW; ++n) {
+                const int dd = (warp * NW + n) * 8 + 2 * tq;
+                o[dd] = acc[n][0] + acc[n][2];
+                o[dd + 1] = acc[n][1] + acc[n][3];
+            }
+            if (warp == 0 && tq == 0) {
+                o[D] = m;
+                o[D + 1] = l;
+            }
+        }
+    }
 }
 
 // Ordered merge of split states:  M = max_s m_s,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s
@@ -1013,7 +1271,165 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     return st;
 }
 
+// ---- compact cache plan and launch -------------------------------------------------------------
+struct CompactPlan {
+    int tp, ltile, ns;
+    uint32_t tile_bytes, bar_off, qa_off, sc_off, pa_off, st_off, kr_off, tb_off, an_off;
+    size_t smem, ws;
+};
+
+// The largest number of resident tiles per split that fits the device's shared memory, and
+// enough splits to give every SM at least one.  ok = false when no layout fits.
+bool compact_plan(int B, int n_q, int n_kv, int d, int64_t cap, int R, int num_sms, size_t smem_optin,
+                  CompactPlan& pl) {
+    pl = CompactPlan{};
+    pl.tp = tile_slots(d);
+    pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
+    const int64_t nt_max = std::max<int64_t>(1, (cap + pl.tp - 1) / pl.tp);
+    const int G = n_q / n_kv;
+    auto layout = [&](int lt, bool commit) -> size_t {
+        const int L = lt * pl.tp;
+        size_t off = static_cast<size_t>(lt) * pl.tile_bytes;
+        const size_t bar = off;
+        off = align_up(off + static_cast<size_t>(lt) * 8, 128);
+        const size_t qa = off;
+        off = align_up(off + 16ull * (d + 8) * 2, 128);
+        const size_t sc = off;
+        off = align_up(off + static_cast<size_t>(G) * L * 4, 128);
+        const size_t pa = off;
+        off = align_up(off + 16ull * (L + 8) * 2, 128);
+        const size_t st = off;
+        off = align_up(off + 16 * 4, 128);
+        const size_t kr = off;
+        off = align_up(off + 2ull * pl.tp * (R + 8) * 2, 128);
+        const size_t tb = off;
+        off = align_up(off + static_cast<size_t>(pl.tp) * (R / 2) * 8, 128);
+        const size_t an = off;
+        off += static_cast<size_t>(R / 2) * 8;
+        if (commit) {
+            pl.bar_off = static_cast<uint32_t>(bar);
+            pl.qa_off = static_cast<uint32_t>(qa);
+            pl.sc_off = static_cast<uint32_t>(sc);
+            pl.pa_off = static_cast<uint32_t>(pa);
+            pl.st_off = static_cast<uint32_t>(st);
+            pl.kr_off = static_cast<uint32_t>(kr);
+            pl.tb_off = static_cast<uint32_t>(tb);
+            pl.an_off = static_cast<uint32_t>(an);
+        }
+        return align_up(off, 1024) + 1024;
+    };
+    int lmax = 0;
+    for (int lt = 1; lt <= 64; ++lt)   // (the kernel's static shared memory is a few bytes)
+        if (layout(lt, false) + 64 <= smem_optin) lmax = lt;
+    if (lmax == 0) return false;
+    int64_t ns = (nt_max + lmax - 1) / lmax;
+    ns = std::max<int64_t>(ns, std::min<int64_t>(nt_max, (num_sms + static_cast<int64_t>(B) * n_kv - 1) /
+                                                              (static_cast<int64_t>(B) * n_kv)));
+    if (ns > kMaxSplits) return false;
+    pl.ns = static_cast<int>(ns);
+    pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
+    pl.smem = layout(pl.ltile, true);
+    pl.ws = ns > 1 ? static_cast<size_t>(B) * n_q * pl.ns * (d + 2) * sizeof(float) : 0;
+    return true;
+}
+
+const void* pick_compact(int d) {
+    switch (d) {
+        case 64: return reinterpret_cast<const void*>(gqa_compact_kernel<64>);
+        case 128: return reinterpret_cast<const void*>(gqa_compact_kernel<128>);
+        case 256: return reinterpret_cast<const void*>(gqa_compact_kernel<256>);
+        default: return reinterpret_cast<const void*>(gqa_compact_kernel<512>);
+    }
+}
+
 }  // namespace
+
+gem_status compact_check(const CompactAttnOp& op) {
+    if (op.B < 0 || op.n_q < 0 || op.n_kv <= 0 || op.cache_cap <= 0) return GEM_ERR_INVALID_ARG;
+    if (op.d != 64 && op.d != 128 && op.d != 256 && op.d != 512) return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (op.n_q % op.n_kv) return GEM_ERR_INVALID_ARG;
+    if (op.n_q / op.n_kv > 8) return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (op.rope_dim < 0 || op.rope_dim > op.d || (op.rope_dim % 16)) return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (!(op.theta > 0.f)) return GEM_ERR_INVALID_ARG;
+    if (op.B == 0 || op.n_q == 0) return GEM_OK;
+    if (!op.q || !op.v_cache || !op.pos || !op.out || !op.gamma_k) return GEM_ERR_INVALID_ARG;
+    if (op.ldq < static_cast<int64_t>(op.n_q) * op.d || op.ldo < static_cast<int64_t>(op.n_q) * op.d)
+        return GEM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(op.v_cache) & 15) return GEM_ERR_MISALIGNED;
+    if (static_cast<uint64_t>(op.B) * op.n_kv * op.cache_cap >= (1ull << 31)) return GEM_ERR_UNSUPPORTED_SHAPE;
+    return GEM_OK;
+}
+
+size_t compact_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int rope_dim) {
+    if (B <= 0 || n_q <= 0 || n_kv <= 0 || cache_cap <= 0 || n_q % n_kv) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != GEM_OK) return 0;
+    CompactPlan pl;
+    if (!compact_plan(B, n_q, n_kv, d, cache_cap, rope_dim, di.num_sms, di.smem_optin, pl)) return 0;
+    return align_up(pl.ws, 256);
+}
+
+gem_status compact_enqueue(const CompactAttnOp& op, cudaStream_t stream, bool early) {
+    gem_status st = compact_check(op);
+    if (st != GEM_OK || op.B == 0 || op.n_q == 0) return st;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != GEM_OK) return st;
+    CompactPlan pl;
+    if (!compact_plan(op.B, op.n_q, op.n_kv, op.d, op.cache_cap, op.rope_dim, di.num_sms, di.smem_optin, pl))
+        return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (pl.ns > 1 && (!op.workspace || op.ws_bytes < pl.ws)) return GEM_ERR_WORKSPACE;
+    AttnParams P{};
+    P.q = op.q;
+    P.ldq = op.ldq;
+    P.B = op.B;
+    P.n_q = op.n_q;
+    P.n_kv = op.n_kv;
+    P.G = op.n_q / op.n_kv;
+    P.cap = op.cache_cap;
+    P.window = 0;
+    P.scale = op.scale;
+    P.pos = op.pos;
+    P.out = op.out;
+    P.ldo = op.ldo;
+    P.part = static_cast<float*>(op.workspace);
+    P.nsplit_max = pl.ns;
+    P.tp = pl.tp;
+    P.ltile = pl.ltile;
+    P.early = early ? 1 : 0;
+    P.v_cache = op.v_cache;
+    P.tile_bytes = pl.tile_bytes;
+    P.bar_off = pl.bar_off;
+    P.qa_off = pl.qa_off;
+    P.sc_off = pl.sc_off;
+    P.pa_off = pl.pa_off;
+    P.st_off = pl.st_off;
+    P.kr_off = pl.kr_off;
+    P.tb_off = pl.tb_off;
+    P.an_off = pl.an_off;
+    P.status = op.status ? op.status : di.status_word;
+    P.g_k = op.gamma_k;
+    P.rope_dim = op.rope_dim;
+    RopeFreq fr{};
+    for (int i = 0; i < op.rope_dim / 2; ++i)
+        fr.w[i] = std::pow(static_cast<double>(op.theta), -2.0 * i / op.rope_dim);
+    const uint64_t rows = static_cast<uint64_t>(op.B) * op.n_kv * op.cache_cap;
+    CUtensorMap tmV;
+    if ((st = make_tensor_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT16, op.v_cache, op.d, rows,
+                                 static_cast<uint64_t>(op.d) * 2, 64, pl.tp, CU_TENSOR_MAP_SWIZZLE_128B)) != GEM_OK)
+        return st;
+    const void* fn = pick_compact(op.d);
+    if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
+    void* args[] = {&tmV, &P, &fr};
+    if ((st = launch_pdl(fn, dim3(pl.ns, op.n_kv, op.B), dim3(kAttnThreads), pl.smem, stream, args)) != GEM_OK)
+        return st;
+    if (pl.ns > 1) {
+        int D = op.d;
+        void* margs[] = {&P, &D};
+        st = launch_pdl(reinterpret_cast<const void*>(gqa_merge_kernel), dim3(op.B * op.n_q), dim3(kMergeThreads), 0,
+                        stream, margs);
+    }
+    return st;
+}
 
 size_t attn_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int window) {
     if (B <= 0 || n_q <= 0 || n_kv <= 0 || cache_cap <= 0) return 0;
@@ -1190,6 +1606,36 @@ gem_status gem_gqa_decode_attn_fused(const float* qkv, int64_t ldqkv, int B, int
         return GEM_ERR_WORKSPACE;
     if ((st = gem::rope_enqueue(rope, stream)) != GEM_OK) return st;
     return gem::attn_enqueue_in_chain(op, stream);
+}
+
+size_t gem_gqa_decode_attn_compact_workspace(int B, int n_q, int n_kv, int d, int64_t cache_cap, int rope_dim) {
+    return gem::compact_workspace_bytes(B, n_q, n_kv, d, cache_cap, rope_dim);
+}
+
+gem_status gem_gqa_decode_attn_compact(const float* q, int64_t ldq, const uint16_t* v_cache, int B, int n_q,
+                                       int n_kv, int d, int64_t cache_cap, const int32_t* pos, float scale,
+                                       const float* gamma_k, int rope_dim, float theta, float* out, int64_t ldo,
+                                       void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+    gem::CompactAttnOp op{};
+    op.q = q;
+    op.ldq = ldq;
+    op.v_cache = v_cache;
+    op.B = B;
+    op.n_q = n_q;
+    op.n_kv = n_kv;
+    op.d = d;
+    op.cache_cap = cache_cap;
+    op.pos = pos;
+    op.scale = scale;
+    op.gamma_k = gamma_k;
+    op.rope_dim = rope_dim;
+    op.theta = theta;
+    op.out = out;
+    op.ldo = ldo;
+    op.workspace = workspace;
+    op.ws_bytes = ws_bytes;
+    op.status = status;
+    return gem::compact_enqueue(op, static_cast<cudaStream_t>(stream), false);
 }
 
 gem_status gem_gqa_decode_attn_noalloc(const float* q, int64_t ldq, const uint16_t* k_cache,

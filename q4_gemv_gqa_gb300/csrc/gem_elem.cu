@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kRopeWarps * 32) qknorm_rope_kernel(const Rope
             v = e < half ? fmaf(sb[e], c, -sb[e + half] * s) : fmaf(sb[e - half], s, sb[e] * c);
         }
         row[e] = v;
-        if (!is_q) op.k_cache[crow + e] = __half_as_ushort(__float2half_rn(v));
+        if (!is_q && op.k_cache) op.k_cache[crow + e] = __half_as_ushort(__float2half_rn(v));
     }
 }
 
@@ -176,7 +176,9 @@ gem_status rope_check(const RopeOp& op) {
     if (op.window > op.cache_cap) return GEM_ERR_INVALID_ARG;
     if (!(op.theta > 0.f)) return GEM_ERR_INVALID_ARG;
     if (op.B == 0 || op.n_q + op.n_kv == 0) return GEM_OK;
-    if (!op.qkv || !op.pos || (op.n_kv > 0 && (!op.k_cache || !op.v_cache))) return GEM_ERR_INVALID_ARG;
+    // a compact full-attention cache (v_mode 1) may keep V rows only: k_cache NULL
+    if (!op.qkv || !op.pos || (op.n_kv > 0 && (!op.v_cache || (!op.k_cache && op.v_mode != 1))))
+        return GEM_ERR_INVALID_ARG;
     const int64_t need = static_cast<int64_t>(op.n_q + op.n_kv + (op.v_mode ? 0 : op.n_kv)) * op.d;
     if (op.ldqkv < need) return GEM_ERR_INVALID_ARG;
     return GEM_OK;

@@ -151,6 +151,27 @@ bool attn_fusable(int n_q, int n_kv, int d);
 gem_status attn_enqueue_fused(const AttnOp& op, cudaStream_t stream);
 gem_status attn_enqueue_fused_standalone(const AttnOp& op, cudaStream_t stream);
 
+// Attention over a compact full-attention cache (V rows only; K_j = RoPE_j(V_j * gamma_k)).
+struct CompactAttnOp {
+    const float* q; int64_t ldq;      // normalised and rotated query heads
+    const uint16_t* v_cache;          // [B][n_kv][cap][d] binary16
+    int B, n_q, n_kv, d;
+    int64_t cache_cap;
+    const int32_t* pos;
+    float scale;
+    const float* gamma_k;             // [d]
+    int rope_dim;                     // multiple of 16
+    float theta;
+    float* out; int64_t ldo;
+    void* workspace; size_t ws_bytes;
+    int32_t* status;
+};
+gem_status compact_check(const CompactAttnOp& op);
+size_t compact_workspace_bytes(int B, int n_q, int n_kv, int d, int64_t cache_cap, int rope_dim);
+// early: positions and the cached rows are requested before griddepcontrol.wait (inside the
+// layer chain, after the QK-norm / RoPE / V-append launch, whose new row is re-read after it)
+gem_status compact_enqueue(const CompactAttnOp& op, cudaStream_t stream, bool early);
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace gem

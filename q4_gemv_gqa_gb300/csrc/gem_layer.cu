@@ -12,6 +12,8 @@
 //   4  O GEMV with the residual add fused (post_norms: O GEMV, then norm + residual)
 //   5  gate/up GEMV pair, pre-FFN RMSNorm fused in, gated activation in the epilogue
 //   6  down GEMV with the residual add fused (post_norms: down GEMV, then norm + residual)
+// compact_kv (full-attention layers with V from K): 2 appends the V row only and 3 is the
+// compact-cache attention, which rebuilds K_j = RoPE_j(V_j * gamma_k) from the V rows.
 // Every kernel requests its weights (or cached K/V rows) before griddepcontrol.wait, so
 // each launch's HBM stream starts while its predecessor is still running.
 #include <algorithm>
@@ -43,8 +45,11 @@ LayerWs layout(const gem_layer_desc* L, int B, int64_t cap, void* base) {
     w.attn = reinterpret_cast<float*>(take(sizeof(float) * B * L->n_q * L->d));
     w.act = reinterpret_cast<float*>(take(sizeof(float) * B * L->F));
     w.tmp = reinterpret_cast<float*>(take(sizeof(float) * B * L->H));
-    w.attn_ws_bytes = attn_workspace_bytes(B, static_cast<int>(L->n_q), static_cast<int>(L->n_kv),
-                                           static_cast<int>(L->d), cap, L->window);
+    w.attn_ws_bytes = L->compact_kv
+                          ? compact_workspace_bytes(B, static_cast<int>(L->n_q), static_cast<int>(L->n_kv),
+                                                    static_cast<int>(L->d), cap, L->rope_dim)
+                          : attn_workspace_bytes(B, static_cast<int>(L->n_q), static_cast<int>(L->n_kv),
+                                                 static_cast<int>(L->d), cap, L->window);
     w.attn_ws = take(w.attn_ws_bytes);
     const int64_t kmax = std::max<int64_t>(std::max<int64_t>(L->H, L->n_q * L->d), L->F);
     w.rec_bytes = gemv_rec_bytes(B, kmax);
@@ -64,6 +69,8 @@ gem_status check_desc(const gem_layer_desc* L, int B) {
     if (L->qk_norm && (!L->g_q || !L->g_k)) return GEM_ERR_INVALID_ARG;
     if (L->post_norms && (!L->g_post_attn || !L->g_post_ffn)) return GEM_ERR_INVALID_ARG;
     if (L->act < 0 || L->act > 1) return GEM_ERR_INVALID_ARG;
+    // the compact cache rebuilds K from V * gamma_k: V from K, QK-norm, full attention
+    if (L->compact_kv && (!L->v_from_k || !L->qk_norm || L->window)) return GEM_ERR_INVALID_ARG;
     return GEM_OK;
 }
 
@@ -83,7 +90,7 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
     using namespace gem;
     gem_status st = check_desc(L, B);
     if (st != GEM_OK || B == 0) return st;
-    if (!x || !k_cache || !v_cache || !pos) return GEM_ERR_INVALID_ARG;
+    if (!x || (!k_cache && !L->compact_kv) || !v_cache || !pos) return GEM_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return GEM_ERR_MISALIGNED;
     const LayerWs w = layout(L, B, cache_cap, workspace);
     if (!workspace || ws_bytes < w.total) return GEM_ERR_WORKSPACE;
@@ -116,7 +123,7 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
     rope.pos = pos;
     rope.theta = L->theta;
     rope.rope_dim = L->rope_dim;
-    rope.k_cache = k_cache;
+    rope.k_cache = L->compact_kv ? nullptr : k_cache;
     rope.v_cache = v_cache;
     rope.cache_cap = cache_cap;
     rope.window = L->window;
@@ -140,7 +147,7 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
     attn.ws_bytes = w.attn_ws_bytes;
     attn.status = status;
     // flash-eligible shapes: QK-norm, RoPE and the KV append run inside the attention kernel
-    const bool fused = attn_fusable(static_cast<int>(nq), static_cast<int>(nkv), static_cast<int>(d));
+    const bool fused = !L->compact_kv && attn_fusable(static_cast<int>(nq), static_cast<int>(nkv), static_cast<int>(d));
     if (fused) {
         attn.gamma_q = rope.gamma_q;
         attn.gamma_k = rope.gamma_k;
@@ -162,11 +169,37 @@ gem_status gem_decode_layer(const gem_layer_desc* L, int B, float* x, uint16_t* 
     }
     if ((st = gemv_check(qkv)) != GEM_OK || (st = gemv_check(oproj)) != GEM_OK ||
         (st = gemv_check(gateup)) != GEM_OK || (st = gemv_check(down)) != GEM_OK ||
-        (st = rope_check(rope)) != GEM_OK || (st = attn_check(attn)) != GEM_OK)
+        (st = rope_check(rope)) != GEM_OK || (!L->compact_kv && (st = attn_check(attn)) != GEM_OK))
         return st;
 
+    CompactAttnOp cat{};
+    if (L->compact_kv) {
+        cat.q = w.qkv;
+        cat.ldq = nqkv;
+        cat.v_cache = v_cache;
+        cat.B = B;
+        cat.n_q = static_cast<int>(nq);
+        cat.n_kv = static_cast<int>(nkv);
+        cat.d = static_cast<int>(d);
+        cat.cache_cap = cache_cap;
+        cat.pos = pos;
+        cat.scale = L->scale;
+        cat.gamma_k = L->g_k;
+        cat.rope_dim = L->rope_dim;
+        cat.theta = L->theta;
+        cat.out = w.attn;
+        cat.ldo = nq * d;
+        cat.workspace = w.attn_ws;
+        cat.ws_bytes = w.attn_ws_bytes;
+        cat.status = status;
+        if ((st = compact_check(cat)) != GEM_OK) return st;
+    }
+
     if ((st = gemv_enqueue(qkv, stream)) != GEM_OK) return st;
-    if (fused) {
+    if (L->compact_kv) {
+        if ((st = rope_enqueue_in_chain(rope, stream)) != GEM_OK) return st;
+        if ((st = compact_enqueue(cat, stream, true)) != GEM_OK) return st;
+    } else if (fused) {
         if ((st = attn_enqueue_fused(attn, stream)) != GEM_OK) return st;
     } else {
         if ((st = rope_enqueue_in_chain(rope, stream)) != GEM_OK) return st;

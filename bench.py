@@ -364,6 +364,44 @@ def same_shape_layers(wl):
 
 # ---- arms -------------------------------------------------------------------------------------
 
+def attn_full_runner(gem, torch, cache, B, ncopies=2):
+    """The Gemma 4 31B full-attention layer's attention at 32,769 positions (B sequences) over
+    `ncopies` cache copies: cache "standard" (K and V rows; QK-norm, RoPE and the append in the
+    separate launch before it, as the layer chain runs it) or "compact" (V rows only, K rebuilt
+    inside the attention).  Returns (run, algorithmic bytes per attention call, calls per run)."""
+    s = configs.GEMMA31_FULL_COMPACT if cache == "compact" else configs.GEMMA31_FULL
+    P = 32768
+    cap = P + 1
+    qkv = torch.randn((B, s.n_qkv), device="cuda")
+    att = torch.empty((B, s.n_q * s.d), device="cuda")
+    pos = torch.full((B,), P, dtype=torch.int32, device="cuda")
+    gq = torch.ones(s.d, device="cuda")
+    gk = torch.ones(s.d, device="cuda")
+    caches = []
+    for i in range(ncopies):
+        v = torch.from_numpy(gem_synth.normal_f16_bits(0, 8000 + i, (B, s.n_kv, cap, s.d)).view(np.int16)).cuda()
+        k = None if cache == "compact" else torch.from_numpy(
+            gem_synth.normal_f16_bits(0, 8100 + i, (B, s.n_kv, cap, s.d)).view(np.int16)).cuda()
+        caches.append((k, v))
+    if cache == "compact":
+        wsn = gem.gqa_decode_attn_compact_workspace(B, s.n_q, s.n_kv, s.d, cap, s.rope_dim)
+    else:
+        wsn = gem.gqa_decode_attn_workspace(B, s.n_q, s.n_kv, s.d, cap, 0)
+    wsa = torch.empty(max(1, wsn), dtype=torch.uint8, device="cuda")
+
+    def run():
+        for k, v in caches:
+            if cache == "compact":
+                gem.rmsnorm_qknorm_rope(qkv, s.n_q, s.n_kv, s.d, gq, gk, 1, s.eps, pos, s.theta, s.rope_dim,
+                                        None, v)
+                gem.gqa_decode_attn_compact(qkv, v, s.n_q, s.n_kv, s.d, pos, float(s.scale), gk, s.rope_dim,
+                                            s.theta, att, wsa if wsn else None)
+            else:
+                gem.gqa_decode_attn_fused(qkv, s.n_q, s.n_kv, s.d, gq, gk, 1, s.eps, pos, s.theta, s.rope_dim,
+                                          k, v, 0, float(s.scale), att, wsa if wsn else None)
+    return run, attn_bytes(s, B, cap), len(caches)
+
+
 def run_kernel_only(args):
     """A single op on its own (for profiler captures): `gemv` = a 31B FFN projection over --mats
     rotated matrices at --batch (--gemv-shape up: K=5376 -> N=21504; down: K=21504 -> N=5376);
@@ -374,43 +412,34 @@ def run_kernel_only(args):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     res = {"kernel": args.kernel}
     if args.kernel == "attn_full":
-        # the Gemma 4 31B full-attention layer's attention at 32,769 positions (--batch
-        # sequences) over two cache copies: --cache standard (K and V rows; QK-norm, RoPE and
-        # the append in the separate launch before it, as the layer chain runs it) or compact
-        # (V rows only, K rebuilt inside the attention)
-        s = configs.GEMMA31_FULL_COMPACT if args.cache == "compact" else configs.GEMMA31_FULL
-        B, P = args.batch, 32768
-        cap = P + 1
-        res["shape"] = {"n_q": s.n_q, "n_kv": s.n_kv, "d": s.d, "B": B, "positions": cap, "cache": args.cache}
-        qkv = torch.randn((B, s.n_qkv), device="cuda")
-        att = torch.empty((B, s.n_q * s.d), device="cuda")
-        pos = torch.full((B,), P, dtype=torch.int32, device="cuda")
-        gq = torch.ones(s.d, device="cuda")
-        gk = torch.ones(s.d, device="cuda")
-        caches = []
-        for i in range(2):
-            v = torch.from_numpy(gem_synth.normal_f16_bits(0, 8000 + i, (B, s.n_kv, cap, s.d)).view(np.int16)).cuda()
-            k = None if args.cache == "compact" else torch.from_numpy(
-                gem_synth.normal_f16_bits(0, 8100 + i, (B, s.n_kv, cap, s.d)).view(np.int16)).cuda()
-            caches.append((k, v))
-        if args.cache == "compact":
-            wsn = gem.gqa_decode_attn_compact_workspace(B, s.n_q, s.n_kv, s.d, cap, s.rope_dim)
-        else:
-            wsn = gem.gqa_decode_attn_workspace(B, s.n_q, s.n_kv, s.d, cap, 0)
-        wsa = torch.empty(max(1, wsn), dtype=torch.uint8, device="cuda")
+        res["shape"] = {"B": args.batch, "positions": 32769, "cache": args.cache}
+        run, b, n = attn_full_runner(gem, torch, args.cache, args.batch)
+    elif args.kernel == "persistent":
+        # the persistent whole-step kernel over the workload's first --layers layers
+        wl = configs.with_layers(configs.workload(args.workload), args.layers or 2)
+        model = Model(gem, torch, wl, distinct=1)
+        plan = gem.StepPlan(model.layers, wl.B, model.kc, model.vc)
+        res["workload"] = wl.name
 
         def run():
-            for k, v in caches:
-                if args.cache == "compact":
-                    gem.rmsnorm_qknorm_rope(qkv, s.n_q, s.n_kv, s.d, gq, gk, 1, s.eps, pos, s.theta, s.rope_dim,
-                                            None, v)
-                    gem.gqa_decode_attn_compact(qkv, v, s.n_q, s.n_kv, s.d, pos, float(s.scale), gk, s.rope_dim,
-                                                s.theta, att, wsa if wsn else None)
-                else:
-                    gem.gqa_decode_attn_fused(qkv, s.n_q, s.n_kv, s.d, gq, gk, 1, s.eps, pos, s.theta, s.rope_dim,
-                                              k, v, 0, float(s.scale), att, wsa if wsn else None)
-        b = attn_bytes(s, B, cap)
-        n = len(caches)
+            plan.step(model.x, model.pos)
+        b = step_bytes(wl)
+        n = 1
+    elif args.kernel == "elementwise":
+        # the stand-alone RMSNorm (B x 5376) and gated activation (B x 21504) calls
+        B = args.batch
+        xe = torch.randn((B, 5376), device="cuda")
+        ge = torch.ones(5376, device="cuda")
+        oe = torch.empty_like(xe)
+        gate = torch.randn((B, 21504), device="cuda")
+        up = torch.randn((B, 21504), device="cuda")
+        act = torch.empty_like(gate)
+
+        def run():
+            gem.rmsnorm(xe, ge, 1e-6, oe)
+            gem.swiglu(gate, up, 1, act)
+        b = 4 * B * (2 * 5376 + 3 * 21504)
+        n = 1
     elif args.kernel == "q8":
         # the tied Q8_0 logit projection (--vocab x 5376) and the device argmax of its logits
         B, V, Hl = args.batch, args.vocab, 5376
@@ -436,9 +465,15 @@ def run_kernel_only(args):
         y = torch.empty((B, N), device="cuda")
         ws = torch.empty(max(1, gem.q4_0_gemv_workspace(B, K)), dtype=torch.uint8, device="cuda")
 
+        if B > 8:   # the batched prefill GEMM
+            ws = torch.empty(max(1, gem.q4_0_gemm_workspace(B, K)), dtype=torch.uint8, device="cuda")
+
         def run():
             for W in mats:
-                gem.q4_0_gemv(W, N, K, x, y, workspace=ws)
+                if B > 8:
+                    gem.q4_0_gemm(W, None, N, K, x, y, workspace=ws)
+                else:
+                    gem.q4_0_gemv(W, N, K, x, y, workspace=ws)
         b = gemv_bytes(N, K, B)
         n = len(mats)
     else:
@@ -596,6 +631,23 @@ def run_gem(args):
         b = gemv_bytes(21504, 5376, B)
         gemv31["b%d" % B] = {"us": round(us, 3), "gbs": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)}
         del gg
+    # the batched prefill GEMM on the same matrices: 16 and 32 prompt rows per call
+    prefill = {}
+    for M in (16, 32):
+        xm = torch.from_numpy(gem_synth.normal_f32(0, 6001, (M, 5376))).cuda()
+        ym = torch.empty((M, 21504), device="cuda")
+        wsm = torch.empty(max(1, gem.q4_0_gemm_workspace(M, 5376)), dtype=torch.uint8, device="cuda")
+
+        def gm(xm=xm, ym=ym, wsm=wsm):
+            for W in W31:
+                gem.q4_0_gemm(W, None, 21504, 5376, xm, ym, workspace=wsm)
+        gg = capture(torch, gm)
+        us = time_graph(torch, gg, max(5, min(args.steps, 200))) / len(W31) * 1e3
+        b = gemv_bytes(21504, 5376, M)
+        prefill["m%d" % M] = {"us": round(us, 3), "rows_s": round(M / (us * 1e-6), 1),
+                              "gbs": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
+                              "weight_gbs_equiv": round(M * q4_bytes(21504, 5376) / us / 1e3, 1)}
+        del gg
     del W31
     torch.cuda.empty_cache()
 
@@ -619,6 +671,18 @@ def run_gem(args):
         del gl, ga
     del Wq8
     torch.cuda.empty_cache()
+
+    # the Gemma 4 31B full-attention layer's attention (32,769 positions, B = 1): standard
+    # K + V cache against the compact V-only cache (QK-norm / RoPE / append launch included)
+    attn_full = {}
+    for cache in ("standard", "compact"):
+        run, b, n = attn_full_runner(gem, torch, cache, 1)
+        ga = capture(torch, run)
+        us = time_graph(torch, ga, max(5, min(args.steps, 100))) / n * 1e3
+        attn_full[cache] = {"us": round(us, 2), "bytes": b, "gbs": round(b / us / 1e3, 1),
+                            "frac": round(b / us / 1e3 / peak, 4)}
+        del ga, run
+        torch.cuda.empty_cache()
 
     # the other workloads' steps
     subs = {}
@@ -654,7 +718,9 @@ def run_gem(args):
                            "layers shaped like the first, CUDA graph, CUDA events" % len(idx),
             "persistent_step_kernel": persistent,
             "gemv_k5376_n21504": gemv31,
+            "prefill_gemm_k5376_n21504": prefill,
             "logits_q8_0_k5376_v262144": logits,
+            "attn_gemma31_full_p32768": attn_full,
             "workloads": subs,
             "e2e": {"value": round(sbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 4), "wall_ms_per_step": round(e2e_wall_ms, 4),
@@ -759,12 +825,13 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' sub-records")
     ap.add_argument("--vocab", type=int, default=262144, help="--kernel q8: vocabulary rows")
-    ap.add_argument("--kernel", choices=["step", "gemv", "op", "q8", "attn_full"], default="step",
+    ap.add_argument("--kernel", choices=["step", "gemv", "op", "q8", "attn_full", "persistent", "elementwise"], default="step",
                     help="time one op alone (for profiler captures) instead of the step")
     ap.add_argument("--op", default="gqa_decode_attn",
                     choices=["q4_0_gemv_qkv", "gqa_decode_attn", "q4_0_gemv_o", "q4_0_gemv_gate_up",
                              "q4_0_gemv_down"], help="--kernel op: which op of the layer step")
-    ap.add_argument("--batch", type=int, default=1, help="--kernel gemv: activation rows")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="--kernel gemv: activation rows (9..32: the batched prefill GEMM)")
     ap.add_argument("--mats", type=int, default=8, help="--kernel gemv: rotated matrices")
     ap.add_argument("--cache", choices=["standard", "compact"], default="compact",
                     help="--kernel attn_full: the full-attention layer's cache layout")

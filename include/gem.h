@@ -167,6 +167,23 @@ GEM_API gem_status gem_q4_0_gemv_fused(const void *W0, const void *W1, int64_t N
                                        void *stream);
 
 /*
+ * Batched prefill Q4_0 GEMM: M = 1..32 activation rows (prompt tokens) through one matrix (or a
+ * gate/up pair), each weight streamed from HBM once and reused by every row.  [GEM] "Native
+ * Metal diagnostic: buffer ownership" (the batched-Q4 prefill operator: a dequantised weight tile
+ * reused across up to 32 prompt rows with fp32 accumulation, measured in rows/s at the 31B FFN
+ * shape).  Arithmetic, layouts and the optional norm / pair / activation / residual are those of
+ * gem_q4_0_gemv_fused with B = M; the weights stay exact ((q - 8) * d, no rounding to half).
+ *   M        0..32 (M <= 8 runs the decode kernels; 9..32 the column-tiled prefill kernel).
+ *   workspace  gem_q4_0_gemm_workspace(M, K) bytes (0 for M = 1), 256-byte aligned, no
+ *            initialisation: 4 * M * K bytes of operand records plus a row table.
+ */
+GEM_API size_t gem_q4_0_gemm_workspace(int M, int64_t K);
+GEM_API gem_status gem_q4_0_gemm(const void *W0, const void *W1, int64_t N, int64_t K,
+                                 const float *x, int64_t ldx, int M, const float *gamma, float eps,
+                                 int act, float *y, int64_t ldy, const float *residual,
+                                 void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Q8_0 dequantise-and-matvec: the tied token embedding / output (logit) projection.
  * [GEM] "Verified model facts" (the published layout keeps the tied embedding as Q8_0) and
  * "Native Metal diagnostic: buffer ownership" (the Q8 logit matvec, one token, and the

@@ -173,6 +173,36 @@ def q4_0_gemv_fused(W0: torch.Tensor, W1: torch.Tensor | None, N: int, K: int, x
     return y
 
 
+def q4_0_gemm_workspace(M: int, K: int) -> int:
+    return int(lib.gem_q4_0_gemm_workspace(M, K))
+
+
+def q4_0_gemm(W0: torch.Tensor, W1: torch.Tensor | None, N: int, K: int, x: torch.Tensor,
+              y: torch.Tensor, gamma: torch.Tensor | None = None, eps: float = 1e-6,
+              act: int = ACT_SILU, residual: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Batched prefill GEMM: M = x.shape[0] (<= 32) prompt rows through W0 (or the W0/W1 pair),
+    each weight read once.  Same options as q4_0_gemv_fused; workspace allocated when needed."""
+    M = x.shape[0] if x.dim() == 2 else 1
+    _q4_bytes(W0, N, K)
+    if W1 is not None:
+        _q4_bytes(W1, N, K)
+    if x.shape[-1] < K or y.shape[-1] < N:
+        raise ValueError("x must have >= K columns and y >= N")
+    need = q4_0_gemm_workspace(M, K) if K % 32 == 0 else 0
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    st = lib.gem_q4_0_gemm(_dev(W0, torch.uint8, "W0"), _dev(W1, torch.uint8, "W1"), N, K,
+                           _dev(x, torch.float32, "x"), x.shape[-1], M,
+                           _dev(gamma, torch.float32, "gamma"), eps, act,
+                           _dev(y, torch.float32, "y"), y.shape[-1],
+                           _dev(residual, torch.float32, "residual"),
+                           _dev(workspace, torch.uint8, "workspace") if need else None,
+                           workspace.numel() if need else 0, _stream(stream))
+    _check(st, "gem_q4_0_gemm")
+    return y
+
+
 def q8_0_gemv(W: torch.Tensor, N: int, K: int, x: torch.Tensor, y: torch.Tensor,
               stream=None) -> torch.Tensor:
     """Tied Q8_0 embedding / logit projection: y[b] = deq(W) @ x[b].  W: N x (K/32*34) bytes."""

@@ -1,4 +1,4 @@
-// gem_gemv_bn.cu — host plan and launches of the 2..8-row tensor-core Q4_0 GEMV (gem_gemv_bn.cuh):
+// gem_gemv_bn.cu — host plan and launches of the 2..32-row tensor-core Q4_0 GEMV (gem_gemv_bn.cuh):
 // the activation prep kernel, then the GEMV.
 #include <algorithm>
 #include <map>
@@ -48,9 +48,11 @@ gem_status ensure_smem_bn(const void* fn, int device, size_t bytes) {
 
 }  // namespace
 
+int gemv_col_tiles(int B) { return B <= 8 ? 1 : (B <= 16 ? 2 : 4); }
+
 size_t gemv_rec_bytes(int B, int64_t K) {
-    if (B < 2 || K % 256) return 0;
-    return static_cast<size_t>(K / 256) * 2 * kHgBytes + 8 * sizeof(float2);
+    if (B < 2 || B > kMaxRows || K % 256) return 0;
+    return static_cast<size_t>(K / 256) * 2 * kHgBytes * gemv_col_tiles(B) + kMaxRows * sizeof(float2);
 }
 
 gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, bool* planned) {
@@ -79,16 +81,26 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
         rec = static_cast<uint8_t*>(s);
     }
     p.rec = rec;
-    p.rowinfo = reinterpret_cast<const float2*>(rec + rec_bytes - 8 * sizeof(float2));
-    const void* fn = nmat == 2 ? reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<2>)
-                               : reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<1>);
+    p.rowinfo = reinterpret_cast<const float2*>(rec + rec_bytes - kMaxRows * sizeof(float2));
+    const int NT = gemv_col_tiles(B);
+    const void* fn = nullptr;
+    switch (NT * 2 + nmat) {
+        case 3: fn = reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<1, 1>); break;
+        case 4: fn = reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<2, 1>); break;
+        case 5: fn = reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<1, 2>); break;
+        case 6: fn = reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<2, 2>); break;
+        case 9: fn = reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<1, 4>); break;
+        default: fn = reinterpret_cast<const void*>(q4_0_gemv_bn_kernel<2, 4>); break;
+    }
+    const int ncw_per_group = 2 * NT;   // consumer warps per group of a phase
+    const int gps_max = NT == 1 ? 7 : 16 / ncw_per_group;
 
     const size_t budget = std::min<size_t>(gemv_mma::kSmemBudget, di.smem_optin);
     int rps = 1, umax = 1;
     auto layout = [&](int gp, int u, int n, bool commit) -> size_t {
         const size_t stage = static_cast<size_t>(rps * gp) * kBoxBytes;
-        const size_t recbuf = static_cast<size_t>(2 * gp) * kHgBytes;
-        const size_t red = static_cast<size_t>(nmat) * u * (2 * gp) * 32 * 16;
+        const size_t recbuf = static_cast<size_t>(2 * gp) * kHgBytes * NT;
+        const size_t red = static_cast<size_t>(nmat) * u * (ncw_per_group * gp) * NT * 32 * 16;
         size_t off = align_up(static_cast<size_t>(n) * stage, 128);
         const size_t full_off = off;
         off += kMaxSlots * 8;
@@ -125,7 +137,7 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
         const int Gk = (p.G + ks - 1) / ks;
         double best = -1.0;
         gps = 0;
-        for (int c = std::min(7, Gk); c >= 1; --c) {
+        for (int c = std::min(gps_max, Gk); c >= 1; --c) {
             const int nph = (Gk + c - 1) / c;
             for (int u = umax; u >= 1; u = u > 1 ? (u + 1) / 2 : 0) {
                 if (ks > 1 && u < umax) break;
@@ -141,7 +153,7 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
                 if (ks > 1 && static_cast<size_t>(nmat) * u * kUnitRows * B * 4 > static_cast<size_t>(2 * c) * kHgBytes)
                     break;
                 const int passes = (umax + u - 1) / u;
-                const double score = 2.0 * Gk / static_cast<double>(nph) - 0.01 * passes;
+                const double score = 2.0 * Gk / static_cast<double>(nph) - (NT == 1 ? 0.01 : 1.0) * passes;
                 if (score > best) {
                     best = score;
                     gps = c;
@@ -158,12 +170,12 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     int ks = 1, ncl = std::min(di.num_sms, p.U);
     const int um1 = (p.U + di.num_sms - 1) / di.num_sms;
     for (int k : {4, 2}) {
-        if (um1 > 2 || p.G < 32) continue;   // K >= 8192 (shorter K measured no faster split)
+        if (um1 > 2 || p.G < 32 || NT > 1) continue;   // K >= 8192 (shorter K measured no faster split)
         int n = std::min(di.num_sms / k, p.U);
         if (!plan(k, n)) continue;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(n * k);
-        cfg.blockDim = dim3((2 * gps + 1) * 32);
+        cfg.blockDim = dim3((ncw_per_group * gps + 1) * 32);
         cfg.dynamicSmemBytes = layout(gps, up, ns, false);
         cudaLaunchAttribute a[1];
         a[0].id = cudaLaunchAttributeClusterDimension;
@@ -194,7 +206,7 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     p.gps = gps;
     p.nphase = ((p.G + ks - 1) / ks + gps - 1) / gps;
     p.ns = ns;
-    p.ncw = 2 * gps;
+    p.ncw = ncw_per_group * gps;
     const size_t smem = layout(gps, up, ns, true);
 
     const int64_t rowbytes = op.K / 32 * 18;
@@ -221,11 +233,12 @@ gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceIn
     pp.eps = op.eps;
     pp.G = p.G;
     pp.B = B;
+    pp.nt = NT;
     pp.nchunk = std::max(1, std::min((32 * p.G + kPrepThreads - 1) / kPrepThreads, std::max(1, 152 / B)));
     pp.rec = rec;
     pp.clear = op.clear;
     pp.nclear = op.nclear;
-    pp.rowinfo = reinterpret_cast<float2*>(rec + rec_bytes - 8 * sizeof(float2));
+    pp.rowinfo = reinterpret_cast<float2*>(rec + rec_bytes - kMaxRows * sizeof(float2));
     void* pargs[] = {&pp};
     if ((st = launch_pdl(reinterpret_cast<const void*>(act_prep_kernel), dim3(pp.nchunk, B), dim3(kPrepThreads), 0,
                          stream, pargs)) != GEM_OK)

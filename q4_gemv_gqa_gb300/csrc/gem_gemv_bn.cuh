@@ -1,5 +1,7 @@
-// gem_gemv_bn.cuh — Q4_0 GEMV for 2..8 activation rows on mma.sync, with the activations
-// converted once per call into mma operand records (not once per CTA).
+// gem_gemv_bn.cuh — Q4_0 GEMV for 2..32 activation rows on mma.sync, with the activations
+// converted once per call into mma operand records (not once per CTA).  2..8 rows are the
+// batched-decode form; 9..32 rows (column tiles of 8 activation rows, NT = 2 or 4) the batched
+// prefill GEMM, where each weight is reused by up to 32 rows.
 //
 // act_prep_kernel turns x (optionally RMSNorm-weighted: gamma * x, the 1/rms factor being applied
 // to the output) into binary16 hi + lo operand records in global memory, with one power of two per
@@ -12,7 +14,9 @@
 // MMA mapping (m16n8k16, f16 x f16 -> f32): A = 16 weight rows x 16 codes of one block (low
 // nibbles: k-tile 0, high nibbles: k-tile 1), B = the same 16 codes' activations x 8 columns (the
 // activation rows, hi and lo parts in two separate mma), so D[row][b] of one block is scaled by
-// the row's block scale d before it is summed.  A half group is the 4 even or the 4 odd blocks of
+// the row's block scale d before it is summed.  With NT column tiles (8 activation rows each) a
+// block's dequantised A fragments serve NT x 4 mma, and each warp owns 4 / NT of its half
+// group's blocks, so its operand registers stay at 32 whatever the row count.  A half group is the 4 even or the 4 odd blocks of
 // a 256-weight group (as in the one-row kernel): odd blocks give each lane an aligned code word,
 // even ones one byte permute of two words.
 //
@@ -37,10 +41,11 @@ constexpr int kEntryBytes = 32;                    // one lane's hi (16 B) and l
 constexpr int kHgBytes = 4 * 32 * kEntryBytes;     // one half group: 4 blocks x 32 lanes
 constexpr int kPrepThreads = 256;
 
-// Records: [hg][j][lane][hi uint4, lo uint4]; lane (g, t) = activation row g, k-slot t.  For block
+// Records: [hg][j][ct][lane][hi uint4, lo uint4]; lane (g, t) = activation row 8 ct + g, k-slot t.  For block
 // 2j + (hg & 1) of group hg / 2, register r of k-tile tau holds the two elements whose codes sit in
 // bytes r and r + 2 of code word t (nibble tau): the operand layout the weights' A fragments meet.
 // rowinfo[b] = {2^e_b, 2^-e_b (* 1/rms of row b when gamma is given)}.
+constexpr int kMaxRows = 32;
 struct PrepParams {
     const float* x;
     int64_t ldx;
@@ -48,6 +53,7 @@ struct PrepParams {
     float eps;
     int G;
     int B;
+    int nt;              // column tiles of 8 activation rows in the record layout
     int nchunk;          // CTAs per activation row
     uint8_t* rec;
     float2* rowinfo;
@@ -124,7 +130,8 @@ __global__ void __launch_bounds__(kPrepThreads) act_prep_kernel(const PrepParams
             hw[r] = *reinterpret_cast<const uint32_t*>(&hh);
             lw[r] = *reinterpret_cast<const uint32_t*>(&ll);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.rec + (static_cast<size_t>(hg * 4 + j) * 32 + (b * 4 + t)) * kEntryBytes);
+        const size_t ent = (static_cast<size_t>(hg * 4 + j) * p.nt + (b >> 3)) * 32 + ((b & 7) * 4 + t);
+        uint4* dst = reinterpret_cast<uint4*>(p.rec + ent * kEntryBytes);
         dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         dst[1] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
@@ -147,13 +154,15 @@ struct Params {
     int* status;
 };
 
-// One task: the 4 blocks of my half group in rows g and g + 8 of one row block, all B columns.
-// a = shared offset of row g, group jg, plus 16 for odd blocks; acc += d * D per block.
-template <bool ODD>
-__device__ __forceinline__ void task_bn(const uint8_t* smem, uint32_t a, int t, uint32_t sel, const uint4 (&xh)[4],
-                                        const uint4 (&xl)[4], float (&acc)[4]) {
+// One task: blocks j0 .. j0 + BPW - 1 of my half group in rows g and g + 8 of one row block, all
+// NT column tiles.  a = shared offset of row g, group jg, plus 16 for odd blocks; acc += d * D.
+template <bool ODD, int BPW, int NT>
+__device__ __forceinline__ void task_bn(const uint8_t* smem, uint32_t a, int j0, int t, uint32_t sel,
+                                        const uint4 (&xh)[BPW][NT], const uint4 (&xl)[BPW][NT],
+                                        float (&acc)[NT][4]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int jj = 0; jj < BPW; ++jj) {
+        const int j = j0 + jj;
         uint32_t w[2];
         float dsc[2];
 #pragma unroll
@@ -173,16 +182,28 @@ __device__ __forceinline__ void task_bn(const uint8_t* smem, uint32_t a, int t, 
         uint32_t l02, l13, h02, h13, m02, m13, n02, n13;
         gemv_mma::dequant_word(w[0], l02, l13, h02, h13);
         gemv_mma::dequant_word(w[1], m02, m13, n02, n13);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(c, l02, m02, l13, m13, xh[j].x, xh[j].y);
-        mma_16816(c, h02, n02, h13, n13, xh[j].z, xh[j].w);
-        mma_16816(c, l02, m02, l13, m13, xl[j].x, xl[j].y);
-        mma_16816(c, h02, n02, h13, n13, xl[j].z, xl[j].w);
-        acc[0] = fmaf(dsc[0], c[0], acc[0]);
-        acc[1] = fmaf(dsc[0], c[1], acc[1]);
-        acc[2] = fmaf(dsc[1], c[2], acc[2]);
-        acc[3] = fmaf(dsc[1], c[3], acc[3]);
+#pragma unroll
+        for (int ct = 0; ct < NT; ++ct) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(c, l02, m02, l13, m13, xh[jj][ct].x, xh[jj][ct].y);
+            mma_16816(c, h02, n02, h13, n13, xh[jj][ct].z, xh[jj][ct].w);
+            mma_16816(c, l02, m02, l13, m13, xl[jj][ct].x, xl[jj][ct].y);
+            mma_16816(c, h02, n02, h13, n13, xl[jj][ct].z, xl[jj][ct].w);
+            acc[ct][0] = fmaf(dsc[0], c[0], acc[ct][0]);
+            acc[ct][1] = fmaf(dsc[0], c[1], acc[ct][1]);
+            acc[ct][2] = fmaf(dsc[1], c[2], acc[ct][2]);
+            acc[ct][3] = fmaf(dsc[1], c[3], acc[ct][3]);
+        }
     }
+}
+
+// The reduction area: per (row block, consumer warp, column tile) the lanes' float4 partial sums;
+// (row r16 of the unit, activation row b) sits at lane (r16 & 7) * 4 + (b & 7) / 2, component
+// (r16 >> 3) * 2 + (b & 1) of column tile b / 8.
+template <int NT>
+__device__ __forceinline__ int red_index(int rb, int w, int ncw, int r16, int b) {
+    const int ct = b >> 3, gb = b & 7;
+    return ((((rb * ncw + w) * NT + ct) * 32 + (r16 & 7) * 4 + (gb >> 1)) * 4) + (r16 >> 3) * 2 + (gb & 1);
 }
 
 using gemv_b1::cluster_sync_all;
@@ -194,7 +215,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-template <int NMAT>
+template <int NMAT, int NT>
 __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __grid_constant__ CUtensorMap tm0,
                                                                       const __grid_constant__ CUtensorMap tm1,
                                                                       const Params p) {
@@ -203,14 +224,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + p.empty_off);
     uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + p.rfull_off);
     uint64_t* rempty = reinterpret_cast<uint64_t*>(smem + p.rempty_off);
-    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [rb][warp][lane][4]
+    float* red = reinterpret_cast<float*>(smem + p.red_off);   // [rb][warp][ct][lane][4]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ncw = p.ncw, nct = ncw * 32;
     const int gps = p.gps, ns = p.ns, rps = p.rps;
     const uint32_t stage_bytes = p.stage_bytes;
     const uint32_t rstride = static_cast<uint32_t>(gps * kBoxBytes);
-    const uint32_t rec_phase = static_cast<uint32_t>(2 * gps * kHgBytes);   // one record buffer
+    const uint32_t rec_phase = static_cast<uint32_t>(2 * gps * kHgBytes * NT);   // one record buffer
     // K split: cluster cid (of ncl) owns a unit range; its CTA `rank` owns groups [gk0, gk0 + Gr)
     const int ks = p.ks, rank = static_cast<int>(blockIdx.x) % ks, cid = static_cast<int>(blockIdx.x) / ks;
     const int ncl = static_cast<int>(gridDim.x) / ks;
@@ -285,10 +306,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                     // the buffer is free once every warp holds phase q - 1's operands
                     if (q >= 1 && !(ok = mbar_wait(rempty, (q - 1) & 1, p.status))) break;
                     const int ng = min(gps, Gr - ph * gps);
-                    const uint32_t bytes = static_cast<uint32_t>(2 * ng * kHgBytes);
+                    const uint32_t bytes = static_cast<uint32_t>(2 * ng * kHgBytes * NT);
                     mbar_arrive_expect_tx(rfull, bytes);
                     bulk_load(smem + p.xf_off,
-                              p.rec + static_cast<size_t>(2 * gk0) * kHgBytes + static_cast<size_t>(ph) * rec_phase,
+                              p.rec + static_cast<size_t>(2 * gk0) * kHgBytes * NT + static_cast<size_t>(ph) * rec_phase,
                               bytes, rfull);
                     for (int v = (q == 0 ? pre : 0); v < nv && ok; ++v) ok = issue(pass, ph, v);
                 }
@@ -306,10 +327,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
     // ---------------- consumer warps ----------------
     pdl_wait_trigger();   // row scales (and the residual) come from earlier kernels
 
+    constexpr int BPW = 4 / NT;   // blocks of the half group per warp
     const int g = lane >> 2, t = lane & 3;
-    const int jg = warp >> 1;
-    const bool odd = warp & 1;
-    const bool col = g < p.B;   // activation row g exists
+    const int hgl = warp / NT, j0 = (warp % NT) * BPW;   // half group of the phase, first block
+    const int jg = hgl >> 1;
+    const bool odd = hgl & 1;
     const uint32_t aoff = static_cast<uint32_t>(jg * kBoxBytes + g * kGroupBytes + (odd ? 16 : 0));
     const uint32_t sel = t == 0 ? 0x3254u : 0x3210u;   // even blocks: word 0 joins the two tails
 
@@ -327,17 +349,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
             for (int ph = 0; ph < nphr; ++ph, ++q) {
                 const bool mine = jg < min(gps, Gr - ph * gps);
                 if (ok) ok = mbar_wait(rfull, q & 1, p.status);
-                uint4 xh[4], xl[4];
+                uint4 xh[BPW][NT], xl[BPW][NT];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) xh[j] = xl[j] = make_uint4(0u, 0u, 0u, 0u);
-                if (mine && col && ok) {
-                    const uint4* e = reinterpret_cast<const uint4*>(smem + p.xf_off + (warp * 4 * 32 + lane) * kEntryBytes);
+                for (int jj = 0; jj < BPW; ++jj)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        xh[j] = e[j * 32 * 2];
-                        xl[j] = e[j * 32 * 2 + 1];
+                    for (int ct = 0; ct < NT; ++ct) {
+                        xh[jj][ct] = xl[jj][ct] = make_uint4(0u, 0u, 0u, 0u);
+                        if (mine && ok && ct * 8 + g < p.B) {   // activation row 8 ct + g exists
+                            const uint4* e = reinterpret_cast<const uint4*>(
+                                smem + p.xf_off + (((hgl * 4 + j0 + jj) * NT + ct) * 32 + lane) * kEntryBytes);
+                            xh[jj][ct] = e[0];
+                            xl[jj][ct] = e[1];
+                        }
                     }
-                }
                 // The next bulk copy into the buffer (async proxy) may follow the arrive at once:
                 // order my reads of it (generic proxy) before that write.
                 fence_proxy_async_smem();
@@ -348,15 +372,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                     if (mine && ok) {
                         const int nr = min(rps, nrb - v * rps);
                         for (int r = 0; r < nr; ++r) {
-                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                            task_bn<ODD>(smem, static_cast<uint32_t>(slot) * stage_bytes + r * rstride + aoff, t, sel,
-                                         xh, xl, acc);
-                            float4* rr = reinterpret_cast<float4*>(red) + ((v * rps + r) * ncw + warp) * 32 + lane;
-                            if (ph) {
-                                const float4 o = *rr;
-                                acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+                            float acc[NT][4];
+#pragma unroll
+                            for (int ct = 0; ct < NT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
+                            task_bn<ODD, BPW, NT>(smem, static_cast<uint32_t>(slot) * stage_bytes + r * rstride + aoff,
+                                                  j0, t, sel, xh, xl, acc);
+#pragma unroll
+                            for (int ct = 0; ct < NT; ++ct) {
+                                float4* rr = reinterpret_cast<float4*>(red) + (((v * rps + r) * ncw + warp) * NT + ct) * 32 + lane;
+                                if (ph) {
+                                    const float4 o = *rr;
+                                    acc[ct][0] += o.x; acc[ct][1] += o.y; acc[ct][2] += o.z; acc[ct][3] += o.w;
+                                }
+                                *rr = make_float4(acc[ct][0], acc[ct][1], acc[ct][2], acc[ct][3]);
                             }
-                            *rr = make_float4(acc[0], acc[1], acc[2], acc[3]);
                         }
                     }
                     __syncwarp();
@@ -378,9 +407,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                 for (int idx = tid; idx < items; idx += nct) {
                     const int rb = idx / (kUnitRows * B), rem = idx - rb * (kUnitRows * B);
                     const int r16 = rem / B, b = rem - r16 * B;
-                    const int ln = (r16 & 7) * 4 + (b >> 1), comp = (r16 >> 3) * 2 + (b & 1);
                     float v = 0.f;
-                    for (int w = 0; w < ncw; ++w) v += red[((rb * ncw + w) * 32 + ln) * 4 + comp];
+                    for (int w = 0; w < ncw; ++w) v += red[red_index<NT>(rb, w, ncw, r16, b)];
                     part[idx] = v;
                 }
                 cluster_sync_all();
@@ -415,16 +443,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) q4_0_gemv_bn_kernel(const __gr
                 if (NMAT == 2 && (rb & 1)) continue;
                 const int64_t n = static_cast<int64_t>(ub + rb / NMAT) * kUnitRows + r16;
                 if (n >= p.N) continue;
-                const int ln = (r16 & 7) * 4 + (b >> 1), comp = (r16 >> 3) * 2 + (b & 1);
                 float v = 0.f;
-                for (int w = 0; w < ncw; ++w) v += red[((rb * ncw + w) * 32 + ln) * 4 + comp];
+                for (int w = 0; w < ncw; ++w) v += red[red_index<NT>(rb, w, ncw, r16, b)];
                 const float out = p.rowinfo[b].y;
                 v *= out;
                 if (NMAT == 1) {
                     if (p.residual) v += p.residual[b * p.ldr + n];
                 } else {
                     float uv = 0.f;
-                    for (int w = 0; w < ncw; ++w) uv += red[(((rb + 1) * ncw + w) * 32 + ln) * 4 + comp];
+                    for (int w = 0; w < ncw; ++w) uv += red[red_index<NT>(rb + 1, w, ncw, r16, b)];
                     v = gemv_mma::act_fn(v, p.act) * (uv * out);
                 }
                 p.y[b * p.ldy + n] = v;

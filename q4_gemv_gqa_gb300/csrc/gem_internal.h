@@ -77,6 +77,7 @@ gem_status gemv_enqueue_b1(const GemvOp& op, cudaStream_t stream, const DeviceIn
 // gemv_rec_bytes(B, K), else in a library-owned per-device array of kGemvRecScratchBytes (shared
 // by every call on the device: calls on concurrently running streams must not both use it).
 constexpr size_t kGemvRecScratchBytes = size_t(4) << 20;
+constexpr int kMaxGemmRows = 32;   // the batched prefill GEMM's activation rows
 size_t gemv_rec_bytes(int B, int64_t K);
 gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, bool* planned);
 

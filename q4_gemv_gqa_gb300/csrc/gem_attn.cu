@@ -748,37 +748,47 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
 // V * key_norm, rotated at the row's own position: K_j = RoPE_j(V_j * gamma_k).  Half the
 // bytes of the standard layout per cached position.
 //
-// One CTA per split of the prefix; the split's V tiles (TP slots x D) all stay resident in
-// shared memory, requested before griddepcontrol.wait.  Scores: the dims >= R pass through
-// the rotation, so they are an mma of the binary16 V tile against (scale * q * gamma_k) (hi +
-// lo rows, as in gqa_split_kernel); for the R rotated dims each tile first rebuilds K in
-// shared memory (fp32 rotation by cos/sin of (j0 + t) w_i = anchor (fp64-reduced angle of the
-// tile's first position j0) combined with an offset table of t w_i, then split into binary16
-// hi + lo) and the mma runs against both parts.  Then the split's exact softmax and P V from
-// the same resident tiles; splits are merged by gqa_merge_kernel in ascending order.
+// One CTA of 8 warps per split of the prefix streams the split's V tiles (TP slots x D) through
+// a ring of kCompactSlots TMA stages, each V byte read once.  Per tile:
+//   1. the rotated dims of K are rebuilt in shared memory as binary16 hi + lo: fp32 rotation by
+//      cos / sin of (j0 + t) w_i = tile anchor (fp64-reduced angle of the tile's first position,
+//      taken for every tile of the split before the wait) x offset tables of 8 a w_i and b w_i
+//      (t = 8 a + b);
+//   2. scores on tensor cores: the dims >= R pass through the rotation, so their part is an mma
+//      of the V tile itself against (scale * q * gamma_k); the R rotated dims an mma against the
+//      rebuilt hi and lo rows; warps take (n8 tile, part) items;
+//   3. online softmax, one warp per query head: running max, rescale factor, P as hi + lo;
+//   4. each warp rescales its output accumulators and adds P V for its output dims.
+// The split's state (unnormalised output, max, denominator) goes to the workspace and the
+// ordered merge kernel combines the splits in ascending order (deterministic).
+constexpr int kCompactWarps = 8;
+constexpr int kCompactThreads = kCompactWarps * 32;
+constexpr int kCompactSlots = 4;
+
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1) gqa_compact_kernel(const __grid_constant__ CUtensorMap tmV,
-                                                                      const AttnParams P,
-                                                                      const __grid_constant__ RopeFreq fr) {
+__global__ void __launch_bounds__(kCompactThreads, 1) gqa_compact_kernel(const __grid_constant__ CUtensorMap tmV,
+                                                                         const AttnParams P,
+                                                                         const __grid_constant__ RopeFreq fr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);   // [ltile]
-    __half* qa = reinterpret_cast<__half*>(smem + P.qa_off);          // [16][D + 8]
-    float* sc = reinterpret_cast<float*>(smem + P.sc_off);            // [G][L]
-    __half* pa = reinterpret_cast<__half*>(smem + P.pa_off);          // [16][L + 8]
-    float* st = reinterpret_cast<float*>(smem + P.st_off);            // [8][2]: max, denominator
-    __half* kr = reinterpret_cast<__half*>(smem + P.kr_off);          // [2][TP][R + 8]: rebuilt K hi, lo
-    float2* tb = reinterpret_cast<float2*>(smem + P.tb_off);          // [TP][R / 2]: cos, sin of t w_i
-    float2* an = reinterpret_cast<float2*>(smem + P.an_off);          // [R / 2]: cos, sin of j0 w_i
+    const int TP = P.tp;
+    const int R = P.rope_dim, HR = R / 2, KP = R + 8;
+    const int NA = TP / 8;   // offset table rows of 8 a w_i
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);    // [kCompactSlots]
+    __half* qa = reinterpret_cast<__half*>(smem + P.qa_off);           // [16][D + 8]
+    float* sc = reinterpret_cast<float*>(smem + P.sc_off);             // [2][8][TP]: rotated, pass-through
+    __half* pa = reinterpret_cast<__half*>(smem + P.pa_off);           // [16][TP + 8]
+    float* st = reinterpret_cast<float*>(smem + P.st_off);             // [3][8]: max, denominator, rescale
+    __half* kr = reinterpret_cast<__half*>(smem + P.kr_off);           // [2][TP][R + 8]
+    float2* an = reinterpret_cast<float2*>(smem + P.an_off);           // [ltile][HR]: tile anchors
+    float2* tlo = reinterpret_cast<float2*>(smem + P.tb_off);          // [8][HR]: b w_i
+    float2* thi = tlo + 8 * HR;                                         // [NA][HR]: 8 a w_i
+    float* gks = reinterpret_cast<float*>(thi + NA * HR);               // [R]: gamma_k of the rotated dims
     __shared__ int abort_flag;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int TP = P.tp;
-    const int L = P.ltile * TP;
-    const int QA = D + 8, PA = L + 8;
-    const int R = P.rope_dim, HR = R / 2, KP = R + 8;
-    const float* gk = P.g_k;
+    const int QA = D + 8, PA = TP + 8;
 
     if (!P.early) pdl_wait_trigger();
     const int p = P.pos[b];
@@ -794,74 +804,109 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_compact_kernel(const __gr
         if (P.early) pdl_wait_trigger();
         return;
     }
-    const int ntile = t1 - t0;   // <= ltile: every tile of the split gets its own slot
+    const int ntile = t1 - t0;   // <= ltile
     const int64_t row0 = (static_cast<int64_t>(b) * P.n_kv + g) * P.cap;
+    uint64_t policy = 0;
+    auto issue = [&](int kt) {
+        const int slot = kt % kCompactSlots;
+        uint8_t* dst = smem + static_cast<size_t>(slot) * P.tile_bytes;
+        fence_proxy_async_smem();   // generic writes to this slot (row refresh, zeroing) precede the TMA
+        mbar_arrive_expect_tx(&bars[slot], P.tile_bytes);
+        for (int j = 0; j < D / 64; ++j)
+            tma_load_2d(dst + j * TP * 128, &tmV, j * 64, static_cast<int32_t>(row0 + static_cast<int64_t>(t0 + kt) * TP),
+                        &bars[slot], policy);
+    };
     if (t == 0) {
         abort_flag = 0;
-        for (int i = 0; i < ntile; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kCompactSlots; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmV);
-        const uint64_t policy = l2_policy_evict_first();
-        for (int i = 0; i < ntile; ++i) {
-            uint8_t* dst = smem + static_cast<size_t>(i) * P.tile_bytes;
-            mbar_arrive_expect_tx(&bars[i], P.tile_bytes);
-            for (int j = 0; j < D / 64; ++j)
-                tma_load_2d(dst + j * TP * 128, &tmV, j * 64, static_cast<int32_t>(row0 + static_cast<int64_t>(t0 + i) * TP),
-                            &bars[i], policy);
-        }
+        policy = l2_policy_evict_first();
+        for (int kt = 0; kt < min(kCompactSlots, ntile); ++kt) issue(kt);
     }
-    // cos, sin of t * w_i for the offsets t inside a tile (the same for every tile)
-    for (int idx = t; idx < TP * HR; idx += kAttnThreads) {
-        const int tt = idx / HR, i = idx - tt * HR;
+    // rotation tables (positions only: before the wait): offsets b w_i, 8 a w_i and every tile's anchor
+    for (int idx = t; idx < (8 + NA) * HR; idx += kCompactThreads) {
+        const int r = idx / HR, i = idx - r * HR;
+        const double m = r < 8 ? static_cast<double>(r) : 8.0 * (r - 8);
         float c, sv;
-        rope_cos_sin(static_cast<double>(tt) * fr.w[i], c, sv);
-        tb[idx] = make_float2(c, sv);
+        rope_cos_sin(m * fr.w[i], c, sv);
+        tlo[idx] = make_float2(c, sv);   // tlo rows 0..7, then thi rows 0..NA-1 (contiguous)
+    }
+    for (int idx = t; idx < ntile * HR; idx += kCompactThreads) {
+        const int kt = idx / HR, i = idx - kt * HR;
+        float c, sv;
+        rope_cos_sin(static_cast<double>((t0 + kt) * TP) * fr.w[i], c, sv);
+        an[idx] = make_float2(c, sv);
     }
     if (P.early) pdl_wait_trigger();
 
     // query rows (normalised and rotated at p by the preceding launch): A operand rows h (hi) and
     // h + 8 (lo), scale folded in; the pass-through dims also carry gamma_k
-    for (int e = t; e < 8 * D; e += kAttnThreads) {
+    for (int e = t; e < 8 * D; e += kCompactThreads) {
         const int h = e / D, col = e - h * D;
         float v = 0.f;
         if (h < P.G) {
             v = P.q[b * P.ldq + static_cast<int64_t>(g * P.G + h) * D + col] * P.scale;
-            if (col >= R) v *= gk[col];
+            if (col >= R) v *= P.g_k[col];
         }
         __half hi, lo;
         split_hi_lo(v, hi, lo);
         qa[h * QA + col] = hi;
         qa[(h + 8) * QA + col] = lo;
     }
-    __syncthreads();
-    const int slot_p = p;
-
-    // ---- scores -----------------------------------------------------------------------------
-    const int gq = lane >> 2, tq = lane & 3;
-    for (int kt = 0; kt < ntile; ++kt) {
-        uint8_t* tile = smem + static_cast<size_t>(kt) * P.tile_bytes;
-        if (!mbar_wait(&bars[kt], 0u, P.status)) abort_flag = 1;
-        const int r = slot_p - (t0 + kt) * TP;   // the new row: written by the preceding launch
-        if (r >= 0 && r < TP)
-            for (int c = t * 8; c < D; c += kAttnThreads * 8)
-                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) = __ldcg(reinterpret_cast<const uint4*>(P.v_cache + (row0 + slot_p) * D + c));
-        if (t < HR) {   // anchor: the tile's first position
-            float c, sv;
-            rope_cos_sin(static_cast<double>((t0 + kt) * TP) * fr.w[t], c, sv);
-            an[t] = make_float2(c, sv);
+    for (int i = t; i < R; i += kCompactThreads) gks[i] = P.g_k[i];
+    for (int e = t; e < 8 * TP; e += kCompactThreads) {   // P rows of absent heads stay zero
+        const int h = e / TP, j = e - h * TP;
+        if (h >= P.G) {
+            pa[h * PA + j] = __float2half_rn(0.f);
+            pa[(h + 8) * PA + j] = __float2half_rn(0.f);
         }
+    }
+    if (t < 8) {
+        st[t] = -INFINITY;
+        st[8 + t] = 0.f;
+        st[16 + t] = 0.f;
+    }
+    __syncthreads();
+
+    const int gq = lane >> 2, tq = lane & 3;
+    constexpr int NPI = (D / 16 + kCompactWarps - 1) / kCompactWarps;   // 16-dim output items per warp
+    float acc[NPI][2][4];
+#pragma unroll
+    for (int i = 0; i < NPI; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc[i][h][0] = acc[i][h][1] = acc[i][h][2] = acc[i][h][3] = 0.f;
+
+    for (int kt = 0; kt < ntile; ++kt) {
+        const int slot = kt % kCompactSlots;
+        uint8_t* tile = smem + static_cast<size_t>(slot) * P.tile_bytes;
+        if (!mbar_wait(&bars[slot], static_cast<uint32_t>((kt / kCompactSlots) & 1), P.status)) abort_flag = 1;
+        const int j0 = (t0 + kt) * TP;
+        const int r = p - j0;   // the new row: written by the preceding launch
+        if (r >= 0 && r < TP)
+            for (int c = t * 8; c < D; c += kCompactThreads * 8)
+                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) =
+                    __ldcg(reinterpret_cast<const uint4*>(P.v_cache + (row0 + p) * D + c));
+        const int valid = T - j0;   // rows >= valid hold other slots: zero them (P V reads them)
+        if (valid < TP)
+            for (int e = t * 8; e < (TP - valid) * D; e += kCompactThreads * 8) {
+                const int rr = valid + e / D, c = e % D;
+                *reinterpret_cast<uint4*>(tile + swz(rr, c, TP)) = make_uint4(0, 0, 0, 0);
+            }
         __syncthreads();
         if (abort_flag) {
-            if (t == 0) for (int i = kt; i < ntile; ++i) (void)mbar_wait(&bars[i], 0u, nullptr);
+            if (t == 0) drain_stages(bars, kCompactSlots, kt, min(kt + kCompactSlots - 1, ntile - 1));
             return;
         }
-        // rebuilt K of the rotated dims, as binary16 hi + lo
-        for (int idx = t; idx < TP * HR; idx += kAttnThreads) {
+        // 1. rebuilt K of the rotated dims (hi + lo)
+        const float2* ak = an + kt * HR;
+        for (int idx = t; idx < TP * HR; idx += kCompactThreads) {
             const int tt = idx / HR, i = idx - tt * HR;
-            const float u = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i, TP))) * gk[i];
-            const float w = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i + HR, TP))) * gk[i + HR];
-            const float2 a0 = an[i], o = tb[idx];
-            const float c = a0.x * o.x - a0.y * o.y, sv = a0.y * o.x + a0.x * o.y;
+            const float u = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i, TP))) * gks[i];
+            const float w = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i + HR, TP))) * gks[i + HR];
+            const float2 a0 = ak[i], o1 = thi[(tt >> 3) * HR + i], o2 = tlo[(tt & 7) * HR + i];
+            const float c1 = a0.x * o1.x - a0.y * o1.y, s1 = a0.y * o1.x + a0.x * o1.y;
+            const float c = c1 * o2.x - s1 * o2.y, sv = s1 * o2.x + c1 * o2.y;
             const float k0 = u * c - w * sv, k1 = u * sv + w * c;
             __half h0, l0, h1, l1;
             split_hi_lo(k0, h0, l0);
@@ -872,45 +917,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_compact_kernel(const __gr
             kr[(TP + tt) * KP + i + HR] = l1;
         }
         __syncthreads();
-        const uint32_t tbase = smem_u32(tile), kbase = smem_u32(kr);
-        for (int n8 = warp; n8 < TP / 8; n8 += 4) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            const int brow = n8 * 8 + (lane & 7), bsel = ((lane >> 3) & 1) * 8;
-            for (int k16 = 0; k16 < R / 16; ++k16) {
-                uint32_t a0, a1, a2, a3, b0, b1, e0, e1;
-                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
-                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
-                ldmatrix_x2(b0, b1, kbase + static_cast<uint32_t>((brow * KP + k16 * 16 + bsel) * 2));
-                ldmatrix_x2(e0, e1, kbase + static_cast<uint32_t>(((TP + brow) * KP + k16 * 16 + bsel) * 2));
-                mma_16816(c, a0, a1, a2, a3, b0, b1);
-                mma_16816(c, a0, a1, a2, a3, e0, e1);
-            }
-            for (int k16 = R / 16; k16 < D / 16; ++k16) {
-                uint32_t a0, a1, a2, a3, b0, b1;
-                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
-                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + acol));
-                ldmatrix_x2(b0, b1, tbase + swz(brow, k16 * 16 + bsel, TP));
-                mma_16816(c, a0, a1, a2, a3, b0, b1);
-            }
-            if (gq < P.G) {
-                const int col = kt * TP + n8 * 8 + 2 * tq;
-                const int s0 = (t0 + kt) * TP + n8 * 8 + 2 * tq;
-                sc[gq * L + col] = s0 < T ? c[0] + c[2] : -INFINITY;
-                sc[gq * L + col + 1] = s0 + 1 < T ? c[1] + c[3] : -INFINITY;
+        // 2. scores: items (n8 tile, part), part 0 = rotated dims, 1 = pass-through dims
+        {
+            const uint32_t tbase = smem_u32(tile), kbase = smem_u32(kr);
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+            for (int item = warp; item < 2 * (TP / 8); item += kCompactWarps) {
+                const int part = item & 1, n8 = item >> 1;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                const int brow = n8 * 8 + (lane & 7), bsel = ((lane >> 3) & 1) * 8;
+                if (part == 0) {
+                    for (int k16 = 0; k16 < R / 16; ++k16) {
+                        uint32_t a0, a1, a2, a3, b0, b1, e0, e1;
+                        ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + k16 * 16 + (lane >> 4) * 8));
+                        ldmatrix_x2(b0, b1, kbase + static_cast<uint32_t>((brow * KP + k16 * 16 + bsel) * 2));
+                        ldmatrix_x2(e0, e1, kbase + static_cast<uint32_t>(((TP + brow) * KP + k16 * 16 + bsel) * 2));
+                        mma_16816(c, a0, a1, a2, a3, b0, b1);
+                        mma_16816(c, a0, a1, a2, a3, e0, e1);
+                    }
+                } else {
+                    for (int k16 = R / 16; k16 < D / 16; ++k16) {
+                        uint32_t a0, a1, a2, a3, b0, b1;
+                        ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + k16 * 16 + (lane >> 4) * 8));
+                        ldmatrix_x2(b0, b1, tbase + swz(brow, k16 * 16 + bsel, TP));
+                        mma_16816(c, a0, a1, a2, a3, b0, b1);
+                    }
+                }
+                const int col = n8 * 8 + 2 * tq;   // rows gq (hi) and gq + 8 (lo) of head gq
+                sc[(part * 8 + gq) * TP + col] = c[0] + c[2];
+                sc[(part * 8 + gq) * TP + col + 1] = c[1] + c[3];
             }
         }
-        __syncthreads();   // the rebuilt-K buffer and the anchors are reused by the next tile
-    }
-
-    // ---- softmax over the split (exact: max first) -------------------------------------------
-    const int Ls = ntile * TP;
-    for (int h = warp; h < 8; h += 4) {
-        float m = -INFINITY, l = 0.f;
-        if (h < P.G) {
-            for (int j = lane; j < Ls; j += 32) m = fmaxf(m, sc[h * L + j]);
-            m = warp_max(m);
-            for (int j = lane; j < Ls; j += 32) {
-                const float e = expf(sc[h * L + j] - m);
+        __syncthreads();
+        // 3. online softmax, warp h = query head h
+        if (warp < P.G) {
+            const int h = warp;
+            const float m_old = st[h];
+            float mt = -INFINITY;
+            for (int j = lane; j < TP; j += 32) {
+                const float sj = j < valid ? sc[h * TP + j] + sc[(8 + h) * TP + j] : -INFINITY;
+                sc[h * TP + j] = sj;
+                mt = fmaxf(mt, sj);
+            }
+            mt = warp_max(mt);
+            const float m_new = fmaxf(m_old, mt);
+            float l = 0.f;
+            for (int j = lane; j < TP; j += 32) {
+                const float e = expf(sc[h * TP + j] - m_new);   // (-inf rows: 0)
                 l += e;
                 __half hi, lo;
                 split_hi_lo(e, hi, lo);
@@ -918,78 +970,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_compact_kernel(const __gr
                 pa[(h + 8) * PA + j] = lo;
             }
             l = warp_sum(l);
-        } else {
-            for (int j = lane; j < Ls; j += 32) {
-                pa[h * PA + j] = __float2half_rn(0.f);
-                pa[(h + 8) * PA + j] = __float2half_rn(0.f);
+            if (lane == 0) {
+                const float alpha = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
+                st[h] = m_new;
+                st[8 + h] = st[8 + h] * alpha + l;
+                st[16 + h] = alpha;
             }
         }
-        if (lane == 0) {
-            st[2 * h] = m;
-            st[2 * h + 1] = l;
-        }
-    }
-    // rows of the last tile beyond the prefix hold other slots: zero them for P V
-    {
-        const int kt = ntile - 1, valid = T - (t0 + kt) * TP;
-        uint8_t* tile = smem + static_cast<size_t>(kt) * P.tile_bytes;
-        if (valid < TP)
-            for (int e = t * 8; e < (TP - valid) * D; e += kAttnThreads * 8) {
-                const int r = valid + e / D, c = e % D;
-                *reinterpret_cast<uint4*>(tile + swz(r, c, TP)) = make_uint4(0, 0, 0, 0);
-            }
-    }
-    __syncthreads();
-
-    // ---- P V from the resident tiles ----------------------------------------------------------
-    constexpr int NW = D / 32;  // n8 tiles of output dims per warp
-    float acc[NW][4];
+        __syncthreads();
+        // 4. rescale and accumulate P V for this warp's output dims
+        {
+            const float alpha = gq < P.G ? st[16 + gq] : 0.f;
+            const uint32_t tbase = smem_u32(tile);
 #pragma unroll
-    for (int n = 0; n < NW; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    for (int vt = 0; vt < ntile; ++vt) {
-        const uint32_t tbase = smem_u32(smem + static_cast<size_t>(vt) * P.tile_bytes);
-        for (int k16 = 0; k16 < TP / 16; ++k16) {
-            uint32_t a0, a1, a2, a3;
-            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = vt * TP + k16 * 16 + (lane >> 4) * 8;
-            ldmatrix_x4(a0, a1, a2, a3, smem_u32(pa + arow * PA + acol));
+            for (int pi = 0; pi < NPI; ++pi)
 #pragma unroll
-            for (int n = 0; n < NW; n += 2) {
-                const int d0 = (warp * NW + n) * 8;
-                uint32_t b0, b1, b2, b3;
-                const int vrow = k16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int vcol = d0 + (lane >> 4) * 8;
-                ldmatrix_x4_trans(b0, b1, b2, b3, tbase + swz(vrow, vcol, TP));
-                mma_16816(acc[n], a0, a1, a2, a3, b0, b1);
-                mma_16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) acc[pi][h][q4] *= alpha;
+            for (int k16 = 0; k16 < TP / 16; ++k16) {
+                uint32_t a0, a1, a2, a3;
+                const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
+                ldmatrix_x4(a0, a1, a2, a3, smem_u32(pa + arow * PA + acol));
+#pragma unroll
+                for (int pi = 0; pi < NPI; ++pi) {
+                    const int item = warp + pi * kCompactWarps;
+                    if (item < D / 16) {
+                        uint32_t b0, b1, b2, b3;
+                        const int vrow = k16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const int vcol = item * 16 + (lane >> 4) * 8;
+                        ldmatrix_x4_trans(b0, b1, b2, b3, tbase + swz(vrow, vcol, TP));
+                        mma_16816(acc[pi][0], a0, a1, a2, a3, b0, b1);
+                        mma_16816(acc[pi][1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
             }
         }
+        __syncthreads();   // the slot, the scores and P are free
+        if (t == 0 && kt + kCompactSlots < ntile) issue(kt + kCompactSlots);
     }
 
     // ---- output ------------------------------------------------------------------------------
     if (gq < P.G) {
         const int h = g * P.G + gq;
-        const float m = st[2 * gq], l = st[2 * gq + 1];
-        if (nsplit == 1) {
-            float* o = P.out + b * P.ldo + static_cast<int64_t>(h) * D;
-            const float inv = 1.f / l;
+        const float m = st[gq], l = st[8 + gq];
+        float* o = nsplit == 1 ? P.out + b * P.ldo + static_cast<int64_t>(h) * D
+                               : P.part + ((static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max + split) * (D + 2);
+        const float inv = nsplit == 1 ? 1.f / l : 1.f;
 #pragma unroll
-            for (int n = 0; n < NW; ++n) {
-                const int dd = (warp * NW + n) * 8 + 2 * tq;
-                o[dd] = (acc[n][0] + acc[n][2]) * inv;
-                o[dd + 1] = (acc[n][1] + acc[n][3]) * inv;
-            }
-        } else {
-            float* o = P.part + ((static_cast<int64_t>(b) * P.n_q + h) * P.nsplit_max + split) * (D + 2);
+        for (int pi = 0; pi < NPI; ++pi) {
+            const int item = warp + pi * kCompactWarps;
+            if (item < D / 16) {
 #pragma unroll
-            for (int n = 0; n < NW; ++n) {
-                const int dd = (warp * NW + n) * 8 + 2 * tq;
-                o[dd] = acc[n][0] + acc[n][2];
-                o[dd + 1] = acc[n][1] + acc[n][3];
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int dd = item * 16 + hh * 8 + 2 * tq;
+                    o[dd] = (acc[pi][hh][0] + acc[pi][hh][2]) * inv;
+                    o[dd + 1] = (acc[pi][hh][1] + acc[pi][hh][3]) * inv;
+                }
             }
-            if (warp == 0 && tq == 0) {
-                o[D] = m;
-                o[D + 1] = l;
-            }
+        }
+        if (nsplit > 1 && warp == 0 && tq == 0) {
+            o[D] = m;
+            o[D + 1] = l;
         }
     }
 }
@@ -1278,34 +1320,34 @@ struct CompactPlan {
     size_t smem, ws;
 };
 
-// The largest number of resident tiles per split that fits the device's shared memory, and
-// enough splits to give every SM at least one.  ok = false when no layout fits.
+// About one CTA per SM over the (sequence, KV head) pairs, more splits where a split's tile
+// anchors would not fit shared memory.  ok = false when no layout fits.
 bool compact_plan(int B, int n_q, int n_kv, int d, int64_t cap, int R, int num_sms, size_t smem_optin,
                   CompactPlan& pl) {
+    (void)n_q;
     pl = CompactPlan{};
     pl.tp = tile_slots(d);
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);
     const int64_t nt_max = std::max<int64_t>(1, (cap + pl.tp - 1) / pl.tp);
-    const int G = n_q / n_kv;
+    const int HR = R / 2;
     auto layout = [&](int lt, bool commit) -> size_t {
-        const int L = lt * pl.tp;
-        size_t off = static_cast<size_t>(lt) * pl.tile_bytes;
+        size_t off = static_cast<size_t>(kCompactSlots) * pl.tile_bytes;
         const size_t bar = off;
-        off = align_up(off + static_cast<size_t>(lt) * 8, 128);
+        off = align_up(off + kCompactSlots * 8, 128);
         const size_t qa = off;
         off = align_up(off + 16ull * (d + 8) * 2, 128);
         const size_t sc = off;
-        off = align_up(off + static_cast<size_t>(G) * L * 4, 128);
+        off = align_up(off + 2ull * 8 * pl.tp * 4, 128);
         const size_t pa = off;
-        off = align_up(off + 16ull * (L + 8) * 2, 128);
+        off = align_up(off + 16ull * (pl.tp + 8) * 2, 128);
         const size_t st = off;
-        off = align_up(off + 16 * 4, 128);
+        off = align_up(off + 3 * 8 * 4, 128);
         const size_t kr = off;
         off = align_up(off + 2ull * pl.tp * (R + 8) * 2, 128);
-        const size_t tb = off;
-        off = align_up(off + static_cast<size_t>(pl.tp) * (R / 2) * 8, 128);
+        const size_t tb = off;   // offsets b w_i (8 rows), 8 a w_i (tp / 8 rows), then gamma_k[R]
+        off = align_up(off + static_cast<size_t>(8 + pl.tp / 8) * HR * 8 + static_cast<size_t>(R) * 4, 128);
         const size_t an = off;
-        off += static_cast<size_t>(R / 2) * 8;
+        off += static_cast<size_t>(lt) * HR * 8;
         if (commit) {
             pl.bar_off = static_cast<uint32_t>(bar);
             pl.qa_off = static_cast<uint32_t>(qa);
@@ -1318,14 +1360,10 @@ bool compact_plan(int B, int n_q, int n_kv, int d, int64_t cap, int R, int num_s
         }
         return align_up(off, 1024) + 1024;
     };
-    int lmax = 0;
-    for (int lt = 1; lt <= 64; ++lt)   // (the kernel's static shared memory is a few bytes)
-        if (layout(lt, false) + 64 <= smem_optin) lmax = lt;
-    if (lmax == 0) return false;
-    int64_t ns = (nt_max + lmax - 1) / lmax;
-    ns = std::max<int64_t>(ns, std::min<int64_t>(nt_max, (num_sms + static_cast<int64_t>(B) * n_kv - 1) /
-                                                              (static_cast<int64_t>(B) * n_kv)));
-    if (ns > kMaxSplits) return false;
+    const int64_t pairs = static_cast<int64_t>(B) * n_kv;
+    int64_t ns = std::max<int64_t>(1, std::min<int64_t>(nt_max, (num_sms + pairs - 1) / pairs));
+    while (ns <= nt_max && layout(static_cast<int>((nt_max + ns - 1) / ns), false) + 2048 > smem_optin) ++ns;
+    if (ns > nt_max || ns > kMaxSplits) return false;
     pl.ns = static_cast<int>(ns);
     pl.ltile = static_cast<int>((nt_max + ns - 1) / ns);
     pl.smem = layout(pl.ltile, true);
@@ -1420,7 +1458,7 @@ gem_status compact_enqueue(const CompactAttnOp& op, cudaStream_t stream, bool ea
     const void* fn = pick_compact(op.d);
     if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
     void* args[] = {&tmV, &P, &fr};
-    if ((st = launch_pdl(fn, dim3(pl.ns, op.n_kv, op.B), dim3(kAttnThreads), pl.smem, stream, args)) != GEM_OK)
+    if ((st = launch_pdl(fn, dim3(pl.ns, op.n_kv, op.B), dim3(kCompactThreads), pl.smem, stream, args)) != GEM_OK)
         return st;
     if (pl.ns > 1) {
         int D = op.d;

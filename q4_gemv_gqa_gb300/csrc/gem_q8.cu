@@ -27,9 +27,13 @@ namespace gem {
 namespace {
 
 constexpr int kQ8Block = 34;
-constexpr int kQ8RowsPerWarp = 4;
-constexpr int kQ8ChunkBlocks = 16;          // a K-chunk: 512 weights = 544 bytes per row
-constexpr int kQ8RingBytes = 8 * 8 * kQ8RowsPerWarp * kQ8ChunkBlocks * kQ8Block;   // 139,264
+// A stage: each consumer warp's rows x one K-chunk.  Up to two activation rows: 2 rows per warp
+// and chunks of 32 blocks (1088 contiguous bytes per row: short per-row runs cost HBM
+// throughput); more rows: 4 rows per warp and 16-block chunks, so each activation load from L1
+// serves more weights.  Either way a stage is 34,816 (16 warps) or 17,408 bytes (8 warps).
+__host__ __device__ constexpr int q8_rows_per_warp(int bmax) { return bmax <= 2 ? 2 : 4; }
+__host__ __device__ constexpr int q8_chunk_blocks(int bmax) { return bmax <= 2 ? 32 : 16; }
+constexpr int kQ8RingBytes = 139264;   // 4 stages of 16 warps' rows, 8 of 8 warps' rows
 // consumer warps (four rows of a tile each): 16 for up to two activation rows, else 8
 __host__ __device__ constexpr int q8_warps(int bmax) { return bmax <= 2 ? 16 : 8; }
 
@@ -69,11 +73,17 @@ template <int BMAX>
 __global__ void __launch_bounds__((q8_warps(BMAX) + 1) * 32, 1) q8_0_gemv_kernel(const Q8Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kQ8Warps = q8_warps(BMAX);
+    constexpr int kQ8RowsPerWarp = q8_rows_per_warp(BMAX);
+    constexpr int kQ8ChunkBlocks = q8_chunk_blocks(BMAX);
     constexpr int kQ8TileRows = kQ8Warps * kQ8RowsPerWarp;
     constexpr uint32_t kStageBytes = kQ8TileRows * kQ8ChunkBlocks * kQ8Block;
     constexpr int kQ8MaxStages = kQ8RingBytes / kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQ8MaxStages * kStageBytes);
     uint64_t* empty = full + kQ8MaxStages;
+    // up to two activation rows stay resident in shared memory for the whole call; more rows are
+    // read through L1
+    constexpr bool kXRes = BMAX <= 2;
+    float* xs = reinterpret_cast<float*>(smem + kQ8MaxStages * kStageBytes + 2 * kQ8MaxStages * 8);
     __shared__ int any_failed;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ns = p.ns;
@@ -119,6 +129,13 @@ __global__ void __launch_bounds__((q8_warps(BMAX) + 1) * 32, 1) q8_0_gemv_kernel
     }
 
     pdl_wait_trigger();   // the activations come from the previous kernel
+    if constexpr (kXRes) {
+        const int n4 = p.K / 4;
+        for (int bb = 0; bb < p.B; ++bb)
+            for (int i = tid; i < n4; i += kQ8Warps * 32)
+                reinterpret_cast<float4*>(xs + bb * p.K)[i] = __ldg(reinterpret_cast<const float4*>(p.x + bb * p.ldx) + i);
+        asm volatile("bar.sync 1, %0;" ::"r"(kQ8Warps * 32) : "memory");
+    }
     bool ok = true;
     int s = 0, slot = 0;
     uint32_t par = 0;
@@ -139,11 +156,16 @@ __global__ void __launch_bounds__((q8_warps(BMAX) + 1) * 32, 1) q8_0_gemv_kernel
                 const uint32_t st = smem_u32(smem) + static_cast<uint32_t>(slot) * kStageBytes +
                                     static_cast<uint32_t>(kQ8RowsPerWarp * warp) * kRowChunk;
                 const float4* xc = reinterpret_cast<const float4*>(p.x + static_cast<int64_t>(c) * kQ8ChunkBlocks * 32);
+                const float4* xr = reinterpret_cast<const float4*>(xs + c * kQ8ChunkBlocks * 32);
                 for (int blk = bl; blk < nb; blk += 4) {
                     float4 xv[BMAX];
 #pragma unroll
-                    for (int bb = 0; bb < BMAX; ++bb)
-                        if (bb < B) xv[bb] = __ldg(xc + bb * (p.ldx >> 2) + blk * 8 + m);
+                    for (int bb = 0; bb < BMAX; ++bb) {
+                        if (bb < B) {
+                            if constexpr (kXRes) xv[bb] = xr[bb * (p.K >> 2) + blk * 8 + m];
+                            else xv[bb] = __ldg(xc + bb * (p.ldx >> 2) + blk * 8 + m);
+                        }
+                    }
 #pragma unroll
                     for (int rr = 0; rr < kQ8RowsPerWarp; ++rr) {
                         const uint32_t a = st + rr * kRowChunk + blk * kQ8Block;
@@ -216,6 +238,7 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* y, int
     const int64_t lo = (N * c) / nchunk, hi = (N * (c + 1)) / nchunk;
     float bv = 0.f;
     int bi = -1;
+#pragma unroll 8
     for (int64_t i = lo + tid; i < hi; i += kArgThreads) {   // increasing i: ties keep the first
         const float v = __ldg(row + i);
         if (!isnan(v) && (bi < 0 || v > bv)) {
@@ -282,7 +305,8 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* y, int
     }
 }
 
-int argmax_chunks(int64_t N) { return static_cast<int>(std::min<int64_t>(256, std::max<int64_t>(1, (N + 8191) / 8192))); }
+// chunks of 2048 values (8 per thread): about one CTA per SM at the 262,144-entry vocabulary
+int argmax_chunks(int64_t N) { return static_cast<int>(std::min<int64_t>(1024, std::max<int64_t>(1, (N + 2047) / 2048))); }
 
 gem_status ensure_smem_q8(const void* fn, int device, size_t bytes) {
     static std::mutex mu;
@@ -324,20 +348,23 @@ gem_status gem_q8_0_gemv(const void* W, int64_t N, int64_t K, const float* x, in
     p.B = B;
     p.y = y;
     p.ldy = ldy;
-    p.nchunk = static_cast<int>((K / 32 + kQ8ChunkBlocks - 1) / kQ8ChunkBlocks);
-    p.status = di.status_word;
     const int bmax = B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8));
+    p.nchunk = static_cast<int>((K / 32 + q8_chunk_blocks(bmax) - 1) / q8_chunk_blocks(bmax));
+    p.status = di.status_word;
     const int nw = q8_warps(bmax);
-    const size_t stage = static_cast<size_t>(nw) * kQ8RowsPerWarp * kQ8ChunkBlocks * kQ8Block;
+    const size_t stage = static_cast<size_t>(nw) * q8_rows_per_warp(bmax) * q8_chunk_blocks(bmax) * kQ8Block;
     p.ns = static_cast<int>(kQ8RingBytes / stage);
-    const size_t smem = kQ8RingBytes + 2 * static_cast<size_t>(p.ns) * 8;
+    // the ring, its barriers (sized for the most stages any instance has), then x for up to two rows
+    const size_t stage8 = static_cast<size_t>(q8_warps(8)) * q8_rows_per_warp(8) * q8_chunk_blocks(8) * kQ8Block;
+    const size_t smem = kQ8RingBytes + 2 * (kQ8RingBytes / std::min(stage, stage8)) * 8 +
+                        (bmax <= 2 ? static_cast<size_t>(bmax) * K * 4 : 0);
     if (smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
     const void* fn = bmax == 1 ? reinterpret_cast<const void*>(q8_0_gemv_kernel<1>)
                      : bmax == 2 ? reinterpret_cast<const void*>(q8_0_gemv_kernel<2>)
                      : bmax == 4 ? reinterpret_cast<const void*>(q8_0_gemv_kernel<4>)
                                  : reinterpret_cast<const void*>(q8_0_gemv_kernel<8>);
     if ((st = ensure_smem_q8(fn, di.device, smem)) != GEM_OK) return st;
-    const int64_t ntiles = (N + nw * kQ8RowsPerWarp - 1) / (nw * kQ8RowsPerWarp);
+    const int64_t ntiles = (N + nw * q8_rows_per_warp(bmax) - 1) / (nw * q8_rows_per_warp(bmax));
     const int grid = static_cast<int>(std::min<int64_t>(ntiles, di.num_sms));
     void* args[] = {&p};
     return launch_pdl(fn, dim3(grid), dim3((nw + 1) * 32), smem, static_cast<cudaStream_t>(stream), args);

@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
 // V * key_norm, rotated at the row's own position: K_j = RoPE_j(V_j * gamma_k).  Half the
 // bytes of the standard layout per cached position.
 //
-// One CTA of 8 warps per split of the prefix streams the split's V tiles (TP slots x D) through
+// One CTA of 16 warps per split of the prefix streams the split's V tiles (TP slots x D) through
 // a ring of kCompactSlots TMA stages, each V byte read once.  Per tile:
 //   1. the rotated dims of K are rebuilt in shared memory as binary16 hi + lo: fp32 rotation by
 //      cos / sin of (j0 + t) w_i = tile anchor (fp64-reduced angle of the tile's first position,
@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
 //   4. each warp rescales its output accumulators and adds P V for its output dims.
 // The split's state (unnormalised output, max, denominator) goes to the workspace and the
 // ordered merge kernel combines the splits in ascending order (deterministic).
-constexpr int kCompactWarps = 8;
+constexpr int kCompactWarps = 16;
 constexpr int kCompactThreads = kCompactWarps * 32;
 constexpr int kCompactSlots = 4;
 
@@ -776,14 +776,15 @@ __global__ void __launch_bounds__(kCompactThreads, 1) gqa_compact_kernel(const _
     const int NA = TP / 8;   // offset table rows of 8 a w_i
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);    // [kCompactSlots]
     __half* qa = reinterpret_cast<__half*>(smem + P.qa_off);           // [16][D + 8]
-    float* sc = reinterpret_cast<float*>(smem + P.sc_off);             // [2][8][TP]: rotated, pass-through
+    float* sc = reinterpret_cast<float*>(smem + P.sc_off);             // [16 / (TP / 16)][8][TP]: partial scores
     __half* pa = reinterpret_cast<__half*>(smem + P.pa_off);           // [16][TP + 8]
     float* st = reinterpret_cast<float*>(smem + P.st_off);             // [3][8]: max, denominator, rescale
     __half* kr = reinterpret_cast<__half*>(smem + P.kr_off);           // [2][TP][R + 8]
     float2* an = reinterpret_cast<float2*>(smem + P.an_off);           // [ltile][HR]: tile anchors
     float2* tlo = reinterpret_cast<float2*>(smem + P.tb_off);          // [8][HR]: b w_i
     float2* thi = tlo + 8 * HR;                                         // [NA][HR]: 8 a w_i
-    float* gks = reinterpret_cast<float*>(thi + NA * HR);               // [R]: gamma_k of the rotated dims
+    float2* toff = thi + NA * HR;                                       // [TP][HR]: t w_i = 8 a w_i + b w_i
+    float* gks = reinterpret_cast<float*>(toff + TP * HR);              // [R]: gamma_k of the rotated dims
     __shared__ int abort_flag;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -855,6 +856,12 @@ __global__ void __launch_bounds__(kCompactThreads, 1) gqa_compact_kernel(const _
         qa[(h + 8) * QA + col] = lo;
     }
     for (int i = t; i < R; i += kCompactThreads) gks[i] = P.g_k[i];
+    __syncthreads();   // the offset tables are complete
+    for (int idx = t; idx < TP * HR; idx += kCompactThreads) {   // one rotation per row offset t
+        const int tt = idx / HR, i = idx - tt * HR;
+        const float2 o1 = thi[(tt >> 3) * HR + i], o2 = tlo[(tt & 7) * HR + i];
+        toff[idx] = make_float2(o1.x * o2.x - o1.y * o2.y, o1.y * o2.x + o1.x * o2.y);
+    }
     for (int e = t; e < 8 * TP; e += kCompactThreads) {   // P rows of absent heads stay zero
         const int h = e / TP, j = e - h * TP;
         if (h >= P.G) {
@@ -898,54 +905,80 @@ __global__ void __launch_bounds__(kCompactThreads, 1) gqa_compact_kernel(const _
             if (t == 0) drain_stages(bars, kCompactSlots, kt, min(kt + kCompactSlots - 1, ntile - 1));
             return;
         }
-        // 1. rebuilt K of the rotated dims (hi + lo)
+        // 1. rebuilt K of the rotated dims (hi + lo): warp rows, two adjacent dims per lane (R is a
+        // multiple of 16, so dims i, i + 1 share a 16-byte chunk of the swizzled tile)
         const float2* ak = an + kt * HR;
-        for (int idx = t; idx < TP * HR; idx += kCompactThreads) {
-            const int tt = idx / HR, i = idx - tt * HR;
-            const float u = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i, TP))) * gks[i];
-            const float w = __half2float(*reinterpret_cast<const __half*>(tile + swz(tt, i + HR, TP))) * gks[i + HR];
-            const float2 a0 = ak[i], o1 = thi[(tt >> 3) * HR + i], o2 = tlo[(tt & 7) * HR + i];
-            const float c1 = a0.x * o1.x - a0.y * o1.y, s1 = a0.y * o1.x + a0.x * o1.y;
-            const float c = c1 * o2.x - s1 * o2.y, sv = s1 * o2.x + c1 * o2.y;
-            const float k0 = u * c - w * sv, k1 = u * sv + w * c;
-            __half h0, l0, h1, l1;
-            split_hi_lo(k0, h0, l0);
-            split_hi_lo(k1, h1, l1);
-            kr[tt * KP + i] = h0;
-            kr[tt * KP + i + HR] = h1;
-            kr[(TP + tt) * KP + i] = l0;
-            kr[(TP + tt) * KP + i + HR] = l1;
+        for (int tt = warp; tt < TP; tt += kCompactWarps) {
+            const float2* ro = toff + tt * HR;
+            for (int i = 2 * lane; i < HR; i += 64) {
+                const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(tile + swz(tt, i, TP)));
+                const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(tile + swz(tt, i + HR, TP)));
+                const float2 gu = *reinterpret_cast<const float2*>(gks + i);
+                const float2 gw = *reinterpret_cast<const float2*>(gks + i + HR);
+                const float4 a01 = *reinterpret_cast<const float4*>(ak + i);   // anchors of dims i, i + 1
+                const float4 o01 = *reinterpret_cast<const float4*>(ro + i);   // row offsets of dims i, i + 1
+                const float c0 = a01.x * o01.x - a01.y * o01.y, s0 = a01.y * o01.x + a01.x * o01.y;
+                const float c1 = a01.z * o01.z - a01.w * o01.w, s1 = a01.w * o01.z + a01.z * o01.w;
+                const float u0 = uf.x * gu.x, u1 = uf.y * gu.y, w0 = wf.x * gw.x, w1 = wf.y * gw.y;
+                const float ka0 = u0 * c0 - w0 * s0, ka1 = u1 * c1 - w1 * s1;   // dims i, i + 1
+                const float kb0 = u0 * s0 + w0 * c0, kb1 = u1 * s1 + w1 * c1;   // dims i + HR, i + HR + 1
+                const __half2 ha = __floats2half2_rn(ka0, ka1), hb = __floats2half2_rn(kb0, kb1);
+                const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+                const __half2 la = __floats2half2_rn(ka0 - fa.x, ka1 - fa.y), lb = __floats2half2_rn(kb0 - fb.x, kb1 - fb.y);
+                *reinterpret_cast<__half2*>(kr + tt * KP + i) = ha;
+                *reinterpret_cast<__half2*>(kr + tt * KP + i + HR) = hb;
+                *reinterpret_cast<__half2*>(kr + (TP + tt) * KP + i) = la;
+                *reinterpret_cast<__half2*>(kr + (TP + tt) * KP + i + HR) = lb;
+            }
         }
         __syncthreads();
-        // 2. scores: items (n8 tile, part), part 0 = rotated dims, 1 = pass-through dims
+        // 2. scores: item = (16 positions, one of NKS cost-balanced parts of the k16 steps); a
+        // rotated step takes two mma (hi and lo), a pass-through step one.  Each q fragment loaded
+        // serves two n8 tiles; two accumulator pairs halve the dependent mma chains.
         {
             const uint32_t tbase = smem_u32(tile), kbase = smem_u32(kr);
-            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
-            for (int item = warp; item < 2 * (TP / 8); item += kCompactWarps) {
-                const int part = item & 1, n8 = item >> 1;
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
-                const int brow = n8 * 8 + (lane & 7), bsel = ((lane >> 3) & 1) * 8;
-                if (part == 0) {
-                    for (int k16 = 0; k16 < R / 16; ++k16) {
-                        uint32_t a0, a1, a2, a3, b0, b1, e0, e1;
-                        ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + k16 * 16 + (lane >> 4) * 8));
-                        ldmatrix_x2(b0, b1, kbase + static_cast<uint32_t>((brow * KP + k16 * 16 + bsel) * 2));
-                        ldmatrix_x2(e0, e1, kbase + static_cast<uint32_t>(((TP + brow) * KP + k16 * 16 + bsel) * 2));
-                        mma_16816(c, a0, a1, a2, a3, b0, b1);
-                        mma_16816(c, a0, a1, a2, a3, e0, e1);
-                    }
+            const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
+            const int brow = (lane & 7) + ((lane >> 4) << 3), bcol = ((lane >> 3) & 1) * 8;
+            const int nrot = R / 16, nk = D / 16, cost = nk + nrot;
+            const int NP = TP / 16, NKS = kCompactWarps / NP;   // NP * NKS = kCompactWarps items
+            const int item = warp, np = item % NP, ks = item / NP;
+            // k16 range of part ks: the first step whose cumulative cost reaches ks * cost / NKS
+            auto kstart = [&](int q) {
+                const int c = (q * cost + NKS - 1) / NKS;   // cost before the part
+                return 2 * nrot >= c ? (c + 1) / 2 : nrot + (c - 2 * nrot);
+            };
+            const int kb = kstart(ks), ke = ks + 1 == NKS ? nk : kstart(ks + 1);
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+            const int r16 = np * 16 + brow;
+            for (int k16 = kb; k16 < ke; ++k16) {
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + k16 * 16 + acol));
+                if (k16 < nrot) {
+                    uint32_t f0, f1, f2, f3;
+                    ldmatrix_x4(b0, b1, b2, b3, kbase + static_cast<uint32_t>((r16 * KP + k16 * 16 + bcol) * 2));
+                    ldmatrix_x4(f0, f1, f2, f3, kbase + static_cast<uint32_t>(((TP + r16) * KP + k16 * 16 + bcol) * 2));
+                    mma_16816(c0, a0, a1, a2, a3, b0, b1);
+                    mma_16816(c1, a0, a1, a2, a3, b2, b3);
+                    mma_16816(e0, a0, a1, a2, a3, f0, f1);
+                    mma_16816(e1, a0, a1, a2, a3, f2, f3);
                 } else {
-                    for (int k16 = R / 16; k16 < D / 16; ++k16) {
-                        uint32_t a0, a1, a2, a3, b0, b1;
-                        ldmatrix_x4(a0, a1, a2, a3, smem_u32(qa + arow * QA + k16 * 16 + (lane >> 4) * 8));
-                        ldmatrix_x2(b0, b1, tbase + swz(brow, k16 * 16 + bsel, TP));
-                        mma_16816(c, a0, a1, a2, a3, b0, b1);
+                    ldmatrix_x4(b0, b1, b2, b3, tbase + swz(r16, k16 * 16 + bcol, TP));
+                    if (k16 & 1) {
+                        mma_16816(e0, a0, a1, a2, a3, b0, b1);
+                        mma_16816(e1, a0, a1, a2, a3, b2, b3);
+                    } else {
+                        mma_16816(c0, a0, a1, a2, a3, b0, b1);
+                        mma_16816(c1, a0, a1, a2, a3, b2, b3);
                     }
                 }
-                const int col = n8 * 8 + 2 * tq;   // rows gq (hi) and gq + 8 (lo) of head gq
-                sc[(part * 8 + gq) * TP + col] = c[0] + c[2];
-                sc[(part * 8 + gq) * TP + col + 1] = c[1] + c[3];
             }
+            // rows gq (hi) and gq + 8 (lo) of head gq; positions 16 np + 2 tq (+1), and + 8
+            float* sp = sc + (ks * 8 + gq) * TP + np * 16 + 2 * tq;
+            sp[0] = (c0[0] + c0[2]) + (e0[0] + e0[2]);
+            sp[1] = (c0[1] + c0[3]) + (e0[1] + e0[3]);
+            sp[8] = (c1[0] + c1[2]) + (e1[0] + e1[2]);
+            sp[9] = (c1[1] + c1[3]) + (e1[1] + e1[3]);
         }
         __syncthreads();
         // 3. online softmax, warp h = query head h
@@ -953,8 +986,13 @@ __global__ void __launch_bounds__(kCompactThreads, 1) gqa_compact_kernel(const _
             const int h = warp;
             const float m_old = st[h];
             float mt = -INFINITY;
+            const int nks = kCompactWarps / (TP / 16);
             for (int j = lane; j < TP; j += 32) {
-                const float sj = j < valid ? sc[h * TP + j] + sc[(8 + h) * TP + j] : -INFINITY;
+                float sj = -INFINITY;
+                if (j < valid) {
+                    sj = 0.f;
+                    for (int q = 0; q < nks; ++q) sj += sc[(q * 8 + h) * TP + j];
+                }
                 sc[h * TP + j] = sj;
                 mt = fmaxf(mt, sj);
             }
@@ -980,14 +1018,16 @@ __global__ void __launch_bounds__(kCompactThreads, 1) gqa_compact_kernel(const _
         __syncthreads();
         // 4. rescale and accumulate P V for this warp's output dims
         {
-            const float alpha = gq < P.G ? st[16 + gq] : 0.f;
+            const float alpha = gq < P.G ? st[16 + gq] : 1.f;   // (rows of absent heads stay zero)
             const uint32_t tbase = smem_u32(tile);
+            if (!__all_sync(0xffffffffu, alpha == 1.f)) {   // a maximum moved (or the first tile)
 #pragma unroll
-            for (int pi = 0; pi < NPI; ++pi)
+                for (int pi = 0; pi < NPI; ++pi)
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) acc[pi][h][q4] *= alpha;
+                        for (int q4 = 0; q4 < 4; ++q4) acc[pi][h][q4] *= alpha;
+            }
             for (int k16 = 0; k16 < TP / 16; ++k16) {
                 uint32_t a0, a1, a2, a3;
                 const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = k16 * 16 + (lane >> 4) * 8;
@@ -1336,16 +1376,16 @@ bool compact_plan(int B, int n_q, int n_kv, int d, int64_t cap, int R, int num_s
         off = align_up(off + kCompactSlots * 8, 128);
         const size_t qa = off;
         off = align_up(off + 16ull * (d + 8) * 2, 128);
-        const size_t sc = off;
-        off = align_up(off + 2ull * 8 * pl.tp * 4, 128);
+        const size_t sc = off;   // kCompactWarps / (tp / 16) partial score blocks of 8 x tp floats
+        off = align_up(off + static_cast<size_t>(kCompactWarps) * 16 * 8 * 4, 128);
         const size_t pa = off;
         off = align_up(off + 16ull * (pl.tp + 8) * 2, 128);
         const size_t st = off;
         off = align_up(off + 3 * 8 * 4, 128);
         const size_t kr = off;
         off = align_up(off + 2ull * pl.tp * (R + 8) * 2, 128);
-        const size_t tb = off;   // offsets b w_i (8 rows), 8 a w_i (tp / 8 rows), then gamma_k[R]
-        off = align_up(off + static_cast<size_t>(8 + pl.tp / 8) * HR * 8 + static_cast<size_t>(R) * 4, 128);
+        const size_t tb = off;   // offsets b w_i (8 rows), 8 a w_i (tp / 8 rows), t w_i (tp rows), gamma_k[R]
+        off = align_up(off + static_cast<size_t>(8 + pl.tp / 8 + pl.tp) * HR * 8 + static_cast<size_t>(R) * 4, 128);
         const size_t an = off;
         off += static_cast<size_t>(lt) * HR * 8;
         if (commit) {

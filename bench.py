@@ -152,18 +152,18 @@ class Clocks:
 
     def run_timed(self, torch, enqueue, steps, stream):
         """Record an event, enqueue `steps` units of work, record an event, and sample the clocks
-        until the second event has completed.  Returns the elapsed milliseconds."""
+        while the queued work runs, until the second event has completed.  Returns the elapsed
+        milliseconds.  Nothing is sampled between the launches: a sample takes the host long
+        enough to leave the GPU idle between steps."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        every = max(1, steps // 50)
         e0.record(stream)
-        for i in range(steps):
+        for _ in range(steps):
             enqueue()
-            if i % every == 0:
-                self.sample()
         e1.record(stream)
+        self.sample()   # the region's start (the queued steps are running)
         while not e1.query():
             self.sample()
-            time.sleep(0.001)
+            time.sleep(0.0005)
         self.sample()   # the region's end
         return e0.elapsed_time(e1)
 

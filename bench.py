@@ -461,6 +461,15 @@ def run_kernel_only(args):
         res["shape"] = {"N": N, "K": K, "B": B}
         mats = [torch.from_numpy(gem_synth.q4_0_matrix(0, 5000 + i, N, K)).cuda()
                 for i in range(args.mats)]
+        if args.cuda_core:
+            # weights 2 bytes off a 16-byte boundary: the library's general CUDA-core kernel (one
+            # warp per row, plain loads), the comparison point for the tensor-core path
+            def shifted(W):
+                buf = torch.empty(W.numel() + 16, dtype=torch.uint8, device="cuda")
+                buf[2:2 + W.numel()].copy_(W.reshape(-1))
+                return buf[2:2 + W.numel()]
+            mats = [shifted(W) for W in mats]
+            res["path"] = "cuda-core (general kernel)"
         x = torch.from_numpy(gem_synth.normal_f32(0, 6000, (B, K))).cuda()
         y = torch.empty((B, N), device="cuda")
         ws = torch.empty(max(1, gem.q4_0_gemv_workspace(B, K)), dtype=torch.uint8, device="cuda")
@@ -833,6 +842,8 @@ def main():
     ap.add_argument("--batch", type=int, default=1,
                     help="--kernel gemv: activation rows (9..32: the batched prefill GEMM)")
     ap.add_argument("--mats", type=int, default=8, help="--kernel gemv: rotated matrices")
+    ap.add_argument("--cuda-core", action="store_true",
+                    help="--kernel gemv: misaligned weights, so the general CUDA-core kernel runs")
     ap.add_argument("--cache", choices=["standard", "compact"], default="compact",
                     help="--kernel attn_full: the full-attention layer's cache layout")
     ap.add_argument("--gemv-shape", choices=["up", "down"], default="up",

@@ -82,6 +82,8 @@ def lib():
             L.gem_oracle_argmax.restype = C.c_int64
             L.gem_oracle_argmax.argtypes = [p, C.c_int64]
             L.gem_oracle_q8_0_dequant.argtypes = [p, C.c_int64, C.c_int64, p]
+            L.gem_oracle_topk.restype = C.c_int
+            L.gem_oracle_topk.argtypes = [p, C.c_int64, C.c_int, p, p]
             L.gem_oracle_gqa_attention_compact.restype = C.c_int
             L.gem_oracle_gqa_attention_compact.argtypes = [p, p, p, C.c_int, C.c_int, C.c_int, C.c_int64,
                                                            C.c_int64, C.c_int, C.c_double, C.c_double, p]
@@ -222,6 +224,18 @@ def q8_0_gemv(W: np.ndarray, N: int, K: int, x: np.ndarray) -> np.ndarray:
 def argmax(v: np.ndarray) -> int:
     v = _c(v, np.float64)
     return int(lib().gem_oracle_argmax(_ptr(v), v.size))
+
+
+def topk(v: np.ndarray, k: int):
+    """(indices, values) of the k largest entries, largest first; ties by lowest index, NaN
+    after every number (by index)."""
+    v = _c(v, np.float64)
+    idx = np.empty(k, np.int64)
+    val = np.empty(k, np.float64)
+    rc = lib().gem_oracle_topk(_ptr(v), v.size, int(k), _ptr(idx), _ptr(val))
+    if rc:
+        raise ValueError("oracle top-k rejected arguments (rc=%d)" % rc)
+    return idx, val
 
 
 def num_threads() -> int:

@@ -546,6 +546,41 @@ int64_t gem_oracle_argmax(const double *v, int64_t n)
     return best < 0 ? 0 : best;
 }
 
+/* The k largest entries, largest first: the order ranks numbers by value (descending, -inf
+ * included), equal values by index (ascending, as the argmax above), and places entries that are
+ * not numbers after every number, by index.  [GEM] sampler note (top-k with ties broken by token
+ * id); the NaN rank is this library's reading.  Plain selection: k scans over the n entries.
+ * idx, val: [k]; 1 <= k <= n. */
+static int oracle_before(const double *v, int64_t a, int64_t b)
+{
+    const int na = isnan(v[a]), nb = isnan(v[b]);
+    if (na != nb)
+        return nb;   /* a number comes before a NaN */
+    if (!na && v[a] != v[b])
+        return v[a] > v[b];
+    return a < b;
+}
+
+int gem_oracle_topk(const double *v, int64_t n, int k, int64_t *idx, double *val)
+{
+    if (k < 1 || k > n)
+        return 1;
+    unsigned char *taken = calloc((size_t)n, 1);
+    if (!taken)
+        return 3;
+    for (int r = 0; r < k; ++r) {
+        int64_t best = -1;
+        for (int64_t i = 0; i < n; ++i)
+            if (!taken[i] && (best < 0 || oracle_before(v, i, best)))
+                best = i;
+        taken[best] = 1;
+        idx[r] = best;
+        val[r] = v[best];
+    }
+    free(taken);
+    return 0;
+}
+
 int gem_oracle_num_threads(void)
 {
 #ifdef _OPENMP

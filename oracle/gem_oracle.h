@@ -116,6 +116,10 @@ int gem_oracle_gqa_attention_compact(const double *q, const uint16_t *v_cache, c
 /* Index of the largest value; ties go to the lowest index. */
 int64_t gem_oracle_argmax(const double *v, int64_t n);
 
+/* The k largest entries, largest first (ties: lowest index; NaN after every number, by
+ * index); returns 0, or 1 for k outside 1..n.  idx, val: [k]. */
+int gem_oracle_topk(const double *v, int64_t n, int k, int64_t *idx, double *val);
+
 /* Q8_0: 34-byte blocks (binary16 scale, 32 int8 codes), weight = q * d. */
 void gem_oracle_q8_0_dequant(const uint8_t *W, int64_t N, int64_t K, double *out);
 int gem_oracle_q8_0_gemv_f64(const uint8_t *W, int64_t N, int64_t K, const double *x,

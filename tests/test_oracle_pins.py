@@ -586,3 +586,34 @@ def test_compact_layer_appends_v_only_and_tracks_the_standard_layer():
     assert np.array_equal(vc, vs)                   # same appended V row, nothing else touched
     assert np.allclose(got, ref, rtol=1e-3, atol=1e-3)
     assert not np.array_equal(got, ref)             # the K rows really are rebuilt, not read
+
+
+# ---- top-k (the sampler's selection; ties by lowest index, NaN after every number) -----------
+
+def test_topk_hand_cases():
+    nan, inf = float("nan"), float("inf")
+    i, v = oracle.topk(np.array([1.0, 3.0, 3.0, 2.0, 3.0]), 3)
+    assert list(i) == [1, 2, 4] and list(v) == [3.0, 3.0, 3.0]
+    i, _ = oracle.topk(np.array([nan, 1.0, nan, 0.0]), 4)
+    assert list(i) == [1, 3, 0, 2]
+    i, _ = oracle.topk(np.array([-inf, -inf, 5.0]), 3)
+    assert list(i) == [2, 0, 1]
+    i, v = oracle.topk(np.array([7.0]), 1)
+    assert list(i) == [0] and v[0] == 7.0
+    with pytest.raises(ValueError):
+        oracle.topk(np.array([1.0, 2.0]), 3)
+
+
+def test_topk_equals_a_stable_sort_and_the_argmax():
+    """Against numpy's lexicographic sort (value descending, then index), NaN rows last."""
+    rng = np.random.default_rng(5)
+    for n, k in [(1, 1), (10, 10), (1000, 64), (4097, 17)]:
+        v = np.round(rng.normal(size=n), 1)   # rounding makes ties common
+        v[rng.integers(0, n, size=max(1, n // 50))] = np.nan
+        num = np.nonzero(~np.isnan(v))[0]
+        order = num[np.lexsort((num, -v[num]))]
+        order = np.concatenate([order, np.nonzero(np.isnan(v))[0]])
+        i, vals = oracle.topk(v, k)
+        assert list(i) == list(order[:k])
+        assert np.array_equal(vals, v[order[:k]], equal_nan=True)
+        assert i[0] == oracle.argmax(v) or np.all(np.isnan(v))

@@ -674,10 +674,15 @@ def run_gem(args):
         us = time_graph(torch, gl, max(5, min(args.steps, 50))) * 1e3
         ga = capture(torch, lambda yl=yl, il=il, aws=aws: gem.argmax(yl, il, aws))
         us_a = time_graph(torch, ga, max(5, min(args.steps, 200))) * 1e3
+        ti = torch.empty((B, 64), dtype=torch.int32, device="cuda")
+        tv = torch.empty((B, 64), device="cuda")
+        tws = torch.empty(max(1, gem.topk_workspace(B, V, 64)), dtype=torch.uint8, device="cuda")
+        gt = capture(torch, lambda yl=yl, ti=ti, tv=tv, tws=tws: gem.topk(yl, 64, ti, tv, tws))
+        us_t = time_graph(torch, gt, max(5, min(args.steps, 200))) * 1e3
         b = V * (Hl // 32) * 34 + 4 * B * (Hl + V)
         logits["b%d" % B] = {"us": round(us, 2), "gbs": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
-                             "argmax_us": round(us_a, 2)}
-        del gl, ga
+                             "argmax_us": round(us_a, 2), "top64_us": round(us_t, 2)}
+        del gl, ga, gt
     del Wq8
     torch.cuda.empty_cache()
 

@@ -214,6 +214,22 @@ GEM_API gem_status gem_argmax(const float *y, int64_t ldy, int B, int64_t N, int
                               void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Device top-k of logit rows: the sampler's candidate list.  [GEM] "Native Metal diagnostic:
+ * buffer ownership" (the top-k sampler: a seeded test matches the full-sort token sequence,
+ * equal logits broken by token id).
+ *   idx[b][r], val[b][r] (r < k): the k largest entries of row b, largest first; equal values
+ *   by lowest index; entries that are not numbers after every number, by index (so r = 0 is
+ *   gem_argmax's index whenever the row holds a number).  val copies y bit for bit.
+ *   y [B][ldy] fp32; 1 <= k <= 64, k <= N; N up to 2048 / k * 8192 (262,144 at k = 64), else
+ *   GEM_ERR_UNSUPPORTED_SHAPE.  Workspace: gem_topk_workspace(B, N, k) bytes, 256-byte
+ *   aligned, no initialisation (the call zeroes its arrival counters with a 4 * B-byte
+ *   memset on the stream).  Deterministic.
+ */
+GEM_API size_t gem_topk_workspace(int B, int64_t N, int k);
+GEM_API gem_status gem_topk(const float *y, int64_t ldy, int B, int64_t N, int k, int32_t *idx,
+                            float *val, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Weighted RMSNorm  [GEM] "weighted RMSNorm over one or many heads"; [GELO] 06 pre-norm.
  *   out[b][i] = x[b][i] / sqrt(mean_i x[b][i]^2 + eps) * gamma[i]   (gamma NULL: 1)
  * x, out: [B][H] fp32 (may alias).

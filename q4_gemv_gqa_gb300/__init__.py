@@ -237,6 +237,26 @@ def argmax(y: torch.Tensor, idx: torch.Tensor, workspace: torch.Tensor | None = 
     return idx
 
 
+def topk_workspace(B: int, N: int, k: int) -> int:
+    return int(lib.gem_topk_workspace(B, N, k))
+
+
+def topk(y: torch.Tensor, k: int, idx: torch.Tensor, val: torch.Tensor,
+         workspace: torch.Tensor | None = None, stream=None):
+    """The k largest entries of each row of y [B, N] fp32, largest first (ties: lowest index;
+    NaN after every number): idx int32 [B, k], val fp32 [B, k]."""
+    B = y.shape[0] if y.dim() == 2 else 1
+    N = y.shape[-1]
+    need = topk_workspace(B, N, k)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=y.device)
+    st = lib.gem_topk(_dev(y, torch.float32, "y"), N, B, N, k, _dev(idx, torch.int32, "idx"),
+                      _dev(val, torch.float32, "val"), _dev(workspace, torch.uint8, "workspace"),
+                      workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(st, "gem_topk")
+    return idx, val
+
+
 def rmsnorm(x: torch.Tensor, gamma: torch.Tensor | None, eps: float, out: torch.Tensor,
             stream=None) -> torch.Tensor:
     B = x.shape[0] if x.dim() == 2 else 1

@@ -42,6 +42,8 @@ PROTOTYPES = {
                                   C.c_size_t, p]),
     "gem_q4_0_gemm_workspace": (C.c_size_t, [i32, i64]),
     "gem_q4_0_gemm": (i32, [p, p, i64, i64, p, i64, i32, p, C.c_float, i32, p, i64, p, p, C.c_size_t, p]),
+    "gem_topk_workspace": (C.c_size_t, [i32, i64, i32]),
+    "gem_topk": (i32, [p, i64, i32, i64, i32, p, p, p, C.c_size_t, p]),
     "gem_q8_0_gemv": (i32, [p, i64, i64, p, i64, i32, p, i64, p]),
     "gem_argmax_workspace": (C.c_size_t, [i32, i64]),
     "gem_argmax": (i32, [p, i64, i32, i64, p, p, C.c_size_t, p]),

@@ -306,6 +306,121 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* y, int
 }
 
 // chunks of 2048 values (8 per thread): about one CTA per SM at the 262,144-entry vocabulary
+// ---- top-k ---------------------------------------------------------------------------------
+// The k (<= 64) largest entries of each row, largest first, ties by lowest index, NaN after every
+// number (by index).  Each entry becomes one 64-bit key whose order is that order: the high word
+// maps the float to an unsigned integer in value order (NaN to 0, below -inf), the low word is the
+// inverted index.  A warp selects k keys by k rounds of a warp maximum over the keys its lanes
+// hold (the winner's lane clears its key); warp 0 merges the warps' lists the same way; a CTA
+// publishes its chunk's list and the CTA taking the last ticket merges the chunks' lists.
+constexpr int kTopkMax = 64;
+constexpr int kTopkThreads = 256;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkMerge = 2048;   // the chunks' lists together: at most this many keys
+
+__device__ __forceinline__ uint64_t topk_key(float v, int64_t i) {
+    uint32_t u = __float_as_uint(v);
+    u = isnan(v) ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+    return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+}
+__device__ __forceinline__ int topk_index(uint64_t key) { return static_cast<int>(~static_cast<uint32_t>(key)); }
+
+// k rounds: the warp's largest remaining key, written (lane 0) to out[r]; its holder clears it.
+// A key of 0 is "nothing" (every real key has a nonzero low word).
+template <int NPL>
+__device__ __forceinline__ void topk_warp_select(uint64_t (&key)[NPL], int k, uint64_t* out, int lane) {
+    for (int r = 0; r < k; ++r) {
+        uint64_t best = 0;
+#pragma unroll
+        for (int u = 0; u < NPL; ++u) best = key[u] > best ? key[u] : best;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+        }
+#pragma unroll
+        for (int u = 0; u < NPL; ++u)
+            if (key[u] == best) key[u] = 0;
+        if (lane == 0) out[r] = best;
+    }
+}
+
+// the CTA's k largest of the keys its threads hold, into res[0, k) (shared); cand: [warps][64]
+template <int NPL>
+__device__ __forceinline__ void topk_cta(uint64_t (&key)[NPL], int k, uint64_t* cand, uint64_t* res, int tid) {
+    const int lane = tid & 31, warp = tid >> 5;
+    topk_warp_select<NPL>(key, k, cand + warp * kTopkMax, lane);
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int M = kTopkWarps * kTopkMax / 32;
+        uint64_t mk[M];
+#pragma unroll
+        for (int u = 0; u < M; ++u) {
+            const int e = lane + 32 * u, w = e / kTopkMax, r = e - w * kTopkMax;
+            mk[u] = r < k ? cand[w * kTopkMax + r] : 0ull;
+        }
+        topk_warp_select<M>(mk, k, res, lane);
+    }
+    __syncthreads();
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* y, int64_t ldy, int64_t N, int k,
+                                                            uint64_t* part, unsigned* cnt, int32_t* idx, float* val) {
+    __shared__ uint64_t cand[kTopkWarps * kTopkMax];
+    __shared__ uint64_t res[kTopkMax];
+    __shared__ int last_sh;
+    pdl_wait_trigger();
+    const int c = blockIdx.x, b = blockIdx.y, nchunk = gridDim.x;
+    const int tid = threadIdx.x;
+    const float* row = y + b * ldy;
+    const int64_t lo = (N * c) / nchunk, hi = (N * (c + 1)) / nchunk;
+    uint64_t key[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {   // loads first (independent)
+        const int64_t i = lo + tid + static_cast<int64_t>(u) * kTopkThreads;
+        key[u] = i < hi ? topk_key(__ldg(row + i), i) : 0ull;
+    }
+    topk_cta<VPT>(key, k, cand, res, tid);
+    uint64_t* mine = part + (static_cast<int64_t>(b) * nchunk + c) * k;
+    if (tid < k) mine[tid] = res[tid];
+    // the barrier orders every thread's list writes before thread 0's ticket, whose release
+    // (cumulative) publishes them; its acquire orders the merging CTA's reads after the tickets
+    __syncthreads();
+    if (tid == 0) {
+        unsigned ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(cnt + b) : "memory");
+        last_sh = ticket == static_cast<unsigned>(nchunk - 1);
+    }
+    __syncthreads();
+    if (!last_sh) return;
+    constexpr int MPT = kTopkMerge / kTopkThreads;
+    uint64_t mk[MPT];
+    const int64_t m = static_cast<int64_t>(nchunk) * k;
+#pragma unroll
+    for (int u = 0; u < MPT; ++u) {
+        const int64_t e = tid + static_cast<int64_t>(u) * kTopkThreads;
+        mk[u] = e < m ? __ldcg(reinterpret_cast<const unsigned long long*>(part) + static_cast<int64_t>(b) * m + e) : 0ull;
+    }
+    topk_cta<MPT>(mk, k, cand, res, tid);
+    if (tid < k) {
+        const int i = topk_index(res[tid]);
+        idx[b * k + tid] = i;
+        val[b * k + tid] = row[i];
+    }
+    if (tid == 0) cnt[b] = 0u;   // ready for the next call
+}
+
+// values per thread for a row of N and a list of k: the fewest (8, 16, 32) whose chunk lists fit
+// the merge (nchunk * k <= 2048); 0 when none does
+int topk_vpt(int64_t N, int k) {
+    for (int v : {8, 16, 32}) {
+        const int64_t nc = (N + 256ll * v - 1) / (256ll * v);
+        if (nc * k <= kTopkMerge) return v;
+    }
+    return 0;
+}
+
 int argmax_chunks(int64_t N) { return static_cast<int>(std::min<int64_t>(1024, std::max<int64_t>(1, (N + 2047) / 2048))); }
 
 gem_status ensure_smem_q8(const void* fn, int device, size_t bytes) {
@@ -375,6 +490,40 @@ size_t gem_argmax_workspace(int B, int64_t N) {
     const int nc = gem::argmax_chunks(N);
     return gem::align_up(static_cast<size_t>(B) * nc * sizeof(float2), 256) +
            gem::align_up(static_cast<size_t>(B) * sizeof(unsigned), 256);
+}
+
+size_t gem_topk_workspace(int B, int64_t N, int k) {
+    if (B <= 0 || N <= 0 || k < 1 || k > gem::kTopkMax || k > N) return 0;
+    const int v = gem::topk_vpt(N, k);
+    if (!v) return 0;
+    const int64_t nc = (N + 256ll * v - 1) / (256ll * v);
+    return gem::align_up(static_cast<size_t>(B) * nc * k * sizeof(uint64_t), 256) +
+           gem::align_up(static_cast<size_t>(B) * sizeof(unsigned), 256);
+}
+
+gem_status gem_topk(const float* y, int64_t ldy, int B, int64_t N, int k, int32_t* idx, float* val, void* workspace,
+                    size_t ws_bytes, void* stream_v) {
+    using namespace gem;
+    if (B < 0 || N < 0 || k < 1 || k > N) return GEM_ERR_INVALID_ARG;
+    if (k > kTopkMax || N >= (int64_t(1) << 31)) return GEM_ERR_UNSUPPORTED_SHAPE;
+    if (B == 0) return GEM_OK;
+    if (!y || !idx || !val || ldy < N) return GEM_ERR_INVALID_ARG;
+    const int v = topk_vpt(N, k);
+    if (!v) return GEM_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = gem_topk_workspace(B, N, k);
+    if (!workspace || ws_bytes < need) return GEM_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return GEM_ERR_MISALIGNED;
+    const int nc = static_cast<int>((N + 256ll * v - 1) / (256ll * v));
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    uint64_t* part = static_cast<uint64_t*>(workspace);
+    unsigned* cnt = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) +
+                                                align_up(static_cast<size_t>(B) * nc * k * sizeof(uint64_t), 256));
+    GEM_CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(unsigned) * B, stream));
+    void* args[] = {const_cast<float**>(&y), &ldy, &N, &k, &part, &cnt, &idx, &val};
+    const void* fn = v == 8 ? reinterpret_cast<const void*>(topk_kernel<8>)
+                     : v == 16 ? reinterpret_cast<const void*>(topk_kernel<16>)
+                               : reinterpret_cast<const void*>(topk_kernel<32>);
+    return launch_pdl(fn, dim3(nc, B), dim3(kTopkThreads), 0, stream, args);
 }
 
 gem_status gem_argmax(const float* y, int64_t ldy, int B, int64_t N, int32_t* idx, void* workspace, size_t ws_bytes,

@@ -121,3 +121,78 @@ def test_tied_q8_0_logits_and_argmax_full_size(env, V, H, B):
         decided += 1
     assert decided >= 1
     assert g.device_status() == 0
+
+
+# ---- device top-k (the sampler's list) ---------------------------------------------------------
+
+def _check_topk(g, t, y_np, k, what):
+    y = _cu(t, np.ascontiguousarray(y_np, dtype=np.float32))
+    B = y.shape[0]
+    idx = t.full((B, k), -7, dtype=t.int32, device="cuda")
+    val = t.full((B, k), -7.0, device="cuda")
+    g.topk(y, k, idx, val)
+    t.cuda.synchronize()
+    gi, gv = idx.cpu().numpy(), val.cpu().numpy()
+    for b in range(B):
+        oi, ov = oracle.topk(y_np[b].astype(np.float32).astype(np.float64), k)
+        assert list(gi[b]) == list(oi), "%s row %d: %s vs %s" % (what, b, gi[b][:8], oi[:8])
+        assert np.array_equal(gv[b].astype(np.float64), ov, equal_nan=True), "%s row %d values" % (what, b)
+
+
+@pytest.mark.parametrize("k", [1, 5, 40, 64])
+def test_topk_semantics(env, k):
+    g, t = env
+    N = 70000   # several chunks and a ragged last one
+    r = gem_synth.normal_f32(24, 1, (N,))
+    rows = [r]
+    tie = np.round(r, 1).astype(np.float32)   # many equal values: ties go to the lowest index
+    rows.append(tie)
+    nan = r.copy()
+    nan[::7] = np.nan
+    rows.append(nan)
+    mostly_nan = np.full(N, np.nan, np.float32)
+    mostly_nan[[5, 60000]] = [-np.inf, 1.0]   # fewer numbers than k: NaN rows fill by index
+    rows.append(mostly_nan)
+    _check_topk(g, t, np.stack(rows), k, "top-%d semantics" % k)
+
+
+@pytest.mark.parametrize("N,k", [(1, 1), (7, 7), (300, 64), (2048, 3), (151936, 40), (262144, 64)])
+def test_topk_shapes(env, N, k):
+    g, t = env
+    _check_topk(g, t, gem_synth.normal_f32(25, N, (3, N)), k, "top-%d of %d" % (k, N))
+
+
+def test_topk_of_q8_0_logits_starts_with_the_argmax(env):
+    g, t = env
+    V, H = 65536, 5376
+    W = gem_synth.q8_0_matrix(26, V + H, V, H)
+    x = gem_synth.normal_f32(26, 7, (2, H))
+    y = t.empty((2, V), device="cuda")
+    g.q8_0_gemv(_cu(t, W), V, H, _cu(t, x), y)
+    idx = t.empty((2, 50), dtype=t.int32, device="cuda")
+    val = t.empty((2, 50), device="cuda")
+    g.topk(y, 50, idx, val)
+    am = t.empty((2,), dtype=t.int32, device="cuda")
+    g.argmax(y, am)
+    t.cuda.synchronize()
+    assert t.equal(idx[:, 0], am)
+    yc = y.cpu().numpy()
+    for b in range(2):
+        oi, _ = oracle.topk(yc[b].astype(np.float64), 50)
+        assert list(idx[b].cpu().numpy()) == list(oi)
+
+
+def test_topk_rejections(env):
+    g, t = env
+    y = t.zeros((1, 100), device="cuda")
+    idx = t.empty((1, 65), dtype=t.int32, device="cuda")
+    val = t.empty((1, 65), device="cuda")
+    with pytest.raises(g.GemError) as ei:   # k > 64
+        g.topk(y, 65, idx, val)
+    assert ei.value.status == 3
+    with pytest.raises(g.GemError) as ei:   # k > N
+        g.topk(t.zeros((1, 10), device="cuda"), 11, idx, val)
+    assert ei.value.status == 1
+    with pytest.raises(g.GemError) as ei:   # a row too long for k = 64
+        g.topk(t.zeros((1, 262145), device="cuda"), 64, idx, val)
+    assert ei.value.status == 3

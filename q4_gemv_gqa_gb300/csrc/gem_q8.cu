@@ -325,22 +325,42 @@ __device__ __forceinline__ uint64_t topk_key(float v, int64_t i) {
 }
 __device__ __forceinline__ int topk_index(uint64_t key) { return static_cast<int>(~static_cast<uint32_t>(key)); }
 
-// k rounds: the warp's largest remaining key, written (lane 0) to out[r]; its holder clears it.
-// A key of 0 is "nothing" (every real key has a nonzero low word).
+// Each lane sorts its keys in descending order once (a bitonic network over register indices
+// known at compile time); then k rounds: the warp maximum of the lanes' first keys is written
+// (lane 0) to out[r] and its holder shifts its list by one.  A key of 0 is "nothing" (every real
+// key has a nonzero low word).
+template <int NPL>
+__device__ __forceinline__ void topk_sort_desc(uint64_t (&a)[NPL]) {
+#pragma unroll
+    for (int k = 2; k <= NPL; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint64_t x = a[i], y = a[l];
+                    const bool swap = (i & k) == 0 ? x < y : x > y;   // descending runs first
+                    a[i] = swap ? y : x;
+                    a[l] = swap ? x : y;
+                }
+            }
+}
+
 template <int NPL>
 __device__ __forceinline__ void topk_warp_select(uint64_t (&key)[NPL], int k, uint64_t* out, int lane) {
+    topk_sort_desc<NPL>(key);
     for (int r = 0; r < k; ++r) {
-        uint64_t best = 0;
-#pragma unroll
-        for (int u = 0; u < NPL; ++u) best = key[u] > best ? key[u] : best;
+        uint64_t best = key[0];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
             best = other > best ? other : best;
         }
+        const bool won = key[0] == best;
 #pragma unroll
-        for (int u = 0; u < NPL; ++u)
-            if (key[u] == best) key[u] = 0;
+        for (int u = 0; u + 1 < NPL; ++u) key[u] = won ? key[u + 1] : key[u];
+        if (won) key[NPL - 1] = 0;
         if (lane == 0) out[r] = best;
     }
 }

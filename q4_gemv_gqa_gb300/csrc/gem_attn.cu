@@ -1364,7 +1364,6 @@ struct CompactPlan {
 // anchors would not fit shared memory.  ok = false when no layout fits.
 bool compact_plan(int B, int n_q, int n_kv, int d, int64_t cap, int R, int num_sms, size_t smem_optin,
                   CompactPlan& pl) {
-    (void)n_q;
     pl = CompactPlan{};
     pl.tp = tile_slots(d);
     pl.tile_bytes = static_cast<uint32_t>(pl.tp * d * 2);

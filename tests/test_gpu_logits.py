@@ -115,7 +115,7 @@ def test_tied_q8_0_logits_and_argmax_full_size(env, V, H, B):
     for b in range(B):
         top2 = np.sort(ref[b])[-2:]
         if top2[1] - top2[0] < 2 * MAX_ABS:
-            continue   # ambiguous by construction: counted, not judged
+            continue   # ambiguous by construction: counted, not asserted
         assert int(got[b]) == oracle.argmax(ref[b]), "row %d: device argmax %d, oracle %d" % (
             b, int(got[b]), oracle.argmax(ref[b]))
         decided += 1

@@ -541,7 +541,7 @@ def test_decode_layer_stack_each_layer_from_oracle_input(gem, torch_mod, name, n
 # A Q4_0 GEMV from the final hidden state to a Qwen3-size vocabulary, then the token choice:
 # the GPU logits must match the oracle's within the parity tolerance and pick the same argmax
 # (lowest index on ties).  Rows whose oracle top-2 gap is within twice the max-abs tolerance are
-# ambiguous by construction and are counted, not judged.
+# ambiguous by construction and are counted, not asserted.
 
 @pytest.mark.parametrize("B", [1, 8])
 def test_logit_projection_argmax(gem, torch_mod, B):

@@ -354,13 +354,14 @@ GEM_API gem_status gem_gqa_decode_attn_compact(const float *q, int64_t ldq, cons
  * plan, so the output is bit-identical to that call's), except:
  *   - the split partials need gem_gqa_decode_attn_workspace() bytes for the same shape,
  *     B * n_q * ns * (d + 2) * 4 bytes where ns is the split count of the plan.  ns grows
- *     with the number of SMs (about 2 * SMs / (B * n_kv) splits) and, for d = 512 or
- *     n_q / n_kv = 8, with the attended range: each split covers at most 1024 positions, so
- *     ns >= ceil(min(window or cache_cap, cache_cap) / 1024).  When the need exceeds
- *     GEM_ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) the call launches nothing and returns
- *     GEM_ERR_WORKSPACE.  Example on a 152-SM GPU: the 4-KV-head, d = 512, n_q = 32 layer with
- *     cache_cap = 32769 fits at B = 1 (76 splits, 5.0 MB) but not at B = 8 (33 splits, 17.4 MB); query
- *     gem_gqa_decode_attn_workspace() to know before calling.
+ *     with the number of SMs (about SMs / (B * n_kv) splits for d = 512 or n_q / n_kv = 8,
+ *     more for the other shapes) and, for d = 512 or n_q / n_kv = 8, with the attended range:
+ *     each split covers at most 1024 positions, so ns >= ceil(min(window or cache_cap,
+ *     cache_cap) / 1024).  When the need exceeds GEM_ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) the
+ *     call launches nothing and returns GEM_ERR_WORKSPACE.  Example on a 152-SM GPU: the
+ *     4-KV-head, d = 512, n_q = 32 layer with cache_cap = 32769 fits at B = 1 (38 splits,
+ *     2.5 MB) but not at B = 8 (33 splits, 17.4 MB); query gem_gqa_decode_attn_workspace() to
+ *     know before calling.
  *   - the array exists once per device and every call on that device shares it.  Calls issued
  *     in order on one stream are safe; two calls that can run at the same time on one device
  *     (different streams, or different host threads with different streams) race on the

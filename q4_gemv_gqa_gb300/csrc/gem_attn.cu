@@ -1209,7 +1209,7 @@ Plan make_plan(int B, int n_q, int n_kv, int d, int64_t cap, int window, int num
         }
         return pl;
     }
-    const int64_t target = 2LL * num_sms;
+    const int64_t target = static_cast<int64_t>(num_sms);   // one wave: a CTA per SM
     int64_t ns = std::max<int64_t>(1, (target + pairs - 1) / pairs);
     ns = std::min(ns, nt_max);
     const int max_tiles = kMaxSplitSlots / pl.tp;

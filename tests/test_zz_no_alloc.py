@@ -75,8 +75,9 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row(env, case):
 
 def test_noalloc_rejects_shape_beyond_scratch(env):
     g, t = env
-    # B * n_kv = 256 KV heads with G = 8, d = 512: two splits each need ~8.4 MB of partials.
-    n_q, n_kv, d, cap, B = 1024, 128, 512, 64, 2
+    # the Gemma 4 31B full-attention layer at B = 8: each split covers at most 1024 positions, so
+    # 32,769 positions take 33 splits, 8 x 32 x 33 x 514 floats = 17.4 MB of partials
+    n_q, n_kv, d, cap, B = 32, 4, 512, 32769, 8
     need = g.gqa_decode_attn_workspace(B, n_q, n_kv, d, cap, 0)
     if need <= g.NOALLOC_SCRATCH_BYTES:
         pytest.skip("this device's split plan fits the shape into the scratch array")

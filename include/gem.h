@@ -121,7 +121,9 @@ GEM_API gem_status gem_set_test_injection(int mask);
  *   W        N x (K/32) x 18 bytes, rows contiguous (row stride K/32*18 bytes).
  *   x        [B][ldx] fp32, ldx >= K.       y  [B][ldy] fp32, ldy >= N.
  *   residual nullable, [B][ldy] fp32; may alias y (read before write, element-wise).
- *   Accumulation is fp32.  y must not overlap W or x.
+ *   Accumulation is fp32 (on tensor cores where K % 256 == 0 and the inputs are aligned: exact
+ *   weights times each activation as a binary16 hi + lo pair of about 22 significant bits,
+ *   under power-of-two scales that are undone exactly).  y must not overlap W or x.
  *   For B >= 2 the call converts x into tensor-core operand records first (a second launch on the
  *   same stream), kept in a library-owned array of 4 MiB per device (K <= 130816): calls on two
  *   streams of one device that may run at the same time must not both have B >= 2.  Use
@@ -195,7 +197,10 @@ GEM_API gem_status gem_q4_0_gemm(const void *W0, const void *W1, int64_t N, int6
  *       codes q (element j of the block in byte 2 + j); 16-byte aligned (GEM_ERR_MISALIGNED).
  *   K   a multiple of 256 (GEM_ERR_UNSUPPORTED_SHAPE otherwise); B in 0..8.
  *   x   [B][ldx] fp32, ldx >= K, 16-byte aligned with ldx % 4 == 0 (GEM_ERR_MISALIGNED);
- *   y   [B][ldy] fp32, ldy >= N.  Accumulation is fp32.
+ *   y   [B][ldy] fp32, ldy >= N.  Accumulation is fp32: the products are formed on tensor
+ *       cores from the exact codes and each activation as a binary16 hi + lo pair (about 22
+ *       significant bits; each activation row is first scaled by a power of two, so any
+ *       finite fp32 magnitude is kept).
  */
 GEM_API gem_status gem_q8_0_gemv(const void *W, int64_t N, int64_t K, const float *x, int64_t ldx,
                                  int B, float *y, int64_t ldy, void *stream);

@@ -8,15 +8,6 @@
 //
 // Q8_0 record (GGML): 34 bytes = binary16 scale d (little endian), then 32 int8 codes q;
 // weight j = q[j] * d.
-//
-// GEMV schedule.  Rows come in tiles of 4 per consumer warp; the CTAs take tiles round robin.  A producer warp
-// bulk-copies (cp.async.bulk, one 1-D copy per row) a tile's rows one K-chunk of 16 blocks at
-// a time into a ring of shared-memory stages; the consumer warps (16 for up to two activation
-// rows, else 8) each take four rows of a stage.  A warp covers four blocks per step: lane (b, m) takes codes 4m .. 4m + 3 of block b
-// for each of its four rows (two 16-bit loads: a block's codes are only 2-byte aligned), with
-// the four activations in one float4 shared by the rows, sums the four products and scales
-// the sum by the block's d (per activation row: independent accumulators per row).  Each row's
-// 32 lane sums are added by a warp reduction (fixed order) after the last chunk.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -27,15 +18,6 @@ namespace gem {
 namespace {
 
 constexpr int kQ8Block = 34;
-// A stage: each consumer warp's rows x one K-chunk.  Up to two activation rows: 2 rows per warp
-// and chunks of 32 blocks (1088 contiguous bytes per row: short per-row runs cost HBM
-// throughput); more rows: 4 rows per warp and 16-block chunks, so each activation load from L1
-// serves more weights.  Either way a stage is 34,816 (16 warps) or 17,408 bytes (8 warps).
-__host__ __device__ constexpr int q8_rows_per_warp(int bmax) { return bmax <= 2 ? 2 : 4; }
-__host__ __device__ constexpr int q8_chunk_blocks(int bmax) { return bmax <= 2 ? 32 : 16; }
-constexpr int kQ8RingBytes = 139264;   // 4 stages of 16 warps' rows, 8 of 8 warps' rows
-// consumer warps (four rows of a tile each): 16 for up to two activation rows, else 8
-__host__ __device__ constexpr int q8_warps(int bmax) { return bmax <= 2 ? 16 : 8; }
 
 struct Q8Params {
     const uint8_t* W;
@@ -48,74 +30,112 @@ struct Q8Params {
     float* y;
     int64_t ldy;
     int nchunk;           // K-chunks per row
-    int ns;               // ring stages
     int* status;
 };
-
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ uint32_t gemv_mma_lds16(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
-}
 
 __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// BMAX: the largest activation row count this instance handles (B <= BMAX at run time).
-template <int BMAX>
-__global__ void __launch_bounds__((q8_warps(BMAX) + 1) * 32, 1) q8_0_gemv_kernel(const Q8Params p) {
+// ---- the GEMV on tensor cores, 1..8 activation rows ------------------------------------------
+// A stage is 128 weight rows (eight m16 tiles) x 8 blocks (272 bytes of each row), one 2-D TMA
+// box: one copy per stage, where one bulk copy per row bounded the stream by the producer's
+// issue rate.  In shared memory the box rows are 272 bytes apart, so the lanes g = 0..7 of a
+// load land on distinct banks.  Consumer warp w takes block w of the stage for all eight m16
+// tiles: the activation operand it builds serves 8 x 4 mma, and the activation rows are read
+// once per 128 weight rows.  k16 tile j of a block gives lane quad t the four consecutive codes
+// 16 j + 4 t .. + 3 (codes 0-1 sit at k = 2t, 2t+1 of the A fragment, codes 2-3 at k = 2t+8,
+// 2t+9), and B column n holds activation row n at the same four positions.  Codes become exact
+// binary16 values: the byte biased by 128 is placed under the exponent of 1024 by a byte
+// permute, then 1152 is subtracted.  Each activation row is scaled by one power of two (its
+// largest magnitude to [2^13, 2^14)) and split into binary16 hi + lo, one mma each.  The two mma
+// of a k16 tile start from zero and their sum is scaled by the row's d into the tile
+// accumulator (short chains); after the last stage of a row tile the warps' sums are added in a
+// fixed order through shared memory and the row's power of two is undone.
+constexpr int kQ8mWarps = 8;
+constexpr int kQ8mTiles = 8;                                    // m16 tiles per stage
+constexpr int kQ8mRows = 16 * kQ8mTiles;
+constexpr int kQ8mChunk = 8;                                    // blocks per stage row
+constexpr int kQ8mBpw = kQ8mChunk / kQ8mWarps;                  // blocks of a chunk per warp
+constexpr int kQ8mBoxBlocks = 8;                                // blocks per TMA box row (272 bytes)
+constexpr int kQ8mBoxPitch = kQ8mBoxBlocks * kQ8Block;          // 272
+constexpr uint32_t kQ8mBoxBytes = kQ8mRows * kQ8mBoxPitch;      // 8,704
+constexpr uint32_t kQ8mStage = (kQ8mChunk / kQ8mBoxBlocks) * kQ8mBoxBytes;   // 34,816
+constexpr int kQ8mStages = 4;
+constexpr uint32_t kQ8mRedFloats = kQ8mWarps * kQ8mTiles * 4 * 32;   // one buffer: [warp][tile * 4 + e][lane]
+constexpr size_t kQ8mSmem = kQ8mStages * kQ8mStage + 2 * kQ8mStages * 8 + 2 * kQ8mRedFloats * 4 + 16 * 4;
+
+__device__ __forceinline__ void mma_16816_zero(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Four int8 codes (the bytes of w, lowest first) as two exact binary16 pairs (c0, c1), (c2, c3).
+__device__ __forceinline__ void q8_codes_half2(uint32_t w, uint32_t& h01, uint32_t& h23) {
+    const uint32_t u = w ^ 0x80808080u;   // code + 128 as an unsigned byte
+    uint32_t p01, p23;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(p01) : "r"(u), "r"(0x64646464u));   // (1024 + u0, 1024 + u1)
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(p23) : "r"(u), "r"(0x64646464u));   // (1024 + u2, 1024 + u3)
+    const uint32_t bias = 0x64806480u;                                              // (1152, 1152)
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h01) : "r"(p01), "r"(bias));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(p23), "r"(bias));
+}
+
+// Four activations as binary16 hi + lo pairs: hi = (v0, v1), (v2, v3) rounded; lo the remainders.
+__device__ __forceinline__ void q8_split4(float4 v, uint32_t (&hi)[2], uint32_t (&lo)[2]) {
+    const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+    const __half2 l01 = __floats2half2_rn(v.x - f01.x, v.y - f01.y), l23 = __floats2half2_rn(v.z - f23.x, v.w - f23.y);
+    hi[0] = *reinterpret_cast<const uint32_t*>(&h01);
+    hi[1] = *reinterpret_cast<const uint32_t*>(&h23);
+    lo[0] = *reinterpret_cast<const uint32_t*>(&l01);
+    lo[1] = *reinterpret_cast<const uint32_t*>(&l23);
+}
+
+__global__ void __launch_bounds__((kQ8mWarps + 1) * 32, 1) q8_0_gemv_mma_kernel(const __grid_constant__ CUtensorMap tm,
+                                                                              const Q8Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int kQ8Warps = q8_warps(BMAX);
-    constexpr int kQ8RowsPerWarp = q8_rows_per_warp(BMAX);
-    constexpr int kQ8ChunkBlocks = q8_chunk_blocks(BMAX);
-    constexpr int kQ8TileRows = kQ8Warps * kQ8RowsPerWarp;
-    constexpr uint32_t kStageBytes = kQ8TileRows * kQ8ChunkBlocks * kQ8Block;
-    constexpr int kQ8MaxStages = kQ8RingBytes / kStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQ8MaxStages * kStageBytes);
-    uint64_t* empty = full + kQ8MaxStages;
-    // up to two activation rows stay resident in shared memory for the whole call; more rows are
-    // read through L1
-    constexpr bool kXRes = BMAX <= 2;
-    float* xs = reinterpret_cast<float*>(smem + kQ8MaxStages * kStageBytes + 2 * kQ8MaxStages * 8);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQ8mStages * kQ8mStage);
+    uint64_t* empty = full + kQ8mStages;
+    float* red = reinterpret_cast<float*>(smem + kQ8mStages * kQ8mStage + 2 * kQ8mStages * 8);
+    float* rsc = red + 2 * kQ8mRedFloats;   // [8] 2^e of each activation row, [8..16) 2^-e
     __shared__ int any_failed;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ns = p.ns;
-    const int64_t ntiles = (p.N + kQ8TileRows - 1) / kQ8TileRows;
+    constexpr int ns = kQ8mStages;
+    const int64_t ntiles = (p.N + kQ8mRows - 1) / kQ8mRows;
+    const int nblk = p.K / 32;
     if (tid == 0) {
         any_failed = 0;
         for (int i = 0; i < ns; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kQ8Warps);
+            mbar_init(&empty[i], kQ8mWarps);
         }
         fence_mbar_init();
+        prefetch_tensormap(&tm);
     }
     __syncthreads();
 
-    if (warp == kQ8Warps) {   // producer: (tile, chunk) stages in order
+    if (warp == kQ8mWarps) {   // producer: (tile, chunk) stages in order
         if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
             bool ok = true;
             int s = 0, slot = 0;
             uint32_t par = 1;
-            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int64_t r0 = t * kQ8TileRows;
-                const int nr = static_cast<int>(p.N - r0 < kQ8TileRows ? p.N - r0 : kQ8TileRows);
+            for (int64_t tl = blockIdx.x; tl < ntiles && ok; tl += gridDim.x) {
+                const int64_t r0 = tl * kQ8mRows;
                 for (int c = 0; c < p.nchunk; ++c) {
                     if (s >= ns && !(ok = mbar_wait(&empty[slot], par, p.status))) break;
-                    const int nb = min(kQ8ChunkBlocks, p.K / 32 - c * kQ8ChunkBlocks);
-                    const uint32_t cb = static_cast<uint32_t>(nb * kQ8Block);   // multiple of 16 (K % 256 == 0)
-                    uint8_t* dst = smem + static_cast<size_t>(slot) * kStageBytes;
-                    mbar_arrive_expect_tx(&full[slot], cb * static_cast<uint32_t>(nr));
-                    for (int r = 0; r < nr; ++r)
-                        bulk_copy(dst + r * (kQ8ChunkBlocks * kQ8Block),
-                                  p.W + (r0 + r) * p.rowbytes + static_cast<int64_t>(c) * kQ8ChunkBlocks * kQ8Block, cb,
-                                  &full[slot]);
+                    // boxes of 8 blocks (K % 256 == 0: whole boxes); rows past N arrive as zeros
+                    // and count toward the bytes like the others
+                    const int nbox = min(kQ8mChunk, nblk - c * kQ8mChunk) / kQ8mBoxBlocks;
+                    uint8_t* dst = smem + static_cast<size_t>(slot) * kQ8mStage;
+                    mbar_arrive_expect_tx(&full[slot], kQ8mBoxBytes * static_cast<uint32_t>(nbox));
+                    for (int q = 0; q < nbox; ++q)   // x in 16-bit units (17 per block): a multiple of 8
+                        tma_load_2d(dst + q * kQ8mBoxBytes, &tm, (c * kQ8mChunk + q * kQ8mBoxBlocks) * (kQ8Block / 2),
+                                    static_cast<int32_t>(r0), &full[slot], policy);
                     ++s;
                     if (++slot == ns) {
                         slot = 0;
@@ -129,61 +149,98 @@ __global__ void __launch_bounds__((q8_warps(BMAX) + 1) * 32, 1) q8_0_gemv_kernel
     }
 
     pdl_wait_trigger();   // the activations come from the previous kernel
-    if constexpr (kXRes) {
-        const int n4 = p.K / 4;
-        for (int bb = 0; bb < p.B; ++bb)
-            for (int i = tid; i < n4; i += kQ8Warps * 32)
-                reinterpret_cast<float4*>(xs + bb * p.K)[i] = __ldg(reinterpret_cast<const float4*>(p.x + bb * p.ldx) + i);
-        asm volatile("bar.sync 1, %0;" ::"r"(kQ8Warps * 32) : "memory");
+    const int B = p.B;
+    // per activation row: the power of two taking its largest magnitude to [2^13, 2^14)
+    if (warp < 8) {
+        float m = 0.f;
+        if (warp < B) {
+            const float4* xr = reinterpret_cast<const float4*>(p.x + warp * p.ldx);
+            const int n4 = p.K / 4;
+            for (int i0 = lane; i0 < n4; i0 += 32 * 6) {
+                float4 v[6];
+#pragma unroll
+                for (int u = 0; u < 6; ++u)
+                    v[u] = i0 + 32 * u < n4 ? __ldg(xr + i0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < 6; ++u)
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
+            }
+            m = warp_max(m);
+        }
+        int e = 0;
+        if (m > 0.f) e = 13 - (((__float_as_int(m) >> 23) & 0xff) - 127);
+        e = max(-126, min(126, e));
+        if (lane == 0) {
+            rsc[warp] = __int_as_float((127 + e) << 23);
+            rsc[8 + warp] = __int_as_float((127 - e) << 23);
+        }
     }
+    asm volatile("bar.sync 1, %0;" ::"r"(kQ8mWarps * 32) : "memory");
+
+    const int g = lane >> 2, t = lane & 3;
+    const bool xrow = g < B;                  // B column g is a real activation row
+    const float sg = rsc[g];
+    const float* xg = p.x + (xrow ? g : 0) * p.ldx + 4 * t;
     bool ok = true;
     int s = 0, slot = 0;
     uint32_t par = 0;
-    const int B = p.B;
-    const int bl = lane >> 3, m = lane & 7;   // block of a step, code quad of the block
-    constexpr uint32_t kRowChunk = kQ8ChunkBlocks * kQ8Block;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const int64_t r0 = t * kQ8TileRows;
-        float acc[kQ8RowsPerWarp][BMAX];
+    int it = 0;
+    for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x, ++it) {
+        const int64_t r0 = tl * kQ8mRows;
+        float acc[kQ8mTiles][4];
 #pragma unroll
-        for (int rr = 0; rr < kQ8RowsPerWarp; ++rr)
-#pragma unroll
-            for (int b = 0; b < BMAX; ++b) acc[rr][b] = 0.f;
+        for (int mt = 0; mt < kQ8mTiles; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
         for (int c = 0; c < p.nchunk; ++c) {
-            const int nb = min(kQ8ChunkBlocks, p.K / 32 - c * kQ8ChunkBlocks);   // a multiple of 8
+            const int nb = min(kQ8mChunk, nblk - c * kQ8mChunk);   // a multiple of 8: the same count per warp
+            // this warp's activations for the chunk, requested before the stage wait
+            float4 xv[kQ8mBpw][2];
+#pragma unroll
+            for (int i = 0; i < kQ8mBpw; ++i) {
+                const int blk = warp + kQ8mWarps * i;
+                const float* xb = xg + (c * kQ8mChunk + blk) * 32;
+                const bool in = xrow && blk < nb;
+                xv[i][0] = in ? __ldg(reinterpret_cast<const float4*>(xb)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[i][1] = in ? __ldg(reinterpret_cast<const float4*>(xb + 16)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             if (ok) ok = mbar_wait(&full[slot], par, p.status);
             if (ok) {
-                const uint32_t st = smem_u32(smem) + static_cast<uint32_t>(slot) * kStageBytes +
-                                    static_cast<uint32_t>(kQ8RowsPerWarp * warp) * kRowChunk;
-                const float4* xc = reinterpret_cast<const float4*>(p.x + static_cast<int64_t>(c) * kQ8ChunkBlocks * 32);
-                const float4* xr = reinterpret_cast<const float4*>(xs + c * kQ8ChunkBlocks * 32);
-                for (int blk = bl; blk < nb; blk += 4) {
-                    float4 xv[BMAX];
+                const uint8_t* st = smem + static_cast<size_t>(slot) * kQ8mStage;
 #pragma unroll
-                    for (int bb = 0; bb < BMAX; ++bb) {
-                        if (bb < B) {
-                            if constexpr (kXRes) xv[bb] = xr[bb * (p.K >> 2) + blk * 8 + m];
-                            else xv[bb] = __ldg(xc + bb * (p.ldx >> 2) + blk * 8 + m);
+                for (int i = 0; i < kQ8mBpw; ++i) {
+                    const int blk = warp + kQ8mWarps * i;
+                    if (blk < nb) {
+                        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            float4 v = xv[i][j];
+                            v.x *= sg; v.y *= sg; v.z *= sg; v.w *= sg;
+                            q8_split4(v, bh[j], bl[j]);
                         }
-                    }
 #pragma unroll
-                    for (int rr = 0; rr < kQ8RowsPerWarp; ++rr) {
-                        const uint32_t a = st + rr * kRowChunk + blk * kQ8Block;
-                        const float d = half_bits_to_float(gemv_mma_lds16(a));
-                        const uint32_t c4 = gemv_mma_lds16(a + 2 + 4 * m) | (gemv_mma_lds16(a + 4 + 4 * m) << 16);
-                        // each code sign-extended by moving its byte to the top and shifting back
-                        const float q0 = static_cast<float>(static_cast<int>(c4 << 24) >> 24);
-                        const float q1 = static_cast<float>(static_cast<int>(c4 << 16) >> 24);
-                        const float q2 = static_cast<float>(static_cast<int>(c4 << 8) >> 24);
-                        const float q3 = static_cast<float>(static_cast<int>(c4) >> 24);
+                        for (int mt = 0; mt < kQ8mTiles; ++mt) {
+                            // rows g and g + 8 of m16 tile mt (plain loads: the stage wait above
+                            // orders them after the copy)
+                            const uint16_t* ra = reinterpret_cast<const uint16_t*>(
+                                st + (blk / kQ8mBoxBlocks) * kQ8mBoxBytes + (mt * 16 + g) * kQ8mBoxPitch +
+                                (blk % kQ8mBoxBlocks) * kQ8Block);
+                            const uint16_t* rb = ra + 8 * kQ8mBoxPitch / 2;
+                            const float dg = half_bits_to_float(ra[0]);
+                            const float dg8 = half_bits_to_float(rb[0]);
 #pragma unroll
-                        for (int bb = 0; bb < BMAX; ++bb) {
-                            if (bb < B) {
-                                float v = q0 * xv[bb].x;
-                                v = fmaf(q1, xv[bb].y, v);
-                                v = fmaf(q2, xv[bb].z, v);
-                                v = fmaf(q3, xv[bb].w, v);
-                                acc[rr][bb] = fmaf(d, v, acc[rr][bb]);
+                            for (int j = 0; j < 2; ++j) {
+                                const int o = 1 + 8 * j + 2 * t;   // in 16-bit units
+                                const uint32_t wg = ra[o] | (static_cast<uint32_t>(ra[o + 1]) << 16);
+                                const uint32_t wg8 = rb[o] | (static_cast<uint32_t>(rb[o + 1]) << 16);
+                                uint32_t a0, a1, a2, a3;
+                                q8_codes_half2(wg, a0, a2);
+                                q8_codes_half2(wg8, a1, a3);
+                                float cj[4];
+                                mma_16816_zero(cj, a0, a1, a2, a3, bh[j][0], bh[j][1]);
+                                mma_16816(cj, a0, a1, a2, a3, bl[j][0], bl[j][1]);
+                                acc[mt][0] = fmaf(dg, cj[0], acc[mt][0]);
+                                acc[mt][1] = fmaf(dg, cj[1], acc[mt][1]);
+                                acc[mt][2] = fmaf(dg8, cj[2], acc[mt][2]);
+                                acc[mt][3] = fmaf(dg8, cj[3], acc[mt][3]);
                             }
                         }
                     }
@@ -197,22 +254,27 @@ __global__ void __launch_bounds__((q8_warps(BMAX) + 1) * 32, 1) q8_0_gemv_kernel
                 par ^= 1u;
             }
         }
+        // the warps' sums, added in warp order (two buffers: one barrier per tile)
+        float* rb = red + (it & 1) * kQ8mRedFloats;
 #pragma unroll
-        for (int rr = 0; rr < kQ8RowsPerWarp; ++rr) {
-            const int64_t n = r0 + kQ8RowsPerWarp * warp + rr;
+        for (int mt = 0; mt < kQ8mTiles; ++mt)
 #pragma unroll
-            for (int bb = 0; bb < BMAX; ++bb) {
-                if (bb < B) {
-                    const float v = warp_sum(acc[rr][bb]);
-                    if (lane == 0 && n < p.N) p.y[bb * p.ldy + n] = v;
-                }
-            }
+            for (int e = 0; e < 4; ++e) rb[(warp * kQ8mTiles * 4 + mt * 4 + e) * 32 + lane] = acc[mt][e];
+        asm volatile("bar.sync 1, %0;" ::"r"(kQ8mWarps * 32) : "memory");
+        for (int o = tid; o < kQ8mTiles * 4 * 32; o += kQ8mWarps * 32) {
+            const int q = o >> 5, ln = o & 31;   // q = tile * 4 + e
+            float v = 0.f;
+            for (int w = 0; w < kQ8mWarps; ++w) v += rb[(w * kQ8mTiles * 4 + q) * 32 + ln];
+            const int e = q & 3;
+            const int64_t row = r0 + (q >> 2) * 16 + (ln >> 2) + (e >> 1) * 8;
+            const int bcol = 2 * (ln & 3) + (e & 1);
+            if (bcol < B && row < p.N) p.y[bcol * p.ldy + row] = v * rsc[8 + bcol];
         }
     }
     // a wait that gave up: the copies of the last stages still get a bounded chance to land
     // before the CTA exits
     if (!ok) atomicOr(&any_failed, 1);
-    asm volatile("bar.sync 1, %0;" ::"r"(kQ8Warps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(kQ8mWarps * 32) : "memory");
     if (any_failed && tid == 0) drain_stages(full, ns, max(0, s - ns), s - 1);
 }
 
@@ -483,26 +545,21 @@ gem_status gem_q8_0_gemv(const void* W, int64_t N, int64_t K, const float* x, in
     p.B = B;
     p.y = y;
     p.ldy = ldy;
-    const int bmax = B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8));
-    p.nchunk = static_cast<int>((K / 32 + q8_chunk_blocks(bmax) - 1) / q8_chunk_blocks(bmax));
     p.status = di.status_word;
-    const int nw = q8_warps(bmax);
-    const size_t stage = static_cast<size_t>(nw) * q8_rows_per_warp(bmax) * q8_chunk_blocks(bmax) * kQ8Block;
-    p.ns = static_cast<int>(kQ8RingBytes / stage);
-    // the ring, its barriers (sized for the most stages any instance has), then x for up to two rows
-    const size_t stage8 = static_cast<size_t>(q8_warps(8)) * q8_rows_per_warp(8) * q8_chunk_blocks(8) * kQ8Block;
-    const size_t smem = kQ8RingBytes + 2 * (kQ8RingBytes / std::min(stage, stage8)) * 8 +
-                        (bmax <= 2 ? static_cast<size_t>(bmax) * K * 4 : 0);
-    if (smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
-    const void* fn = bmax == 1 ? reinterpret_cast<const void*>(q8_0_gemv_kernel<1>)
-                     : bmax == 2 ? reinterpret_cast<const void*>(q8_0_gemv_kernel<2>)
-                     : bmax == 4 ? reinterpret_cast<const void*>(q8_0_gemv_kernel<4>)
-                                 : reinterpret_cast<const void*>(q8_0_gemv_kernel<8>);
-    if ((st = ensure_smem_q8(fn, di.device, smem)) != GEM_OK) return st;
-    const int64_t ntiles = (N + nw * q8_rows_per_warp(bmax) - 1) / (nw * q8_rows_per_warp(bmax));
+    p.nchunk = static_cast<int>((K / 32 + kQ8mChunk - 1) / kQ8mChunk);
+    if (kQ8mSmem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
+    // the matrix as 16-bit elements: rows of K / 32 * 17, boxes of 8 blocks x the tile's rows
+    CUtensorMap tm;
+    if ((st = make_tensor_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, static_cast<uint64_t>(p.rowbytes / 2),
+                                 static_cast<uint64_t>(N), static_cast<uint64_t>(p.rowbytes), kQ8mBoxPitch / 2,
+                                 kQ8mRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != GEM_OK)
+        return st;
+    const void* fn = reinterpret_cast<const void*>(q8_0_gemv_mma_kernel);
+    if ((st = ensure_smem_q8(fn, di.device, kQ8mSmem)) != GEM_OK) return st;
+    const int64_t ntiles = (N + kQ8mRows - 1) / kQ8mRows;
     const int grid = static_cast<int>(std::min<int64_t>(ntiles, di.num_sms));
-    void* args[] = {&p};
-    return launch_pdl(fn, dim3(grid), dim3((nw + 1) * 32), smem, static_cast<cudaStream_t>(stream), args);
+    void* args[] = {&tm, &p};
+    return launch_pdl(fn, dim3(grid), dim3((kQ8mWarps + 1) * 32), kQ8mSmem, static_cast<cudaStream_t>(stream), args);
 }
 
 size_t gem_argmax_workspace(int B, int64_t N) {

@@ -27,8 +27,10 @@ def env():
 
 
 Q8_CASES = [
-    # (N, K, B): ragged tiles, one chunk, a chunk plus a tail chunk, several chunks
+    # (N, K, B): ragged tiles, one chunk, a chunk plus a tail chunk, several chunks; one row
+    # takes the CUDA-core kernel, two to eight rows the tensor-core one (32-row tiles)
     (37, 256, 1), (37, 256, 8), (16, 1024, 2), (100, 1280, 3), (5000, 2048, 5), (333, 5376, 8),
+    (31, 256, 4), (1025, 5376, 6), (96, 2560, 7), (3000, 768, 2),
 ]
 
 
@@ -41,6 +43,30 @@ def test_q8_0_gemv_matches_oracle(env, N, K, B):
     g.q8_0_gemv(_cu(t, W), N, K, _cu(t, x), y)
     t.cuda.synchronize()
     assert_close(y.cpu().numpy(), oracle.q8_0_gemv(W, N, K, x), "q8_0 gemv N=%d K=%d B=%d" % (N, K, B))
+    assert g.device_status() == 0
+
+
+def test_q8_0_gemv_rows_of_any_scale(env):
+    """Each activation row is scaled by its own power of two before the binary16 split, so
+    rows far outside the binary16 range (and a zero row) give the unscaled result times the
+    same power of two, whatever the other rows of the call hold."""
+    g, t = env
+    N, K = 300, 2304
+    W = gem_synth.q8_0_matrix(22, N, N, K)
+    x = gem_synth.normal_f32(22, 5, (4, K))
+    shifts = [-60, 0, 40, None]   # None: the row is zero
+    xs = np.stack([x[i] * np.float32(2.0 ** s) if s is not None else np.zeros(K, np.float32)
+                   for i, s in enumerate(shifts)]).astype(np.float32)
+    y = t.full((4, N), float("nan"), device="cuda")
+    g.q8_0_gemv(_cu(t, W), N, K, _cu(t, xs), y)
+    t.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    ref = oracle.q8_0_gemv(W, N, K, x)
+    for i, s in enumerate(shifts):
+        if s is None:
+            assert np.all(got[i] == 0.0), "zero row"
+        else:
+            assert_close(got[i] * 2.0 ** -s, ref[i], "row scaled by 2^%d" % s)
     assert g.device_status() == 0
 
 

@@ -285,10 +285,10 @@ GEM_API gem_status gem_rmsnorm_qknorm_rope(float *qkv, int64_t ldqkv, int B, int
  *   out     [B][ldo] fp32.
  *   d       64, 128, 256 or 512.  n_q % n_kv == 0 and n_q / n_kv <= 8.
  *   workspace  device scratch of gem_gqa_decode_attn_workspace() bytes (same B, n_q, n_kv,
- *           d, cache_cap, window), 256-byte aligned; contents need no initialisation (for
- *           head_dim <= 256 and n_q / n_kv <= 4 the call first clears the splits' arrival
- *           counters in it, a 4 * B * n_kv byte memset on the stream).  The query returns 0
- *           (workspace may be NULL) where one split covers the range.
+ *           d, cache_cap, window), 256-byte aligned; contents need no initialisation (the
+ *           call writes the split partials there and a second launch on the same stream
+ *           combines them).  The query returns 0 (workspace may be NULL) where one split
+ *           covers the range.
  *   Results are deterministic: the split count depends only on (p, shape, device), and
  *   partial states are merged in ascending split order (by whichever split finishes last).
  */

@@ -354,10 +354,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_split_kernel(const __grid
 // in registers (head t lives in lane quad position t), P^T through a 384-byte per-warp
 // buffer, and O^T += V^T P^T on mma (head t's hi and lo columns land in the same thread and
 // are summed at the end).  The W warps' states are merged once per CTA (ascending warp
-// order).  A split then writes its (max, denominator, unnormalised output) to the workspace
-// and takes a ticket from its (sequence, KV head) arrival counter; the CTA that takes the
-// last ticket combines every split in ascending split order (so the result does not depend
-// on which CTA arrives last), writes the output and sets the counter back to zero.
+// order).  A split then writes its (max, denominator, unnormalised output) to the workspace.
+// Inside the layer chain it takes a ticket from its (sequence, KV head) arrival counter; the
+// CTA that takes the last ticket combines every split in ascending split order (so the result
+// does not depend on which CTA arrives last), writes the output and sets the counter back to
+// zero.  A stand-alone call has no cleared counters: the ordered merge kernel combines the
+// splits in a second launch.
 constexpr int kFlashTile = 16;
 constexpr int kFlashStages = 2;
 constexpr int kPbufPitch = 24;        // halves per P^T row (16 used; padding avoids bank conflicts)
@@ -678,7 +680,7 @@ __global__ void __launch_bounds__(W * 32, 1) gqa_flash_kernel(const __grid_const
             }
         }
     }
-    if (nsplit == 1) return;
+    if (nsplit == 1 || !P.cnt) return;   // no counters: a stand-alone call's merge kernel combines the splits
 
     // ---- the last split of this (sequence, KV head) to arrive combines all of them ----------
     // The barrier orders every thread's partial-state writes before thread 0's ticket, whose
@@ -1268,7 +1270,7 @@ gem_status ensure_smem_attn(const void* fn, int device, size_t bytes) {
 }
 
 // chain: launched right after the library's QKV projection, which clears the flash arrival
-// counters; otherwise (stand-alone calls) they are cleared here, on the stream, first.
+// counters; otherwise (stand-alone calls) the split partials go to the merge kernel.
 gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool fuse, bool chain) {
     gem_status st = attn_check(op);
     if (st != GEM_OK || op.B == 0 || op.n_q == 0) return st;
@@ -1305,7 +1307,10 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
     P.pa_off = pl.pa_off;
     P.st_off = pl.st_off;
     P.status = op.status ? op.status : di.status_word;
-    P.cnt = pl.flash && pl.nsplit_max > 1
+    // Inside the layer chain the last-arriving split merges (the QKV projection clears the
+    // counters); a stand-alone call leaves its split partials to the ordered merge kernel, so it
+    // needs no cleared counters and no memset between launches.
+    P.cnt = pl.flash && pl.nsplit_max > 1 && chain
                 ? reinterpret_cast<unsigned*>(static_cast<char*>(op.workspace) + pl.cnt_off)
                 : nullptr;
     RopeFreq fr{};
@@ -1338,13 +1343,11 @@ gem_status attn_launch(const AttnOp& op, cudaStream_t stream, bool early, bool f
         return st;
     const void* fn = pick(op.d, pl.flash, pl.W);
     if ((st = ensure_smem_attn(fn, di.device, pl.smem)) != GEM_OK) return st;
-    if (P.cnt && !chain)
-        GEM_CUDA_TRY(cudaMemsetAsync(P.cnt, 0, static_cast<size_t>(op.B) * op.n_kv * sizeof(unsigned), stream));
     dim3 grid(pl.nsplit_max, op.n_kv, op.B);
     void* args[] = {&tmK, &tmV, &P, &fr};   // the split kernel takes the first three
     if ((st = launch_pdl(fn, grid, dim3(pl.flash ? pl.W * 32 : kAttnThreads), pl.smem, stream, args)) != GEM_OK)
         return st;
-    if (!pl.flash && pl.nsplit_max > 1) {
+    if (pl.nsplit_max > 1 && !P.cnt) {
         int D = op.d;
         void* margs[] = {&P, &D};
         st = launch_pdl(reinterpret_cast<const void*>(gqa_merge_kernel), dim3(op.B * op.n_q), dim3(kMergeThreads), 0,

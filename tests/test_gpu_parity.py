@@ -353,7 +353,7 @@ def test_attention_deterministic_repeat_flash(gem, torch_mod):
     vc = _half_cache(t, gem_synth.normal_f16_bits(11, 3, (1, n_kv, cap, d)))
     pos = _cu(t, np.array([cap - 1], np.int32))
     need = gem.gqa_decode_attn_workspace(1, n_q, n_kv, d, cap, 0)
-    # the workspace starts as garbage: the call clears the split arrival counters itself
+    # the workspace starts as garbage: a stand-alone call writes every split partial it reads
     ws = t.full((max(need, 1),), 0xFF, dtype=t.uint8, device="cuda")
     outs = [t.empty((1, n_q * d), device="cuda") for _ in range(10)]
     for o in outs:   # which split merges varies from call to call; the result must not

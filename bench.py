@@ -264,9 +264,14 @@ class Model:
             fused = s.d <= 256 and s.n_q // s.n_kv <= 4 and not s.compact_kv
             n += (5 if fused else 6) + (2 if s.post_norms else 0)
             if self.B >= 2:
-                n += 4   # one activation prep launch per GEMV
+                # an activation prep launch for each 2..8-row GEMV above 64M weights (the
+                # records kernel); smaller ones build their operands in one launch
+                mats = ((s.n_qkv, s.H, 1), (s.H, s.n_q * s.d, 1), (s.F, s.H, 2), (s.H, s.F, 1))
+                n += sum(1 for N, K, m in mats if m * N * K > (64 << 20))
             if s.compact_kv:
                 split = self.gem.gqa_decode_attn_compact_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.rope_dim) > 0
+            elif fused:
+                split = False   # the last-arriving split merges inside the attention kernel
             else:
                 split = self.gem.gqa_decode_attn_workspace(self.B, s.n_q, s.n_kv, s.d, cap, s.window) > 0
             n += 1 if split else 0

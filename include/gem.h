@@ -16,8 +16,9 @@
  *     allocates device memory in a call (gem_step_plan_create, a set-up call, is the one
  *     exception); calls that need scratch take a caller-provided workspace whose size is
  *     returned by the matching *_workspace() query.  Two calls keep their scratch in arrays
- *     of the library instead, one per device: gem_q4_0_gemv with B >= 2 (its operand records,
- *     4 MiB) and gem_gqa_decode_attn_noalloc (its split partials, 8 MiB).  Calls of the same
+ *     of the library instead, one per device: gem_q4_0_gemv with B >= 2 on matrices of more
+ *     than 64M weights (its operand records, 4 MiB) and gem_gqa_decode_attn_noalloc (its split
+ *     partials, 8 MiB).  Calls of the same
  *     one of these two that can run at the same time on one device (different streams) race
  *     on its array; calls issued in order on one stream are safe.  gem_q4_0_gemv_ws and
  *     gem_gqa_decode_attn take a caller workspace and share nothing.
@@ -124,10 +125,12 @@ GEM_API gem_status gem_set_test_injection(int mask);
  *   Accumulation is fp32 (on tensor cores where K % 256 == 0 and the inputs are aligned: exact
  *   weights times each activation as a binary16 hi + lo pair of about 22 significant bits,
  *   under power-of-two scales that are undone exactly).  y must not overlap W or x.
- *   For B >= 2 the call converts x into tensor-core operand records first (a second launch on the
+ *   For B >= 2 and more than 64M weights (N x K, both matrices in pair mode) on the tensor-core
+ *   path the call converts x into tensor-core operand records first (a second launch on the
  *   same stream), kept in a library-owned array of 4 MiB per device (K <= 130816): calls on two
- *   streams of one device that may run at the same time must not both have B >= 2.  Use
- *   gem_q4_0_gemv_ws to give each call its own records instead.
+ *   streams of one device that may run at the same time must not both be such calls.  Use
+ *   gem_q4_0_gemv_ws to give each call its own records instead.  Smaller 2..8-row calls build
+ *   their operands inside one launch and use no records.
  */
 GEM_API gem_status gem_q4_0_gemv(const void *W, int64_t N, int64_t K, const float *x, int64_t ldx,
                          int B, float *y, int64_t ldy, const float *residual, void *stream);

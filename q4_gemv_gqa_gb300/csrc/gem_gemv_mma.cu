@@ -33,6 +33,11 @@ gem_status ensure_smem_mma(const void* fn, int device, size_t bytes) {
 // Plan and launch; the caller has checked the op and that the fast-path conditions hold
 // (K % 256 == 0, 16-byte aligned matrices and activation rows).
 gem_status gemv_enqueue_mma(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di) {
+    // 2..8 rows: the one-launch tall-tile kernel up to 64M weights per call (the matrices of a
+    // 4B-class layer, where the records kernel's extra launch costs more than it saves); larger
+    // matrices stream faster through the records kernel's deeper per-SM pipeline.
+    const int64_t weights = (op.W1 ? 2 : 1) * op.N * op.K;
+    if (op.B >= 2 && op.B <= 8 && weights <= (int64_t(64) << 20)) return gemv_enqueue_wide(op, stream, di);
     {
         bool planned = false;
         const gem_status st1 = op.B == 1 ? gemv_enqueue_b1(op, stream, di, &planned)

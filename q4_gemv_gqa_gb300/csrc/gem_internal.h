@@ -80,6 +80,8 @@ constexpr size_t kGemvRecScratchBytes = size_t(4) << 20;
 constexpr int kMaxGemmRows = 32;   // the batched prefill GEMM's activation rows
 size_t gemv_rec_bytes(int B, int64_t K);
 gem_status gemv_enqueue_bn(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, bool* planned);
+// 2..8 rows in one launch: tall TMA tiles, activation operands built in the kernel (no records).
+gem_status gemv_enqueue_wide(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di);
 
 // ---- norms / RoPE / activation -------------------------------------------------------------
 struct RopeOp {

@@ -6,9 +6,10 @@
 //
 // Schedule.  A tile is 16 MT rows of each of the NMAT matrices; the CTAs take tiles round robin.
 // A stage is a tile's rows x 16 blocks (two 144-byte groups), one 2-D TMA box per matrix and
-// group, so a copy moves 16 MT rows at once.  Consumer warp w (of 8) takes blocks w and w + 8 of
-// the stage for all the tile's m16 tiles: the activation operand it builds for a block serves
-// NMAT x MT x 4 mma, and the activation rows are read once per tile.
+// group, so a copy moves 16 MT rows at once, plus the 16 blocks' activations of the B rows (two
+// more boxes, copied once the previous kernel is complete).  Consumer warp w (of 16) takes
+// block w of the stage for all the tile's m16 tiles: the activation operand it builds for the
+// block serves NMAT x MT x 4 mma.
 //
 // Fragments.  Lane quad t of a block owns code bytes 4t .. 4t + 3 of a row: their low nibbles
 // (elements 4t .. 4t + 3) form k16 tile 0, their high nibbles (elements 16 + 4t ..) k16 tile 1.
@@ -38,7 +39,7 @@ constexpr int kBlk = 18;                   // Q4_0 block bytes
 constexpr int kGroup = 8 * kBlk;           // 144: one box row (8 blocks)
 constexpr int kStageBlocks = 16;           // blocks per stage row (two boxes per matrix)
 constexpr int kMaxStages = 16;
-constexpr size_t kRingBudget = 147456;     // bytes of stages in flight per CTA
+constexpr int kXCols = 256;                // activations per TMA box row (8 blocks)
 
 struct Params {
     int64_t N;
@@ -46,6 +47,8 @@ struct Params {
     int nblk;                  // K / 32
     int nchunk;                // stages per tile
     int ns;                    // ring stages
+    uint32_t stage;            // bytes of a stage: the weight boxes, then two activation boxes
+    uint32_t xbox;             // bytes of an activation box: B rows x 256 fp32
     int B;
     const float* x;
     int64_t ldx;
@@ -65,11 +68,18 @@ template <int NMAT, int MT>
 struct Shape {
     static constexpr int kRows = 16 * MT;
     static constexpr uint32_t kBox = static_cast<uint32_t>(kRows) * kGroup;        // one box
-    static constexpr uint32_t kStage = NMAT * 2 * kBox;
+    static constexpr uint32_t kWts = NMAT * 2 * kBox;                             // weight boxes of a stage
     static constexpr int kOut = NMAT * MT * 4;                                    // accumulators per lane
     static constexpr uint32_t kRed = kWarps * kOut * 32;                          // floats per buffer
-    static constexpr size_t smem(int ns) { return static_cast<size_t>(ns) * kStage + 2 * kMaxStages * 8 + 2 * kRed * 4 + kWarps * 8 * 4; }
+    // fixed part: barriers, the two reduction buffers and the sums of squares
+    static constexpr size_t kFixed = 2 * kMaxStages * 8 + 2 * kRed * 4 + kWarps * 8 * 4;
 };
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 
 __device__ __forceinline__ void mma_zero(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -93,11 +103,12 @@ __device__ __forceinline__ void split_pairs(float4 v, uint32_t& h0, uint32_t& h1
 template <int NMAT, int MT>
 __global__ void __launch_bounds__((kWarps + 1) * 32, 1) q4_0_gemv_wide_kernel(const __grid_constant__ CUtensorMap tm0,
                                                                               const __grid_constant__ CUtensorMap tm1,
+                                                                              const __grid_constant__ CUtensorMap tmx,
                                                                               const Params p) {
     using S = Shape<NMAT, MT>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int ns = p.ns;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(ns) * S::kStage);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(ns) * p.stage);
     uint64_t* empty = full + kMaxStages;
     float* red = reinterpret_cast<float*>(full + 2 * kMaxStages);
     float* ssw = red + 2 * S::kRed;   // [warp][row]: partial sums of squares of the activation rows
@@ -113,32 +124,60 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) q4_0_gemv_wide_kernel(co
         fence_mbar_init();
         prefetch_tensormap(&tm0);
         if (NMAT == 2) prefetch_tensormap(&tm1);
+        prefetch_tensormap(&tmx);
     }
     __syncthreads();
 
-    if (warp == kWarps) {   // producer: (tile, chunk) stages in order; weights only, before any wait
+    // producer: (tile, chunk) stages in order.  A stage is the tile's weight boxes and the
+    // chunk's activation boxes (B rows x 256 values each).  The
+    // weights of the first ring's worth of stages are requested before griddepcontrol.wait
+    // (nothing running writes them); activations, which the previous kernel writes, only after.
+    if (warp == kWarps) {
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
             bool ok = true;
             int s = 0, slot = 0;
             uint32_t par = 1;
+            const uint64_t keep = l2_policy_evict_last();   // the activations are read by every tile
+            auto issue_x = [&](int sl, int c) {
+                const int nbox = min(kStageBlocks, p.nblk - c * kStageBlocks) / 8;
+                uint8_t* dst = smem + static_cast<size_t>(sl) * p.stage + S::kWts;
+                for (int q = 0; q < nbox; ++q)
+                    tma_load_2d(dst + q * p.xbox, &tmx, c * kStageBlocks * 32 + q * kXCols, 0, &full[sl], keep);
+            };
+            int pend[kMaxStages];   // chunk of each stage issued before the wait
+            bool waited = false;
             for (int64_t tl = blockIdx.x; tl < ntiles && ok; tl += gridDim.x) {
                 const int32_t r0 = static_cast<int32_t>(tl * S::kRows);
                 for (int c = 0; c < p.nchunk; ++c) {
                     if (s >= ns && !(ok = mbar_wait(&empty[slot], par, p.status))) break;
                     const int nbox = min(kStageBlocks, p.nblk - c * kStageBlocks) / 8;   // 1 or 2 (K % 256 == 0)
-                    uint8_t* dst = smem + static_cast<size_t>(slot) * S::kStage;
-                    mbar_arrive_expect_tx(&full[slot], S::kBox * static_cast<uint32_t>(NMAT * nbox));
+                    uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage;
+                    mbar_arrive_expect_tx(&full[slot], (S::kBox * NMAT + p.xbox) * static_cast<uint32_t>(nbox));
                     for (int m = 0; m < NMAT; ++m)
                         for (int q = 0; q < nbox; ++q)   // x: whole groups of 144 bytes
                             tma_load_2d(dst + (m * 2 + q) * S::kBox, m ? &tm1 : &tm0, (c * 2 + q) * kGroup, r0,
                                         &full[slot], policy);
+                    if (waited) {
+                        issue_x(slot, c);
+                    } else {
+                        pend[slot] = c;
+                        if (s + 1 == ns) {   // the ring is full: wait, then the pending activations
+                            pdl_wait();
+                            waited = true;
+                            for (int i = 0; i < ns; ++i) issue_x(i, pend[i]);
+                        }
+                    }
                     ++s;
                     if (++slot == ns) {
                         slot = 0;
                         par ^= 1u;
                     }
                 }
+            }
+            if (!waited) {   // fewer stages than ring slots (or a wait gave up)
+                pdl_wait();
+                for (int i = 0; i < min(s, ns); ++i) issue_x(i, pend[i]);
             }
             if (!ok) drain_stages(full, ns, max(0, s - ns), s - 1);
         }
@@ -149,22 +188,12 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) q4_0_gemv_wide_kernel(co
     clear_words(p.clear, p.nclear, tid, kWarps * 32);
     const int B = p.B;
     const int g = lane >> 2, t = lane & 3;
-    const bool xrow = g < B;                 // B column g is a real activation row
-    const float* xg = p.x + (xrow ? g : 0) * p.ldx + 4 * t;
     const float* gg = p.gamma ? p.gamma + 4 * t : nullptr;
     float ss = 0.f;                          // this lane's share of row g's sum of squares
-    // this warp's block of chunk c: the activations of row g and gamma (lanes of absent rows
-    // and blocks past K get zeros and ones)
-    auto load_x = [&](int c, float4 (&xv)[2], float4 (&gv)[2]) {
-        const int nb = min(kStageBlocks, p.nblk - c * kStageBlocks);
-        const int e0 = (c * kStageBlocks + warp) * 32;
-        const bool in = xrow && warp < nb;
-        xv[0] = in ? __ldg(reinterpret_cast<const float4*>(xg + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        xv[1] = in ? __ldg(reinterpret_cast<const float4*>(xg + e0 + 16)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const bool gin = gg && warp < nb;
-        gv[0] = gin ? __ldg(reinterpret_cast<const float4*>(gg + e0)) : make_float4(1.f, 1.f, 1.f, 1.f);
-        gv[1] = gin ? __ldg(reinterpret_cast<const float4*>(gg + e0 + 16)) : make_float4(1.f, 1.f, 1.f, 1.f);
-    };
+    // this warp's block of the stage in the stage's activation boxes: row g, columns
+    // (warp % 8) * 32 + 4t (+ 16) of box warp / 8 (lanes of rows past B read nothing)
+    const bool xrow = g < B;
+    const uint32_t xoff = S::kWts + (warp / 8) * p.xbox + ((xrow ? g : 0) * kXCols + (warp % 8) * 32 + 4 * t) * 4;
     bool ok = true;
     int s = 0, slot = 0;
     uint32_t par = 0;
@@ -176,16 +205,25 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) q4_0_gemv_wide_kernel(co
         for (int u = 0; u < NMAT * MT; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
         for (int c = 0; c < p.nchunk; ++c) {
             const int nb = min(kStageBlocks, p.nblk - c * kStageBlocks);   // 8 or 16
-            // this warp's activations for the stage, requested before the stage wait
-            float4 xv[2], gv[2];
-            load_x(c, xv, gv);
+            // gamma of this warp's block (a weight: requested before the stage wait)
+            float4 gv[2];
+            {
+                const int e0 = (c * kStageBlocks + warp) * 32;
+                const bool gin = gg && warp < nb;
+                gv[0] = gin ? __ldg(reinterpret_cast<const float4*>(gg + e0)) : make_float4(1.f, 1.f, 1.f, 1.f);
+                gv[1] = gin ? __ldg(reinterpret_cast<const float4*>(gg + e0 + 16)) : make_float4(1.f, 1.f, 1.f, 1.f);
+            }
             if (ok) ok = mbar_wait(&full[slot], par, p.status);
             if (ok) {
-                const uint8_t* st = smem + static_cast<size_t>(slot) * S::kStage;
+                const uint8_t* st = smem + static_cast<size_t>(slot) * p.stage;
                 {
                     const int blk = warp;
                     if (blk < nb) {
-                        float4 v0 = xv[0], v1 = xv[1];
+                        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+                        if (xrow) {
+                            v0 = *reinterpret_cast<const float4*>(st + xoff);
+                            v1 = *reinterpret_cast<const float4*>(st + xoff + 64);
+                        }
                         if (it == 0)
                             ss += v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w + v1.x * v1.x +
                                   v1.y * v1.y + v1.z * v1.z + v1.w * v1.w;
@@ -320,9 +358,12 @@ gem_status ensure_smem_wide(const void* fn, int device, size_t bytes) {
 template <int NMAT, int MT>
 gem_status launch(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, Params& p) {
     using S = Shape<NMAT, MT>;
-    p.ns = static_cast<int>(std::min<size_t>(kMaxStages, kRingBudget / S::kStage));
-    const size_t smem = S::smem(p.ns);
-    if (smem > di.smem_optin) return GEM_ERR_UNSUPPORTED_SHAPE;
+    p.xbox = static_cast<uint32_t>(op.B) * kXCols * 4;
+    p.stage = static_cast<uint32_t>(align_up(S::kWts + 2 * p.xbox, 128));
+    // as many stages as shared memory holds next to the fixed part, at most kMaxStages
+    if (di.smem_optin < S::kFixed + 2 * p.stage) return GEM_ERR_UNSUPPORTED_SHAPE;
+    p.ns = static_cast<int>(std::min<size_t>(kMaxStages, (di.smem_optin - S::kFixed) / p.stage));
+    const size_t smem = static_cast<size_t>(p.ns) * p.stage + S::kFixed;
     const uint64_t rowbytes = static_cast<uint64_t>(op.K / 32) * kBlk;
     CUtensorMap tm0, tm1;
     gem_status st;
@@ -336,11 +377,17 @@ gem_status launch(const GemvOp& op, cudaStream_t stream, const DeviceInfo& di, P
     } else {
         tm1 = tm0;
     }
+    // the activation rows: K x B fp32 (row stride ldx), boxes of 256 values x B rows
+    CUtensorMap tmx;
+    if ((st = make_tensor_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, op.x, static_cast<uint64_t>(op.K),
+                                 static_cast<uint64_t>(op.B), static_cast<uint64_t>(op.ldx) * 4, kXCols,
+                                 static_cast<uint32_t>(op.B), CU_TENSOR_MAP_SWIZZLE_NONE)) != GEM_OK)
+        return st;
     const void* fn = kernel_ptr<NMAT, MT>();
     if ((st = ensure_smem_wide(fn, di.device, smem)) != GEM_OK) return st;
     const int64_t ntiles = (op.N + S::kRows - 1) / S::kRows;
     const int grid = static_cast<int>(std::min<int64_t>(ntiles, di.num_sms));
-    void* args[] = {&tm0, &tm1, &p};
+    void* args[] = {&tm0, &tm1, &tmx, &p};
     return launch_pdl(fn, dim3(grid), dim3((kWarps + 1) * 32), smem, stream, args);
 }
 

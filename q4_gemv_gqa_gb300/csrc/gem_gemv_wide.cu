@@ -129,9 +129,9 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) q4_0_gemv_wide_kernel(co
     __syncthreads();
 
     // producer: (tile, chunk) stages in order.  A stage is the tile's weight boxes and the
-    // chunk's activation boxes (B rows x 256 values each).  The
-    // weights of the first ring's worth of stages are requested before griddepcontrol.wait
-    // (nothing running writes them); activations, which the previous kernel writes, only after.
+    // chunk's activation boxes (B rows x 256 values each).  The weights of the first ring's worth
+    // of stages are requested before griddepcontrol.wait (nothing running writes them); the
+    // activations, which the previous kernel writes, only after it.
     if (warp == kWarps) {
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1) q4_0_gemv_wide_kernel(co
                     uint8_t* dst = smem + static_cast<size_t>(slot) * p.stage;
                     mbar_arrive_expect_tx(&full[slot], (S::kBox * NMAT + p.xbox) * static_cast<uint32_t>(nbox));
                     for (int m = 0; m < NMAT; ++m)
-                        for (int q = 0; q < nbox; ++q)   // x: whole groups of 144 bytes
+                        for (int q = 0; q < nbox; ++q)   // column coordinate: whole 144-byte groups
                             tma_load_2d(dst + (m * 2 + q) * S::kBox, m ? &tm1 : &tm0, (c * 2 + q) * kGroup, r0,
                                         &full[slot], policy);
                     if (waited) {

@@ -85,7 +85,9 @@ GEMV_CASES = [
     (40, 65536, 1),                     # one row, operand records beyond shared memory: fallback kernel
     (5376, 21504, 1), (2600, 16384, 1), # one row, K split over CTA pairs (uneven units per CTA)
     (2600, 32768, 1),                   # the same, each CTA's half of the row read twice
-    (24, 131328, 2),                    # two rows, records beyond the library array: fallback kernel
+    (24, 131328, 2),                    # two rows, very long K: the one-launch kernel, 257 stages per tile
+    (520, 131328, 2),                   # two rows above 64M weights, records beyond the library array:
+                                        # fallback kernel
 ]
 
 
